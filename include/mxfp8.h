@@ -1,0 +1,178 @@
+/*
+ * mxfp8.h -- C ABI of the GB300 (sm_103a) MXFP8 block-scaled linear layer.
+ *
+ * The layer, as vLLM PR #52204 "[Kernel] Add FlashInfer TRTLLM MXFP8 linear
+ * backend" states it (Purpose; review thread on apply_weights):
+ *   load time : quantize the weight [N, K] to MXFP8 (FP8 E4M3 elements, one
+ *               E8M0 power-of-two scale per 32 consecutive K elements),
+ *               require K % 256 == 0, pad N to a multiple of 128 (data and
+ *               scales), lay data and scales out for the GEMM, remember N;
+ *   per call  : quantize the BF16 activations [M, K] on the fly with the 8x4
+ *               scale layout, run the block-scaled GEMM with FP32
+ *               accumulation, slice the padded N back to N, add the bias and
+ *               write BF16 [M, N].  Only N is padded, never the input.
+ * The grouped entry point runs the same product over per-expert row segments
+ * of expert-sorted activations (the MoE gate_up GEMM of SGLang PR #18945 "Add
+ * support for FlashInfer mxfp8" and FlashInfer PR #4026).
+ *
+ * Conventions shared by every call:
+ *  - All pointers named x, q, sf, bias, y, workspace, expert_offsets are
+ *    DEVICE pointers on the current CUDA device; `stream` is a cudaStream_t
+ *    (NULL = legacy default stream).  Every call that takes a stream is
+ *    asynchronous on it, never synchronises and never allocates, frees or
+ *    touches memory other than its arguments.  The caller owns all memory and
+ *    must keep it alive until the stream work completes.
+ *  - Arguments are checked on the host before any launch; a failed check
+ *    returns its status and launches nothing.  A launch failure returns
+ *    MXFP8_ERR_CUDA and mxfp8_last_cuda_error() gives the cudaError_t.
+ *  - M = 0 (or rows = 0) returns MXFP8_OK without launching.
+ *  - Results are deterministic: the same inputs give the same bytes.
+ *  - Every call can be captured in a CUDA graph (no host synchronisation,
+ *    no allocation); the kernel parameters capture the pointers.
+ *  - The library runs on compute capability 10.3 (GB300) only; any other
+ *    device gets MXFP8_ERR_UNSUPPORTED_DEVICE.
+ *
+ * Formats (the byte orders are readings of this library; the pages give only
+ * the 8x4 buffer size):
+ *  - E4M3: torch.float8_e4m3fn bytes.  E8M0: one byte, value 2^(b-127),
+ *    0xFF is NaN.
+ *  - Scale rule: byte = clamp(floor(log2(amax)) - 8 + 127, 0, 254) with amax
+ *    the largest magnitude of the 32-block (OCP MX v1.0 rule for MXFP8).
+ *    An all-zero block gets byte 0x00; a block holding NaN/Inf gets byte
+ *    0xFF and elements 0x7F.  Elements are v / 2^(byte-127) rounded to
+ *    nearest-even E4M3, saturating to +-448, signed zeros kept.
+ *  - 8x4 activation scale layout (KB = K/32): the scale of row m, block b is
+ *    at byte ((m/8)*(KB/4) + b/4)*32 + (m%8)*4 + (b%4); the buffer holds
+ *    ceil(M/8)*8 * KB bytes (the size printed in the prhub summary of vLLM PR
+ *    #52204, key source snippets); rows M..ceil8(M)-1 hold 0x00.
+ *  - Prepared weight: data [N_pad][K] row-major E4M3 (rows N..N_pad-1 are
+ *    0x00); scales in tiles of 128 rows x 4 blocks (512 bytes): tile
+ *    (t = n/128, q = b/4) starts at byte (t*(KB/4) + q)*512 and row r = n%128,
+ *    block b sits at (r%32)*16 + (r/32)*4 + (b%4) inside it; padding rows are
+ *    0x00.  Experts are stacked: expert e's data starts at e*N_pad*K and its
+ *    scales at e*N_pad*KB.
+ */
+#ifndef MXFP8_GB300_H
+#define MXFP8_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum mxfp8_status {
+    MXFP8_OK = 0,
+    MXFP8_ERR_INVALID_ARG = 1,           /* null pointer, negative or too large size, bad struct */
+    MXFP8_ERR_K_NOT_MULTIPLE_OF_256 = 2, /* K % 256 != 0 (load-time check of the pages) */
+    MXFP8_ERR_MISALIGNED = 3,            /* a device pointer is not 16-byte aligned */
+    MXFP8_ERR_UNSUPPORTED_DEVICE = 4,    /* current device is not compute capability 10.3 */
+    MXFP8_ERR_WORKSPACE_TOO_SMALL = 5,   /* workspace_bytes below the size helper's value */
+    MXFP8_ERR_DEVICE_TIMEOUT = 6,        /* a kernel gave up waiting (see mxfp8_device_error) */
+    MXFP8_ERR_CUDA = 7                   /* a CUDA call failed: mxfp8_last_cuda_error() */
+} mxfp8_status;
+
+typedef enum mxfp8_in_dtype {
+    MXFP8_IN_F32 = 0,  /* float32 weights (e.g. a checkpoint in FP32) */
+    MXFP8_IN_BF16 = 1  /* bfloat16 weights */
+} mxfp8_in_dtype;
+
+/* A prepared MXFP8 weight: a VIEW of caller-owned device buffers.
+ * Fill it with mxfp8_weight_view(); n_pad is derived, not chosen. */
+typedef struct mxfp8_weight {
+    int64_t num_experts; /* 1 for a dense layer */
+    int64_t n;           /* logical output features per expert */
+    int64_t n_pad;       /* ceil(n / 128) * 128 */
+    int64_t k;           /* input features, a multiple of 256 */
+    void* q;             /* [num_experts][n_pad][k] E4M3 bytes, 16-B aligned */
+    void* sf;            /* [num_experts][n_pad * k / 32] E8M0 bytes, tiled, 16-B aligned */
+} mxfp8_weight;
+
+/* ------------------------------------------------------------ size helpers
+ * Pure functions of the shape; return 0 for invalid shapes. */
+
+/* Bytes of the 8x4 activation scale buffer: ceil(m/8)*8 * k/32. */
+size_t mxfp8_act_scale_bytes(int64_t m, int64_t k);
+/* Bytes of one expert's prepared data: ceil(n/128)*128 * k. */
+size_t mxfp8_weight_bytes(int64_t n, int64_t k);
+/* Bytes of one expert's prepared scales: ceil(n/128)*128 * k/32. */
+size_t mxfp8_weight_scale_bytes(int64_t n, int64_t k);
+/* Workspace of mxfp8_linear / mxfp8_grouped_linear for m activation rows:
+ * the quantized activations (m*k bytes, rounded up to 256) followed by their
+ * 8x4 scales. */
+size_t mxfp8_linear_workspace_bytes(int64_t m, int64_t k);
+
+/* Fill *w as a view of (q, sf) for num_experts x [n, k]; checks the shape
+ * (k % 256 == 0, sizes > 0) and the 16-byte alignment of q and sf. */
+mxfp8_status mxfp8_weight_view(mxfp8_weight* w, int64_t num_experts, int64_t n,
+                               int64_t k, void* q, void* sf);
+
+/* ------------------------------------------------------------- operations */
+
+/* Load-time weight preparation (vLLM PR #52204, process_weights_after_loading:
+ * quantize, pad N to 128, lay out data and scales, keep the logical N).
+ * src: device [num_experts][n][k] float32 or bfloat16, row-major, 16-B aligned.
+ * Writes every byte of w->q and w->sf (padding included). */
+mxfp8_status mxfp8_prepare_weight(const void* src, mxfp8_in_dtype dtype,
+                                  const mxfp8_weight* w, void* stream);
+
+/* Per-call activation quantizer with the 8x4 scale layout (vLLM PR #52204,
+ * flashinfer_mxfp8_quantize_8x4 custom op and its fake implementation).
+ * x: device bfloat16 [m][k] row-major, 16-B aligned; q: device [m][k] E4M3;
+ * sf: device mxfp8_act_scale_bytes(m, k) bytes, written in full (padding
+ * rows 0x00).  k % 256 == 0. */
+mxfp8_status mxfp8_quantize_act(const void* x, int64_t m, int64_t k, void* q,
+                                void* sf, void* stream);
+
+/* Block-scaled GEMM + slice + bias on already-quantized activations
+ * (the mm_mxfp8 call with use_8x4_sf_layout of vLLM PR #52204):
+ * y[i][j] = bf16( sum_k deq(qa)[i][k] * deq(W)[j][k] + bias[j] ), j < n.
+ * qa: [m][k] E4M3, sfa: 8x4 scales for (m, k); bias: bfloat16 [n] or NULL;
+ * y: bfloat16 [m][n] row-major (contiguous, logical n).  Dense weights only
+ * (w->num_experts == 1). */
+mxfp8_status mxfp8_gemm(const void* qa, const void* sfa, int64_t m,
+                        const mxfp8_weight* w, const void* bias, void* y,
+                        void* stream);
+
+/* The whole per-call layer (vLLM PR #52204, apply_weights): quantize x with
+ * the 8x4 layout into the workspace, then the block-scaled GEMM with the
+ * padded-N slice and the bias fused into its epilogue.
+ * x: bfloat16 [m][k]; bias: bfloat16 [n] or NULL; y: bfloat16 [m][n];
+ * workspace: device, >= mxfp8_linear_workspace_bytes(m, k), 256-B aligned
+ * preferred (16-B required); its contents are scratch. */
+mxfp8_status mxfp8_linear(const void* x, int64_t m, const mxfp8_weight* w,
+                          const void* bias, void* y, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
+/* Grouped (MoE expert) layer over expert-sorted rows: rows
+ * [off[e], off[e+1]) of x_sorted use expert e of w.  expert_offsets: device
+ * int32 [num_experts + 1], non-decreasing, off[0] = 0, off[E] = rows (empty
+ * experts allowed; the values are read on the device, not checked).
+ * bias: bfloat16 [num_experts][n] or NULL; y: bfloat16 [rows][n].
+ * The activations are quantized as one [rows, k] matrix.  num_experts <= 1024. */
+mxfp8_status mxfp8_grouped_linear(const void* x_sorted, int64_t rows,
+                                  const int32_t* expert_offsets,
+                                  const mxfp8_weight* w, const void* bias,
+                                  void* y, void* workspace,
+                                  size_t workspace_bytes, void* stream);
+
+/* --------------------------------------------------------- status helpers */
+
+const char* mxfp8_status_string(mxfp8_status status);
+/* cudaError_t of the last call that returned MXFP8_ERR_CUDA (per thread). */
+int mxfp8_last_cuda_error(void);
+/* Reads and clears the device-side error word that the GEMM kernels set when
+ * a wait gives up (a hang turned into an error).  SYNCHRONISES the current
+ * device.  Returns MXFP8_OK or MXFP8_ERR_DEVICE_TIMEOUT. */
+mxfp8_status mxfp8_device_error(void);
+
+/* Testing hook: pin the GEMM schedule.  tokens_per_tile in {0 (automatic),
+ * 16, 32, 64, 128, 256}; split_k in {0 (automatic), 1..8}.  Process-wide. */
+void mxfp8_set_schedule(int tokens_per_tile, int split_k);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXFP8_GB300_H */

@@ -1,0 +1,253 @@
+"""GB300 (sm_103a) MXFP8 block-scaled linear layer: Python binding.
+
+A thin ctypes layer over the C ABI of ``include/mxfp8.h`` (the shared library
+``_lib/libmxfp8_gb300.so``, built in-tree by ``_build.py``).  This module only
+marshals arguments -- shapes, device pointers and the current CUDA stream --
+and allocates outputs with PyTorch; every step of the layer runs in the
+library's CUDA kernels.  There is no fallback: if the library is missing or
+the device is not a GB300, calls raise.
+
+The layer (vLLM PR #52204 "[Kernel] Add FlashInfer TRTLLM MXFP8 linear
+backend"): weights are prepared once (MXFP8 quantization with one E8M0 scale
+per 32 K elements, N padded to 128, GEMM layout); each call quantizes the BF16
+activations with the 8x4 scale layout, runs the block-scaled GEMM with FP32
+accumulation, slices the padded N and adds the bias, writing BF16.
+"""
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "Mxfp8Error", "PreparedWeight", "prepare_weight", "quantize_act", "gemm",
+    "linear", "grouped_linear", "act_scale_bytes", "weight_bytes",
+    "weight_scale_bytes", "linear_workspace_bytes", "set_schedule",
+    "device_error", "library", "library_path",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_lib", "libmxfp8_gb300.so")
+
+OK = 0
+STATUS_NAMES = {
+    0: "MXFP8_OK", 1: "MXFP8_ERR_INVALID_ARG", 2: "MXFP8_ERR_K_NOT_MULTIPLE_OF_256",
+    3: "MXFP8_ERR_MISALIGNED", 4: "MXFP8_ERR_UNSUPPORTED_DEVICE",
+    5: "MXFP8_ERR_WORKSPACE_TOO_SMALL", 6: "MXFP8_ERR_DEVICE_TIMEOUT", 7: "MXFP8_ERR_CUDA",
+}
+IN_F32 = 0
+IN_BF16 = 1
+
+
+class Mxfp8Error(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        msg = "%s: %s (%s)" % (where, STATUS_NAMES.get(status, status),
+                               _lib_status_string(status))
+        if status == 7:
+            msg += ", cudaError %d" % library().mxfp8_last_cuda_error()
+        super().__init__(msg)
+
+
+class mxfp8_weight(ctypes.Structure):
+    """Mirror of ``struct mxfp8_weight`` in include/mxfp8.h."""
+    _fields_ = [("num_experts", ctypes.c_int64), ("n", ctypes.c_int64),
+                ("n_pad", ctypes.c_int64), ("k", ctypes.c_int64),
+                ("q", ctypes.c_void_p), ("sf", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def library():
+    """The loaded C library (ctypes.CDLL) with argument types declared."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(
+            "MXFP8 CUDA library not built: %s is missing (run "
+            "`python -c 'import __graft_entry__ as g; g.build()'` or "
+            "`python mxfp8_block_scaled_x4_gb300/_build.py`)" % _LIB_PATH)
+    lib = ctypes.CDLL(_LIB_PATH)
+    i64, vp, sz = ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t
+    W = ctypes.POINTER(mxfp8_weight)
+    sig = {
+        "mxfp8_act_scale_bytes": (sz, [i64, i64]),
+        "mxfp8_weight_bytes": (sz, [i64, i64]),
+        "mxfp8_weight_scale_bytes": (sz, [i64, i64]),
+        "mxfp8_linear_workspace_bytes": (sz, [i64, i64]),
+        "mxfp8_weight_view": (ctypes.c_int, [W, i64, i64, i64, vp, vp]),
+        "mxfp8_prepare_weight": (ctypes.c_int, [vp, ctypes.c_int, W, vp]),
+        "mxfp8_quantize_act": (ctypes.c_int, [vp, i64, i64, vp, vp, vp]),
+        "mxfp8_gemm": (ctypes.c_int, [vp, vp, i64, W, vp, vp, vp]),
+        "mxfp8_linear": (ctypes.c_int, [vp, i64, W, vp, vp, vp, sz, vp]),
+        "mxfp8_grouped_linear": (ctypes.c_int, [vp, i64, vp, W, vp, vp, vp, sz, vp]),
+        "mxfp8_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+        "mxfp8_last_cuda_error": (ctypes.c_int, []),
+        "mxfp8_device_error": (ctypes.c_int, []),
+        "mxfp8_set_schedule": (None, [ctypes.c_int, ctypes.c_int]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _lib_status_string(status):
+    try:
+        return library().mxfp8_status_string(int(status)).decode()
+    except Exception:  # noqa: BLE001 - message formatting only
+        return "?"
+
+
+def _check(status, where):
+    if status != OK:
+        raise Mxfp8Error(status, where)
+
+
+def _stream(t: torch.Tensor):
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(cond, msg):
+    if not cond:
+        raise ValueError(msg)
+
+
+# ----------------------------------------------------------------- sizes
+def act_scale_bytes(m: int, k: int) -> int:
+    return library().mxfp8_act_scale_bytes(m, k)
+
+
+def weight_bytes(n: int, k: int) -> int:
+    return library().mxfp8_weight_bytes(n, k)
+
+
+def weight_scale_bytes(n: int, k: int) -> int:
+    return library().mxfp8_weight_scale_bytes(n, k)
+
+
+def linear_workspace_bytes(m: int, k: int) -> int:
+    return library().mxfp8_linear_workspace_bytes(m, k)
+
+
+# ----------------------------------------------------------------- weights
+class PreparedWeight:
+    """A prepared MXFP8 weight: device buffers + the C struct viewing them.
+
+    q  : uint8 [num_experts, n_pad, k]    E4M3 data (rows >= n are zero)
+    sf : uint8 [num_experts, n_pad*k/32]  E8M0 scales, 128x4 tiles
+    n  : logical output features (the padded N is sliced away per call)."""
+
+    def __init__(self, q: torch.Tensor, sf: torch.Tensor, n: int):
+        e, n_pad, k = q.shape
+        self.q, self.sf, self.n, self.k, self.num_experts = q, sf, n, k, e
+        self.n_pad = n_pad
+        self.c = mxfp8_weight()
+        _check(library().mxfp8_weight_view(ctypes.byref(self.c), e, n, k, _ptr(q), _ptr(sf)),
+               "mxfp8_weight_view")
+
+    @property
+    def device(self):
+        return self.q.device
+
+
+def prepare_weight(w: torch.Tensor) -> PreparedWeight:
+    """Quantize + pad + lay out a weight [n, k] (or stacked experts
+    [e, n, k]) given as float32 or bfloat16 on the GPU."""
+    _need(w.is_cuda, "weight must be a CUDA tensor")
+    _need(w.dtype in (torch.float32, torch.bfloat16), "weight must be float32 or bfloat16")
+    w3 = w.unsqueeze(0) if w.dim() == 2 else w
+    _need(w3.dim() == 3, "weight must be [n, k] or [experts, n, k]")
+    w3 = w3.contiguous()
+    e, n, k = w3.shape
+    n_pad = (n + 127) // 128 * 128
+    q = torch.empty((e, n_pad, k), dtype=torch.uint8, device=w.device)
+    sf = torch.empty((e, n_pad * (k // 32)), dtype=torch.uint8, device=w.device)
+    pw = PreparedWeight(q, sf, n)
+    dt = IN_BF16 if w3.dtype == torch.bfloat16 else IN_F32
+    _check(library().mxfp8_prepare_weight(_ptr(w3), dt, ctypes.byref(pw.c), _stream(w)),
+           "mxfp8_prepare_weight")
+    return pw
+
+
+# -------------------------------------------------------------- activations
+def quantize_act(x: torch.Tensor):
+    """BF16 [m, k] -> (E4M3 bytes uint8 [m, k], 8x4 scales uint8 [ceil8(m)*k/32])."""
+    _need(x.is_cuda and x.dtype == torch.bfloat16, "x must be a bfloat16 CUDA tensor")
+    x2 = x.reshape(-1, x.shape[-1]).contiguous()
+    m, k = x2.shape
+    q = torch.empty((m, k), dtype=torch.uint8, device=x.device)
+    sf = torch.empty((max(act_scale_bytes(m, k), 1),), dtype=torch.uint8, device=x.device)
+    _check(library().mxfp8_quantize_act(_ptr(x2), m, k, _ptr(q), _ptr(sf), _stream(x)),
+           "mxfp8_quantize_act")
+    return q, sf[:act_scale_bytes(m, k)]
+
+
+def gemm(qa: torch.Tensor, sfa: torch.Tensor, pw: PreparedWeight, bias=None) -> torch.Tensor:
+    """Block-scaled GEMM on pre-quantized activations -> BF16 [m, n]."""
+    m = qa.shape[0]
+    y = torch.empty((m, pw.n), dtype=torch.bfloat16, device=qa.device)
+    _check(library().mxfp8_gemm(_ptr(qa), _ptr(sfa), m, ctypes.byref(pw.c), _ptr(bias), _ptr(y),
+                                _stream(qa)), "mxfp8_gemm")
+    return y
+
+
+def linear(x: torch.Tensor, pw: PreparedWeight, bias=None, workspace=None) -> torch.Tensor:
+    """The layer: BF16 x [..., k] -> BF16 [..., n] (leading dims kept, as
+    apply_weights does)."""
+    _need(x.is_cuda and x.dtype == torch.bfloat16, "x must be a bfloat16 CUDA tensor")
+    _need(x.shape[-1] == pw.k, "x's last dim must equal the weight's K")
+    lead = x.shape[:-1]
+    x2 = x.reshape(-1, pw.k).contiguous()
+    m = x2.shape[0]
+    if bias is not None:
+        _need(bias.dtype == torch.bfloat16 and bias.numel() == pw.n, "bias must be bf16 [n]")
+    ws_need = linear_workspace_bytes(m, pw.k)
+    if workspace is None:
+        workspace = torch.empty((max(ws_need, 16),), dtype=torch.uint8, device=x.device)
+    y = torch.empty((m, pw.n), dtype=torch.bfloat16, device=x.device)
+    _check(library().mxfp8_linear(_ptr(x2), m, ctypes.byref(pw.c), _ptr(bias), _ptr(y),
+                                  _ptr(workspace), workspace.numel(), _stream(x)), "mxfp8_linear")
+    return y.reshape(*lead, pw.n)
+
+
+def grouped_linear(x_sorted: torch.Tensor, offsets: torch.Tensor, pw: PreparedWeight,
+                   bias=None, workspace=None) -> torch.Tensor:
+    """Per-expert layer over expert-sorted rows: x_sorted bf16 [rows, k],
+    offsets int32 [e+1] (device) -> bf16 [rows, n]."""
+    _need(x_sorted.is_cuda and x_sorted.dtype == torch.bfloat16, "x_sorted must be bf16 CUDA")
+    _need(offsets.dtype == torch.int32 and offsets.is_cuda, "offsets must be int32 CUDA")
+    _need(offsets.numel() == pw.num_experts + 1, "offsets must have num_experts + 1 entries")
+    rows = x_sorted.shape[0]
+    x2 = x_sorted.contiguous()
+    ws_need = linear_workspace_bytes(rows, pw.k)
+    if workspace is None:
+        workspace = torch.empty((max(ws_need, 16),), dtype=torch.uint8, device=x_sorted.device)
+    y = torch.empty((rows, pw.n), dtype=torch.bfloat16, device=x_sorted.device)
+    _check(library().mxfp8_grouped_linear(_ptr(x2), rows, _ptr(offsets.contiguous()),
+                                          ctypes.byref(pw.c), _ptr(bias), _ptr(y),
+                                          _ptr(workspace), workspace.numel(), _stream(x_sorted)),
+           "mxfp8_grouped_linear")
+    return y
+
+
+# ------------------------------------------------------------------ hooks
+def set_schedule(tokens_per_tile: int = 0, split_k: int = 0) -> None:
+    """Pin the GEMM schedule (testing/benchmarking); 0 = automatic."""
+    library().mxfp8_set_schedule(int(tokens_per_tile), int(split_k))
+
+
+def device_error() -> int:
+    """Synchronise and read/clear the kernels' device-side timeout word."""
+    return library().mxfp8_device_error()

@@ -1,0 +1,246 @@
+// api.cu -- the extern "C" boundary declared in include/mxfp8.h.
+//
+// Host-side validation happens before any launch; every entry point is
+// asynchronous on the caller's stream and never allocates.  The layer's
+// steps follow vLLM PR #52204 "[Kernel] Add FlashInfer TRTLLM MXFP8 linear
+// backend": process_weights_after_loading -> mxfp8_prepare_weight,
+// flashinfer_mxfp8_quantize_8x4 -> mxfp8_quantize_act, mm_mxfp8 + slice +
+// bias -> mxfp8_gemm, apply_weights -> mxfp8_linear.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdlib.h>
+
+#include "../../include/mxfp8.h"
+#include "internal.h"
+
+namespace {
+
+thread_local int t_last_cuda_error = 0;
+int g_force_tt = 0;
+int g_force_split = 0;
+
+struct DeviceInfo {
+    int checked;  // 0 unknown, 1 supported, -1 unsupported
+    int sms;
+};
+DeviceInfo g_dev[64];
+
+mxfp8_status cuda_fail(cudaError_t e) {
+    t_last_cuda_error = static_cast<int>(e);
+    return MXFP8_ERR_CUDA;
+}
+
+// Current device must be compute capability 10.3 (GB300).
+mxfp8_status device_sms(int* sms) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= 64) return MXFP8_ERR_UNSUPPORTED_DEVICE;
+    DeviceInfo& d = g_dev[dev];
+    if (d.checked == 0) {
+        int major = 0, minor = 0, count = 0;
+        if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return cuda_fail(e);
+        d.sms = count;
+        d.checked = (major == 10 && minor == 3) ? 1 : -1;
+    }
+    if (d.checked < 0) return MXFP8_ERR_UNSUPPORTED_DEVICE;
+    *sms = d.sms;
+    return MXFP8_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t ceil_to(int64_t v, int64_t q) { return (v + q - 1) / q * q; }
+
+// Shape limits keep every in-kernel index (int32 token/row counts, int64
+// byte offsets) in range.
+constexpr int64_t kMaxRows = (int64_t(1) << 31) - 256;
+constexpr int64_t kMaxK = int64_t(1) << 20;
+
+mxfp8_status check_weight(const mxfp8_weight* w) {
+    if (!w || !w->q || !w->sf) return MXFP8_ERR_INVALID_ARG;
+    if (w->num_experts < 1 || w->num_experts > 1024 || w->n < 1 || w->k < 1) return MXFP8_ERR_INVALID_ARG;
+    if (w->k % 256 != 0) return MXFP8_ERR_K_NOT_MULTIPLE_OF_256;
+    if (w->k > kMaxK || w->n_pad != ceil_to(w->n, 128) || w->num_experts * w->n_pad > kMaxRows)
+        return MXFP8_ERR_INVALID_ARG;
+    if (!aligned16(w->q) || !aligned16(w->sf)) return MXFP8_ERR_MISALIGNED;
+    return MXFP8_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t mxfp8_act_scale_bytes(int64_t m, int64_t k) {
+    if (m < 0 || k <= 0 || k % 32 != 0) return 0;
+    return static_cast<size_t>(ceil_to(m, 8) * ceil_to(k / 32, 4));
+}
+
+size_t mxfp8_weight_bytes(int64_t n, int64_t k) {
+    if (n <= 0 || k <= 0) return 0;
+    return static_cast<size_t>(ceil_to(n, 128) * k);
+}
+
+size_t mxfp8_weight_scale_bytes(int64_t n, int64_t k) {
+    if (n <= 0 || k <= 0 || k % 32 != 0) return 0;
+    return static_cast<size_t>(ceil_to(n, 128) * (k / 32));
+}
+
+size_t mxfp8_linear_workspace_bytes(int64_t m, int64_t k) {
+    if (m < 0 || k <= 0 || k % 32 != 0) return 0;
+    return static_cast<size_t>(ceil_to(m * k, 256)) + mxfp8_act_scale_bytes(m, k);
+}
+
+mxfp8_status mxfp8_weight_view(mxfp8_weight* w, int64_t num_experts, int64_t n, int64_t k, void* q,
+                               void* sf) {
+    if (!w) return MXFP8_ERR_INVALID_ARG;
+    w->num_experts = num_experts;
+    w->n = n;
+    w->n_pad = n > 0 ? ceil_to(n, 128) : 0;
+    w->k = k;
+    w->q = q;
+    w->sf = sf;
+    return check_weight(w);
+}
+
+mxfp8_status mxfp8_prepare_weight(const void* src, mxfp8_in_dtype dtype, const mxfp8_weight* w,
+                                  void* stream) {
+    mxfp8_status st = check_weight(w);
+    if (st != MXFP8_OK) return st;
+    if (!src || (dtype != MXFP8_IN_F32 && dtype != MXFP8_IN_BF16)) return MXFP8_ERR_INVALID_ARG;
+    if (!aligned16(src)) return MXFP8_ERR_MISALIGNED;
+    int sms = 0;
+    if ((st = device_sms(&sms)) != MXFP8_OK) return st;
+    cudaError_t e = mxk::launch_prepare_weight(src, dtype == MXFP8_IN_BF16, w->num_experts, w->n, w->n_pad,
+                                               w->k, static_cast<uint8_t*>(w->q),
+                                               static_cast<uint8_t*>(w->sf), sms,
+                                               static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MXFP8_OK : cuda_fail(e);
+}
+
+mxfp8_status mxfp8_quantize_act(const void* x, int64_t m, int64_t k, void* q, void* sf, void* stream) {
+    if (m < 0 || k < 1) return MXFP8_ERR_INVALID_ARG;
+    if (k % 256 != 0) return MXFP8_ERR_K_NOT_MULTIPLE_OF_256;
+    if (m > kMaxRows || k > kMaxK) return MXFP8_ERR_INVALID_ARG;
+    if (m == 0) return MXFP8_OK;
+    if (!x || !q || !sf) return MXFP8_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(q) || !aligned16(sf)) return MXFP8_ERR_MISALIGNED;
+    int sms = 0;
+    mxfp8_status st = device_sms(&sms);
+    if (st != MXFP8_OK) return st;
+    cudaError_t e = mxk::launch_quant_act(x, m, k, static_cast<uint8_t*>(q), static_cast<uint8_t*>(sf),
+                                          sms, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MXFP8_OK : cuda_fail(e);
+}
+
+static mxfp8_status run_gemm(const void* qa, const void* sfa, int64_t m, const mxfp8_weight* w,
+                             const void* bias, void* y, const int32_t* offsets, bool after_quant,
+                             int sms, cudaStream_t s) {
+    mxk::GemmProblem p;
+    p.qa = static_cast<const uint8_t*>(qa);
+    p.sfa = static_cast<const uint8_t*>(sfa);
+    p.m = m;
+    p.wq = static_cast<const uint8_t*>(w->q);
+    p.wsf = static_cast<const uint8_t*>(w->sf);
+    p.experts = w->num_experts;
+    p.n = w->n;
+    p.n_pad = w->n_pad;
+    p.k = w->k;
+    p.bias = bias;
+    p.y = y;
+    p.offsets = offsets;
+    p.after_quant = after_quant;
+    const mxk::GemmSchedule sch = mxk::choose_schedule(p, sms, g_force_tt, g_force_split);
+    bool enc_fail = false;
+    cudaError_t e = mxk::launch_gemm(p, sch, sms, s, &enc_fail);
+    if (enc_fail) return MXFP8_ERR_INVALID_ARG;
+    return e == cudaSuccess ? MXFP8_OK : cuda_fail(e);
+}
+
+mxfp8_status mxfp8_gemm(const void* qa, const void* sfa, int64_t m, const mxfp8_weight* w,
+                        const void* bias, void* y, void* stream) {
+    mxfp8_status st = check_weight(w);
+    if (st != MXFP8_OK) return st;
+    if (w->num_experts != 1 || m < 0 || m > kMaxRows) return MXFP8_ERR_INVALID_ARG;
+    if (m == 0) return MXFP8_OK;
+    if (!qa || !sfa || !y) return MXFP8_ERR_INVALID_ARG;
+    if (!aligned16(qa) || !aligned16(sfa)) return MXFP8_ERR_MISALIGNED;
+    if ((reinterpret_cast<uintptr_t>(y) & 1u) || (reinterpret_cast<uintptr_t>(bias) & 1u))
+        return MXFP8_ERR_MISALIGNED;
+    int sms = 0;
+    if ((st = device_sms(&sms)) != MXFP8_OK) return st;
+    return run_gemm(qa, sfa, m, w, bias, y, nullptr, false, sms, static_cast<cudaStream_t>(stream));
+}
+
+static mxfp8_status linear_common(const void* x, int64_t m, const int32_t* offsets,
+                                  const mxfp8_weight* w, const void* bias, void* y, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+    mxfp8_status st = check_weight(w);
+    if (st != MXFP8_OK) return st;
+    if (m < 0 || m > kMaxRows) return MXFP8_ERR_INVALID_ARG;
+    if (m == 0) return MXFP8_OK;
+    if (!x || !y || !workspace) return MXFP8_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(workspace)) return MXFP8_ERR_MISALIGNED;
+    if ((reinterpret_cast<uintptr_t>(y) & 1u) || (reinterpret_cast<uintptr_t>(bias) & 1u))
+        return MXFP8_ERR_MISALIGNED;
+    if (workspace_bytes < mxfp8_linear_workspace_bytes(m, w->k)) return MXFP8_ERR_WORKSPACE_TOO_SMALL;
+    int sms = 0;
+    if ((st = device_sms(&sms)) != MXFP8_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* qa = static_cast<uint8_t*>(workspace);
+    uint8_t* sfa = qa + ceil_to(m * w->k, 256);
+    cudaError_t e = mxk::launch_quant_act(x, m, w->k, qa, sfa, sms, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return run_gemm(qa, sfa, m, w, bias, y, offsets, true, sms, s);
+}
+
+mxfp8_status mxfp8_linear(const void* x, int64_t m, const mxfp8_weight* w, const void* bias, void* y,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+    if (w && w->num_experts != 1) return MXFP8_ERR_INVALID_ARG;
+    return linear_common(x, m, nullptr, w, bias, y, workspace, workspace_bytes, stream);
+}
+
+mxfp8_status mxfp8_grouped_linear(const void* x_sorted, int64_t rows, const int32_t* expert_offsets,
+                                  const mxfp8_weight* w, const void* bias, void* y, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+    if (!expert_offsets) return MXFP8_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(expert_offsets) & 3u)) return MXFP8_ERR_MISALIGNED;
+    return linear_common(x_sorted, rows, expert_offsets, w, bias, y, workspace, workspace_bytes, stream);
+}
+
+const char* mxfp8_status_string(mxfp8_status s) {
+    switch (s) {
+        case MXFP8_OK: return "ok";
+        case MXFP8_ERR_INVALID_ARG: return "invalid argument";
+        case MXFP8_ERR_K_NOT_MULTIPLE_OF_256: return "K must be a multiple of 256";
+        case MXFP8_ERR_MISALIGNED: return "device pointer not 16-byte aligned";
+        case MXFP8_ERR_UNSUPPORTED_DEVICE: return "device is not compute capability 10.3 (GB300)";
+        case MXFP8_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+        case MXFP8_ERR_DEVICE_TIMEOUT: return "a kernel gave up waiting (device timeout)";
+        case MXFP8_ERR_CUDA: return "CUDA error (see mxfp8_last_cuda_error)";
+    }
+    return "unknown status";
+}
+
+int mxfp8_last_cuda_error(void) { return t_last_cuda_error; }
+
+mxfp8_status mxfp8_device_error(void) {
+    unsigned int v = 0;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = mxk::read_and_clear_gemm_error(&v);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return v ? MXFP8_ERR_DEVICE_TIMEOUT : MXFP8_OK;
+}
+
+void mxfp8_set_schedule(int tokens_per_tile, int split_k) {
+    const bool tt_ok = tokens_per_tile == 0 || tokens_per_tile == 16 || tokens_per_tile == 32 ||
+                       tokens_per_tile == 64 || tokens_per_tile == 128 || tokens_per_tile == 256;
+    g_force_tt = tt_ok ? tokens_per_tile : 0;
+    g_force_split = (split_k >= 0 && split_k <= 8) ? split_k : 0;
+}
+
+}  // extern "C"

@@ -1,0 +1,665 @@
+// gemm.cu -- MXFP8 block-scaled GEMM + padded-N slice + bias for sm_103a.
+//
+// Computes, for token rows i and output features j < N (vLLM PR #52204
+// "[Kernel] Add FlashInfer TRTLLM MXFP8 linear backend", apply_weights: the
+// mm_mxfp8 product with FP32 accumulation, then output[:, :N] + bias):
+//   y[i][j] = bf16( sum_b 2^(sa[i,b]-127) 2^(sw[j,b]-127) sum_{k in b} qa[i,k] qw[j,k] + bias[j] )
+//
+// Orientation.  The weights are the MMA's A operand (M = 128 rows of N per
+// tile) and the tokens its B operand (N = 16..256 tokens per tile): the
+// accumulator D^T[n, token] lives in TMEM with one weight row per lane.  This
+// is why N is padded to 128 and why the small-M case needs no padding of the
+// token count beyond 16 (the "shuffling for transposed MMA outputs" of
+// FlashInfer PR #1214 names the same choice).
+//
+// Per CTA (320 threads, 10 warps):
+//   warp 0      TMA producer: per 128-wide K block, one 128x128 weight tile,
+//               the token tile (TMA boxes of <= 32 rows), the weight scales
+//               (one 512-byte bulk copy, already in TMEM-copy order) and the
+//               raw 8x4 activation-scale groups (one TMA box).
+//   warp 1      TMEM allocator and MMA issuer: re-orders the activation scales
+//               into the 32x16-byte TMEM-copy order in shared memory, copies
+//               both scale tiles into TMEM (tcgen05.cp 32x128b.warpx4), issues
+//               four tcgen05.mma kind::mxf8f6f4 block_scale (K = 32 each) and
+//               commits the stage back to the producer.
+//   warps 2..9  epilogue: two warps per TMEM lane quadrant, each half of the
+//               token columns; tcgen05.ld, release the accumulator, then
+//               + bias, BF16 rounding and masked stores (j < N, token < M).
+// Schedules:
+//   split_k == 1  persistent: grid <= #SMs, tiles strided over CTAs.
+//   split_k  > 1  a cluster of split_k CTAs per tile, each a K range; FP32
+//                 partials meet in distributed shared memory and are summed in
+//                 rank order (deterministic), each rank finishing a slice of
+//                 the tokens.
+// Every wait is bounded (kWaitNs); a timeout sets g_gemm_error, every role
+// unwinds, in-flight copies and MMAs are drained (again bounded), TMEM is
+// freed and the kernel returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace mxk {
+
+__device__ unsigned int g_gemm_error;
+
+namespace {
+
+constexpr uint64_t kWaitNs = 4000000000ull;   // 4 s per wait, then give up
+constexpr uint64_t kDrainNs = 200000000ull;   // 0.2 s per drain wait
+constexpr int kThreads = 320;
+constexpr int kEpilogueWarps = 8;
+constexpr int kMaxExperts = 1024;
+
+struct GemmArgs {
+    CUtensorMap map_w;     // weights [experts*n_pad, k] u8, box {128, 128}, 128B swizzle
+    CUtensorMap map_a;     // activations [m, k] u8, box {128, box_rows}, 128B swizzle
+    CUtensorMap map_asf;   // 8x4 scales as [m8/8, k/4] u8, box {32, sf_groups}
+    const uint8_t* wsf;
+    const __nv_bfloat16* bias;
+    __nv_bfloat16* y;
+    const int32_t* offsets;  // grouped segment offsets, or null (dense)
+    int m, n, n_pad, kq;     // kq = k / 128
+    int experts, n_tiles;
+    int box_rows, sf_groups;
+    int stages, splits;
+    int num_tiles;           // dense only (grouped counts tiles on the device)
+    uint32_t tmem_cols;
+};
+
+template <int TT>
+struct Geometry {
+    static constexpr int kSfChunks = (TT + 127) / 128;          // 128-token scale chunks
+    static constexpr int kOffW = 0;
+    static constexpr int kOffA = 16384;
+    static constexpr int kOffWsf = kOffA + TT * 128;
+    static constexpr int kOffAsfRaw = kOffWsf + 512;
+    static constexpr int kOffAsfT = kOffAsfRaw + 1152;            // 36 groups x 32 B max
+    static constexpr int kStageBytes = ((kOffAsfT + 512 * kSfChunks) + 1023) / 1024 * 1024;
+    static constexpr int kSfSlotCols = 4 + 4 * kSfChunks;         // TMEM columns per stage
+    static constexpr int kPartialBytes = 128 * TT * 4;
+};
+
+struct TileInfo {
+    int e, n_tile, tok0, count;
+};
+
+template <int TT>
+__device__ __forceinline__ TileInfo decode_tile(int t, const GemmArgs& p, const int* prefix,
+                                                const int* offs) {
+    TileInfo ti;
+    if (p.offsets == nullptr) {
+        const int tok_tiles = (p.m + TT - 1) / TT;
+        constexpr int kBand = 8;  // token tiles per band: the band's weights stay hot in L2
+        const int band_size = kBand * p.n_tiles;
+        const int band = t / band_size;
+        const int r = t - band * band_size;
+        const int g = min(kBand, tok_tiles - band * kBand);
+        const int tt = band * kBand + r % g;
+        ti.e = 0;
+        ti.n_tile = r / g;
+        ti.tok0 = tt * TT;
+        ti.count = min(TT, p.m - ti.tok0);
+    } else {
+        int lo = 0, hi = p.experts;  // find e with prefix[e] <= t < prefix[e+1]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (prefix[mid] <= t) lo = mid; else hi = mid;
+        }
+        const int e = lo;
+        const int seg = offs[e + 1] - offs[e];
+        const int ntt = (seg + TT - 1) / TT;
+        const int local = t - prefix[e];
+        const int nt = local / ntt;
+        const int tt = local - nt * ntt;
+        ti.e = e;
+        ti.n_tile = nt;
+        ti.tok0 = offs[e] + tt * TT;
+        ti.count = min(TT, seg - tt * TT);
+    }
+    return ti;
+}
+
+__device__ __forceinline__ void record_timeout(volatile uint32_t* abort_flag) {
+    atomicOr(&g_gemm_error, 1u);
+    *abort_flag = 1u;
+}
+
+template <int TT>
+__global__ void __launch_bounds__(kThreads, 1) mxfp8_gemm_kernel(const __grid_constant__ GemmArgs p) {
+    using G = Geometry<TT>;
+    extern __shared__ uint8_t smem_dyn[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~static_cast<uintptr_t>(1023));
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int stages = p.stages;
+    const bool split = p.splits > 1;
+
+    uint8_t* partial = smem + stages * G::kStageBytes;  // split-K partials [TT][128] f32
+    uint8_t* ctrl = partial + (split ? G::kPartialBytes : 0);
+    uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
+    uint64_t* empty = full + stages;
+    uint64_t* acc_full = empty + stages;
+    uint64_t* acc_empty = acc_full + 1;
+    uint64_t* drain = acc_empty + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile uint32_t* abort_flag = tmem_slot + 1;
+    int* prefix = reinterpret_cast<int*>(tmem_slot + 2);   // [experts + 1]
+    int* offs = prefix + (kMaxExperts + 1);                 // [experts + 1]
+
+    // ---------------------------------------------------------------- setup
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&p.map_w);
+        tma_prefetch_desc(&p.map_a);
+        tma_prefetch_desc(&p.map_asf);
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(acc_full, 1);
+        mbar_init(acc_empty, kEpilogueWarps);
+        mbar_init(drain, 1);
+        *abort_flag = 0u;
+        fence_barrier_init();
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, p.tmem_cols);
+    if (warp == 2 && p.offsets != nullptr) {
+        // Grouped: per-expert tile counts -> exclusive prefix (tiles ordered
+        // expert-major, then n-tile, then token tile).  The offsets were
+        // written before this layer's first kernel began.
+        const int ne = p.experts;
+        int carry = 0;
+        for (int base = 0; base <= ne; base += 32) {
+            const int i = base + lane;
+            int o = (i <= ne) ? p.offsets[i] : 0;
+            if (i <= ne) offs[i] = o;
+            int o_next = __shfl_down_sync(0xFFFFFFFFu, o, 1);
+            if (lane == 31) o_next = (i + 1 <= ne) ? p.offsets[i + 1] : 0;
+            int cnt = 0;
+            if (i < ne) {
+                const int seg = o_next - o;
+                cnt = seg > 0 ? p.n_tiles * ((seg + TT - 1) / TT) : 0;
+            }
+            int incl = cnt;  // inclusive warp scan
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int v = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+                if (lane >= d) incl += v;
+            }
+            if (i <= ne) prefix[i] = carry + incl - cnt;
+            carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    // Work assignment: a list of (tile, K range).
+    int tile_first, tile_stride, num_tiles, kb_begin, kb_end;
+    if (split) {
+        const int r = static_cast<int>(cluster_rank());
+        tile_first = static_cast<int>(cluster_id_x());
+        tile_stride = 1 << 30;
+        num_tiles = tile_first + 1;
+        kb_begin = (r * p.kq) / p.splits;
+        kb_end = ((r + 1) * p.kq) / p.splits;
+    } else {
+        tile_first = blockIdx.x;
+        tile_stride = gridDim.x;
+        num_tiles = (p.offsets == nullptr) ? p.num_tiles : prefix[p.experts];
+        kb_begin = 0;
+        kb_end = p.kq;
+    }
+
+    if (warp == 0) {
+        // ------------------------------------------------------- producer
+        if (lane == 0) {
+            const uint64_t pol_w = policy_evict_normal();
+            const uint64_t pol_a = policy_evict_last();
+            int job = 0;
+            // Weight bytes of the first `stages` jobs are issued before waiting
+            // for the activation quantizer (programmatic dependent launch):
+            // only the activations and their scales depend on it.
+            int pre = 0;
+            {
+                int t = tile_first;
+                for (; pre < stages && t < num_tiles;) {
+                    const TileInfo ti = decode_tile<TT>(t, p, prefix, offs);
+                    for (int kb = kb_begin; kb < kb_end && pre < stages; ++kb, ++pre) {
+                        const int s = pre;
+                        uint8_t* st = smem + s * G::kStageBytes;
+                        const int nloads = (ti.count + p.box_rows - 1) / p.box_rows;
+                        const uint32_t bytes = 16384u + 512u +
+                                               static_cast<uint32_t>(nloads * p.box_rows * 128) +
+                                               static_cast<uint32_t>(p.sf_groups * 32);
+                        mbar_arrive_expect_tx(&full[s], bytes);
+                        tma_load_2d(st + G::kOffW, &p.map_w, kb * 128,
+                                    ti.e * p.n_pad + ti.n_tile * 128, &full[s], pol_w);
+                        bulk_load(st + G::kOffWsf,
+                                  p.wsf + ((static_cast<size_t>(ti.e) * p.n_tiles + ti.n_tile) * p.kq + kb) * 512,
+                                  512, &full[s], pol_w);
+                    }
+                    if (pre < stages) t += tile_stride;
+                }
+            }
+            pdl_wait();
+            {
+                int t = tile_first, issued = 0;
+                for (; issued < pre;) {
+                    const TileInfo ti = decode_tile<TT>(t, p, prefix, offs);
+                    for (int kb = kb_begin; kb < kb_end && issued < pre; ++kb, ++issued) {
+                        const int s = issued;
+                        uint8_t* st = smem + s * G::kStageBytes;
+                        const int nloads = (ti.count + p.box_rows - 1) / p.box_rows;
+                        for (int l = 0; l < nloads; ++l)
+                            tma_load_2d(st + G::kOffA + l * p.box_rows * 128, &p.map_a, kb * 128,
+                                        ti.tok0 + l * p.box_rows, &full[s], pol_a);
+                        tma_load_2d(st + G::kOffAsfRaw, &p.map_asf, kb * 32, ti.tok0 >> 3, &full[s],
+                                    pol_a);
+                    }
+                    t += tile_stride;
+                }
+            }
+            // Steady state.
+            job = 0;
+            bool stop = false;
+            for (int t = tile_first; t < num_tiles && !stop; t += tile_stride) {
+                const TileInfo ti = decode_tile<TT>(t, p, prefix, offs);
+                const int nloads = (ti.count + p.box_rows - 1) / p.box_rows;
+                const uint32_t bytes = 16384u + 512u +
+                                       static_cast<uint32_t>(nloads * p.box_rows * 128) +
+                                       static_cast<uint32_t>(p.sf_groups * 32);
+                for (int kb = kb_begin; kb < kb_end; ++kb, ++job) {
+                    if (job < pre) continue;
+                    if (*abort_flag) { stop = true; break; }
+                    const int s = job % stages;
+                    const int round = job / stages;
+                    if (!mbar_wait(&empty[s], (round & 1) ^ 1, kWaitNs)) {
+                        record_timeout(abort_flag);
+                        stop = true;
+                        break;
+                    }
+                    uint8_t* st = smem + s * G::kStageBytes;
+                    mbar_arrive_expect_tx(&full[s], bytes);
+                    tma_load_2d(st + G::kOffW, &p.map_w, kb * 128, ti.e * p.n_pad + ti.n_tile * 128,
+                                &full[s], pol_w);
+                    bulk_load(st + G::kOffWsf,
+                              p.wsf + ((static_cast<size_t>(ti.e) * p.n_tiles + ti.n_tile) * p.kq + kb) * 512,
+                              512, &full[s], pol_w);
+                    for (int l = 0; l < nloads; ++l)
+                        tma_load_2d(st + G::kOffA + l * p.box_rows * 128, &p.map_a, kb * 128,
+                                    ti.tok0 + l * p.box_rows, &full[s], pol_a);
+                    tma_load_2d(st + G::kOffAsfRaw, &p.map_asf, kb * 32, ti.tok0 >> 3, &full[s], pol_a);
+                }
+            }
+            // Drain: the last use of each stage must have landed before exit.
+            const int issued_jobs = job > pre ? job : pre;
+            for (int j = issued_jobs - 1; j >= 0 && j >= issued_jobs - stages; --j)
+                (void)mbar_wait(&full[j % stages], (j / stages) & 1, kDrainNs);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        int job = 0, tile_iter = 0;
+        bool stop = false;
+        for (int t = tile_first; t < num_tiles && !stop; t += tile_stride, ++tile_iter) {
+            const TileInfo ti = decode_tile<TT>(t, p, prefix, offs);
+            const uint32_t n_mma = static_cast<uint32_t>((ti.count + 15) & ~15);
+            const int off8 = ti.tok0 & 7;
+            if (tile_iter > 0) {
+                bool ok = true;
+                if (lane == 0) ok = mbar_wait(acc_empty, (tile_iter - 1) & 1, kWaitNs);
+                ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+                if (!ok) { if (lane == 0) record_timeout(abort_flag); break; }
+            }
+            for (int kb = kb_begin; kb < kb_end; ++kb, ++job) {
+                const int s = job % stages;
+                bool ok = mbar_wait(&full[s], (job / stages) & 1, kWaitNs);
+                ok = __all_sync(0xFFFFFFFFu, ok ? 1 : 0) != 0;
+                if (!ok || *abort_flag) {
+                    if (lane == 0 && !ok) record_timeout(abort_flag);
+                    stop = true;
+                    break;
+                }
+                uint8_t* st = smem + s * G::kStageBytes;
+                // Activation scales: token j of the tile is word (off8 + j) of
+                // the raw 8x4 groups; the TMEM-copy order puts token j of each
+                // 128-chunk at word (j%32)*4 + (j%128)/32.
+                const uint32_t* raw = reinterpret_cast<const uint32_t*>(st + G::kOffAsfRaw);
+#pragma unroll
+                for (int c = 0; c < G::kSfChunks; ++c) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int jq = 0; jq < 4; ++jq) {
+                        const int j = c * 128 + jq * 32 + lane;
+                        w[jq] = (j < TT) ? raw[off8 + j] : 0u;
+                    }
+                    *reinterpret_cast<uint4*>(st + G::kOffAsfT + c * 512 + lane * 16) =
+                        make_uint4(w[0], w[1], w[2], w[3]);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tc_fence_after();
+                    const uint32_t sfa = tmem_base + TT + s * G::kSfSlotCols;
+                    const uint32_t sfb = sfa + 4;
+                    tmem_copy_sf(sfa, desc_sf_32x16(smem_addr(st + G::kOffWsf)));
+#pragma unroll
+                    for (int c = 0; c < G::kSfChunks; ++c)
+                        tmem_copy_sf(sfb + 4 * c, desc_sf_32x16(smem_addr(st + G::kOffAsfT + c * 512)));
+                    const uint32_t a_base = smem_addr(st + G::kOffW);
+                    const uint32_t b_base = smem_addr(st + G::kOffA);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint32_t idesc = idesc_mxf8(128, n_mma, kk, kk);
+                        mma_mxf8(tmem_base, desc_kmajor_sw128(a_base + kk * 32),
+                                 desc_kmajor_sw128(b_base + kk * 32), idesc, sfa, sfb,
+                                 (kb > kb_begin || kk > 0) ? 1u : 0u);
+                    }
+                    mma_commit(&empty[s]);
+                    if (kb == kb_end - 1) mma_commit(acc_full);
+                }
+                __syncwarp();
+            }
+        }
+        // Drain every MMA this thread issued before TMEM is released.
+        if (lane == 0) {
+            mma_commit(drain);
+            (void)mbar_wait(drain, 0, kDrainNs);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------- epilogue
+        const int ew = warp - 2;
+        const int quad = warp & 3;             // TMEM lanes [32*quad, 32*quad + 32)
+        const int half = ew >> 2;              // token columns [half*TT/2, (half+1)*TT/2)
+        constexpr int kCols = TT / 2;
+        const int col0 = half * kCols;
+        int tile_iter = 0;
+        for (int t = tile_first; t < num_tiles; t += tile_stride, ++tile_iter) {
+            const TileInfo ti = decode_tile<TT>(t, p, prefix, offs);
+            bool ok = mbar_wait(acc_full, tile_iter & 1, kWaitNs);
+            ok = __all_sync(0xFFFFFFFFu, ok ? 1 : 0) != 0;
+            if (!ok) { if (lane == 0) record_timeout(abort_flag); break; }
+            tc_fence_after();
+            uint32_t acc[kCols];
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + col0;
+            if constexpr (kCols >= 32) {
+#pragma unroll
+                for (int c = 0; c < kCols / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_load_32(taddr + c * 32, r);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) acc[c * 32 + i] = r[i];
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < kCols / 8; ++c) {
+                    uint32_t r[8];
+                    tmem_load_8(taddr + c * 8, r);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) acc[c * 8 + i] = r[i];
+                }
+            }
+            tmem_load_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty);
+
+            const int nl = quad * 32 + lane;  // weight row within the tile
+            if (split) {
+                float* part = reinterpret_cast<float*>(partial);
+#pragma unroll
+                for (int j = 0; j < kCols; ++j) part[(col0 + j) * 128 + nl] = __uint_as_float(acc[j]);
+            } else {
+                const int n = ti.n_tile * 128 + nl;
+                if (n < p.n) {
+                    const float b = p.bias ? __bfloat162float(p.bias[static_cast<size_t>(ti.e) * p.n + n]) : 0.0f;
+                    const int jmax = min(kCols, ti.count - col0);
+                    __nv_bfloat16* yp = p.y + static_cast<size_t>(ti.tok0 + col0) * p.n + n;
+#pragma unroll
+                    for (int j = 0; j < kCols; ++j)
+                        if (j < jmax) yp[static_cast<size_t>(j) * p.n] = __float2bfloat16_rn(__uint_as_float(acc[j]) + b);
+                }
+            }
+        }
+        __syncwarp();
+    }
+
+    // ------------------------------------------------- split-K reduction
+    if (split) {
+        cluster_sync();  // every rank's partial tile is in its shared memory
+        if (warp >= 2 && !*abort_flag) {
+            const TileInfo ti = decode_tile<TT>(tile_first, p, prefix, offs);
+            const int rank = static_cast<int>(cluster_rank());
+            const int per = (TT + p.splits - 1) / p.splits;
+            const int j0 = rank * per;
+            const int j1 = min(TT, j0 + per);
+            const int et = threadIdx.x - 64;
+            const uint32_t pbase = smem_addr(partial);
+            for (int o = et; o < (j1 - j0) * 128; o += kEpilogueWarps * 32) {
+                const int j = j0 + (o >> 7);
+                const int nl = o & 127;
+                const int n = ti.n_tile * 128 + nl;
+                if (j < ti.count && n < p.n) {
+                    const uint32_t a = pbase + static_cast<uint32_t>((j * 128 + nl) * 4);
+                    float sum = 0.0f;
+                    for (int r = 0; r < p.splits; ++r) sum += ld_cluster_f32(map_to_rank(a, r));
+                    if (p.bias) sum += __bfloat162float(p.bias[static_cast<size_t>(ti.e) * p.n + n]);
+                    p.y[static_cast<size_t>(ti.tok0 + j) * p.n + n] = __float2bfloat16_rn(sum);
+                }
+            }
+        }
+        cluster_sync();  // no CTA leaves while another still reads its partials
+    }
+
+    // -------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, p.tmem_cols);
+    }
+}
+
+// ------------------------------------------------------------------- host
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = []() -> EncodeTiledFn {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        return reinterpret_cast<EncodeTiledFn>(ptr);
+    }();
+    return fn;
+}
+
+bool encode_2d_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                  uint64_t row_stride, uint32_t box_inner, uint32_t box_outer, bool swizzle128) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {row_stride};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+uint32_t pow2_cols(int need) {
+    uint32_t c = 32;
+    while (c < static_cast<uint32_t>(need)) c <<= 1;
+    return c;
+}
+
+template <int TT>
+cudaError_t launch_tt(const GemmProblem& pr, int splits, int num_sms, cudaStream_t s,
+                      bool* encode_failed) {
+    using G = Geometry<TT>;
+    GemmArgs a;
+    memset(&a, 0, sizeof(a));
+    const int64_t m8 = (pr.m + 7) / 8 * 8;
+    a.box_rows = TT < 32 ? TT : 32;
+    a.sf_groups = TT / 8 + 1;
+    bool ok = encode_2d_u8(&a.map_w, pr.wq, pr.k, pr.experts * pr.n_pad, pr.k, 128, 128, true) &&
+              encode_2d_u8(&a.map_a, pr.qa, pr.k, pr.m, pr.k, 128, a.box_rows, true) &&
+              encode_2d_u8(&a.map_asf, pr.sfa, pr.k / 4, m8 / 8, pr.k / 4, 32, a.sf_groups, false);
+    if (!ok) {
+        *encode_failed = true;
+        return cudaErrorInvalidValue;
+    }
+    a.wsf = pr.wsf;
+    a.bias = static_cast<const __nv_bfloat16*>(pr.bias);
+    a.y = static_cast<__nv_bfloat16*>(pr.y);
+    a.offsets = pr.offsets;
+    a.m = static_cast<int>(pr.m);
+    a.n = static_cast<int>(pr.n);
+    a.n_pad = static_cast<int>(pr.n_pad);
+    a.kq = static_cast<int>(pr.k / 128);
+    a.experts = static_cast<int>(pr.experts);
+    a.n_tiles = static_cast<int>(pr.n_pad / 128);
+    a.splits = splits;
+
+    // Pipeline depth: as many stages as fit next to the partial buffer and
+    // control block (the split-K schedule never needs more than its K blocks).
+    const int ctrl = 8 * 64 + 8 + 4 * 2 * (kMaxExperts + 1) + 64;
+    const int partial = splits > 1 ? G::kPartialBytes : 0;
+    const int budget = 227 * 1024 - 1024 - ctrl - partial;
+    int stages = budget / G::kStageBytes;
+    if (stages > 8) stages = 8;
+    if (splits > 1) {
+        const int nk = (a.kq + splits - 1) / splits;
+        if (stages > nk) stages = nk;
+        // small tiles: leave room for a second CTA on the SM
+        if (TT <= 32 && stages > 4) stages = 4;
+    }
+    if (stages < 2) stages = 2;
+    a.stages = stages;
+    a.tmem_cols = pow2_cols(TT + stages * G::kSfSlotCols);
+    const size_t smem = 1024 + static_cast<size_t>(stages) * G::kStageBytes + partial + ctrl;
+
+    cudaError_t err = cudaFuncSetAttribute(mxfp8_gemm_kernel<TT>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    if (splits > 1) {
+        err = cudaFuncSetAttribute(mxfp8_gemm_kernel<TT>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (err != cudaSuccess) return err;
+    }
+
+    // TMEM is never oversubscribed: co-resident CTAs x columns <= 512.
+    int per_sm = 1;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mxfp8_gemm_kernel<TT>, kThreads, smem);
+    if (err != cudaSuccess) return err;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    if (static_cast<uint32_t>(per_sm) * a.tmem_cols > 512u) return cudaErrorInvalidConfiguration;
+
+    int grid;
+    if (splits > 1) {
+        const int tok_tiles = static_cast<int>((pr.m + TT - 1) / TT);
+        a.num_tiles = a.n_tiles * tok_tiles;
+        grid = a.num_tiles * splits;
+    } else if (pr.offsets == nullptr) {
+        const int tok_tiles = static_cast<int>((pr.m + TT - 1) / TT);
+        a.num_tiles = a.n_tiles * tok_tiles;
+        grid = a.num_tiles < num_sms * per_sm ? a.num_tiles : num_sms * per_sm;
+    } else {
+        a.num_tiles = 0;  // counted on the device from the offsets
+        grid = num_sms * per_sm;
+    }
+
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attrs[2];
+    int na = 0;
+    if (splits > 1) {
+        attrs[na].id = cudaLaunchAttributeClusterDimension;
+        attrs[na].val.clusterDim.x = splits;
+        attrs[na].val.clusterDim.y = 1;
+        attrs[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (pr.after_quant) {
+        attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attrs[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.attrs = attrs;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, mxfp8_gemm_kernel<TT>, a);
+}
+
+}  // namespace
+
+GemmSchedule choose_schedule(const GemmProblem& p, int num_sms, int force_tt, int force_split) {
+    GemmSchedule sch;
+    int tt;
+    if (p.offsets != nullptr) {
+        // grouped: size the token tile to the mean segment (rounded up)
+        const int64_t mean = (p.m + p.experts - 1) / (p.experts > 0 ? p.experts : 1);
+        tt = mean <= 16 ? 16 : mean <= 32 ? 32 : mean <= 64 ? 64 : mean <= 128 ? 128 : 256;
+    } else {
+        tt = p.m <= 16 ? 16 : p.m <= 32 ? 32 : p.m <= 64 ? 64 : p.m <= 128 ? 128 : 256;
+    }
+    if (force_tt) tt = force_tt;
+    int split = 1;
+    if (p.offsets == nullptr && tt <= 128) {
+        const int64_t tiles = (p.n_pad / 128) * ((p.m + tt - 1) / tt);
+        const int64_t kq = p.k / 128;
+        // enough CTAs to cover the SMs, at least two K blocks per CTA
+        int64_t want = (num_sms + tiles - 1) / tiles;
+        if (tt <= 32) want = (2 * num_sms + tiles - 1) / tiles;
+        if (want > 8) want = 8;
+        if (want > kq / 2) want = kq / 2;
+        if (want < 1) want = 1;
+        split = static_cast<int>(want);
+    }
+    if (force_split) split = force_split;
+    if (p.offsets != nullptr) split = 1;
+    if (split > p.k / 128) split = static_cast<int>(p.k / 128);
+    sch.tokens_per_tile = tt;
+    sch.split_k = split;
+    return sch;
+}
+
+cudaError_t launch_gemm(const GemmProblem& p, const GemmSchedule& sch, int num_sms, cudaStream_t s,
+                        bool* encode_failed) {
+    *encode_failed = false;
+    switch (sch.tokens_per_tile) {
+        case 16: return launch_tt<16>(p, sch.split_k, num_sms, s, encode_failed);
+        case 32: return launch_tt<32>(p, sch.split_k, num_sms, s, encode_failed);
+        case 64: return launch_tt<64>(p, sch.split_k, num_sms, s, encode_failed);
+        case 128: return launch_tt<128>(p, sch.split_k, num_sms, s, encode_failed);
+        case 256: return launch_tt<256>(p, sch.split_k, num_sms, s, encode_failed);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t read_and_clear_gemm_error(unsigned int* out) {
+    unsigned int zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(out, g_gemm_error, sizeof(unsigned int));
+    if (e != cudaSuccess) return e;
+    return cudaMemcpyToSymbol(g_gemm_error, &zero, sizeof(unsigned int));
+}
+
+}  // namespace mxk

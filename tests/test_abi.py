@@ -1,0 +1,116 @@
+"""Host-side checks of the C library (no GPU needed, no kernel launched).
+
+* the library loads and exports every function that include/mxfp8.h declares;
+* size helpers match the pages' formulas (8x4 scale buffer: prhub summary of
+  vLLM PR #52204, key source snippets; N padded to 128: vLLM PR #52204);
+* argument checks return their status before touching the device
+  (K % 256 != 0 is the load-time error of process_weights_after_loading).
+"""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mxfp8.h")
+
+
+@pytest.fixture(scope="module")
+def mx():
+    import __graft_entry__
+    __graft_entry__.build()
+    import mxfp8_block_scaled_x4_gb300 as m
+    return m
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*[\w\s\*]+?\b(mxfp8_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("mxfp8_prepare_weight", "mxfp8_quantize_act", "mxfp8_linear",
+                     "mxfp8_gemm", "mxfp8_grouped_linear", "mxfp8_act_scale_bytes"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(mx):
+    lib = ctypes.CDLL(mx.library_path())
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_size_helpers(mx):
+    for m in (0, 1, 7, 8, 9, 16, 129):
+        for k in (256, 512, 2048, 8192):
+            kb = k // 32
+            assert mx.act_scale_bytes(m, k) == math.ceil(m / 8) * 8 * math.ceil(kb / 4) * 4
+            ws = mx.linear_workspace_bytes(m, k)
+            assert ws == (m * k + 255) // 256 * 256 + mx.act_scale_bytes(m, k)
+    assert mx.weight_bytes(130, 256) == 256 * 256
+    assert mx.weight_scale_bytes(130, 256) == 256 * 8
+    assert mx.weight_bytes(5120, 2048) == 5120 * 2048
+    assert mx.act_scale_bytes(-1, 256) == 0
+    assert mx.weight_bytes(0, 256) == 0
+
+
+def test_status_strings(mx):
+    lib = mx.library()
+    for s in range(8):
+        assert lib.mxfp8_status_string(s)
+    assert b"256" in lib.mxfp8_status_string(2)
+
+
+def _view(mx, e, n, k, q, sf):
+    w = mx.mxfp8_weight()
+    st = mx.library().mxfp8_weight_view(ctypes.byref(w), e, n, k, q, sf)
+    return st, w
+
+
+def test_weight_view_checks(mx):
+    A = 1 << 20  # fake, aligned addresses: never dereferenced by the view
+    st, w = _view(mx, 1, 130, 256, A, A)
+    assert st == 0 and w.n_pad == 256
+    assert _view(mx, 1, 130, 320, A, A)[0] == 2          # K % 256
+    assert _view(mx, 1, 130, 256, A + 8, A)[0] == 3      # misaligned data
+    assert _view(mx, 1, 130, 256, A, A + 4)[0] == 3      # misaligned scales
+    assert _view(mx, 0, 130, 256, A, A)[0] == 1          # no experts
+    assert _view(mx, 1, 0, 256, A, A)[0] == 1            # no rows
+    assert _view(mx, 1, 130, 256, None, A)[0] == 1       # null
+    assert _view(mx, 1025, 128, 256, A, A)[0] == 1       # too many experts
+
+
+def test_argument_errors_before_launch(mx):
+    lib = mx.library()
+    A = 1 << 20
+    st, w = _view(mx, 1, 130, 256, A, A)
+    assert st == 0
+    wp = ctypes.byref(w)
+    # quantize: K % 256, negative M, M = 0 is a no-op
+    assert lib.mxfp8_quantize_act(A, 4, 320, A, A, None) == 2
+    assert lib.mxfp8_quantize_act(A, -1, 256, A, A, None) == 1
+    assert lib.mxfp8_quantize_act(A, 0, 256, A, A, None) == 0
+    assert lib.mxfp8_quantize_act(A + 2, 4, 256, A, A, None) == 3
+    # linear: M = 0 no-op, null / misaligned / small workspace
+    assert lib.mxfp8_linear(A, 0, wp, None, A, A, 0, None) == 0
+    assert lib.mxfp8_linear(None, 4, wp, None, A, A, 1 << 20, None) == 1
+    assert lib.mxfp8_linear(A + 8, 4, wp, None, A, A, 1 << 20, None) == 3
+    assert lib.mxfp8_linear(A, 4, wp, None, A + 1, A, 1 << 20, None) == 3
+    assert lib.mxfp8_linear(A, 4, wp, None, A, A, 16, None) == 5
+    assert lib.mxfp8_linear(A, 4, None, None, A, A, 1 << 20, None) == 1
+    # gemm: dense only
+    st2, w2 = _view(mx, 2, 128, 256, A, A)
+    assert st2 == 0
+    assert lib.mxfp8_gemm(A, A, 4, ctypes.byref(w2), None, A, None) == 1
+    assert lib.mxfp8_linear(A, 4, ctypes.byref(w2), None, A, A, 1 << 20, None) == 1
+    # grouped: offsets required
+    assert lib.mxfp8_grouped_linear(A, 4, None, ctypes.byref(w2), None, A, A, 1 << 20, None) == 1
+    assert lib.mxfp8_grouped_linear(A, 0, A, ctypes.byref(w2), None, A, A, 1 << 20, None) == 0
+    # prepare: bad dtype, misaligned source
+    assert lib.mxfp8_prepare_weight(A, 7, wp, None) == 1
+    assert lib.mxfp8_prepare_weight(A + 4, 0, wp, None) == 3

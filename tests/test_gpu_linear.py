@@ -1,0 +1,142 @@
+"""GPU parity: the dense MXFP8 linear layer (quantize + block-scaled GEMM +
+padded-N slice + bias) against the CPU oracle, per element within
+|y - y_ref| <= 8e-3 |y_ref| + 1e-3 rms(y_ref) (see gpu_common)."""
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+import workloads
+from gpu_common import assert_close_to_oracle, oracle_weight, to_dev_bf16, to_dev_f32
+
+pytestmark = pytest.mark.gpu
+
+
+def _run_dense(mx, d, rows=None, schedule=(0, 0)):
+    pw = mx.prepare_weight(to_dev_f32(d.w))
+    x = to_dev_bf16(d.x)
+    b = None if d.bias is None else to_dev_bf16(d.bias)
+    mx.set_schedule(*schedule)
+    try:
+        y = mx.linear(x, pw, b)
+    finally:
+        mx.set_schedule(0, 0)
+    torch.cuda.synchronize()
+    assert y.shape == (d.m, d.n) and y.is_contiguous()
+    wq, wsf = oracle_weight(d.w)
+    y_ref = oracle.linear(d.x, wq, wsf, d.bias, rows=rows)
+    yy = y if rows is None else y[torch.as_tensor(rows, device=y.device)]
+    assert_close_to_oracle(yy, y_ref, d.name)
+    return y, pw
+
+
+def test_tiny_config(lib):
+    _run_dense(lib, workloads.tiny())
+
+
+@pytest.mark.parametrize("m", [1, 16])
+def test_decode_config(lib, m):
+    _run_dense(lib, workloads.decode(m=m))
+
+
+@pytest.mark.parametrize("n,bias", [(2048, False), (130, True)])
+def test_mid_config(lib, n, bias):
+    _run_dense(lib, workloads.mid(n=n, bias=bias))
+
+
+def test_prefill_config_sampled_rows(lib):
+    """8192^3: every column of 48 rows -- the first token tile's edges, the
+    last row, and seeded random rows."""
+    d = workloads.prefill()
+    rng = np.random.default_rng(40)
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, 255, 256, 4095, 8191],
+                                     rng.integers(0, 8192, 40)]))
+    _run_dense(lib, d, rows=rows)
+
+
+@pytest.mark.parametrize("shape", [(1, 130, 256), (7, 256, 512), (128, 130, 768)])
+def test_vllm_shapes_cosine_and_oracle(lib, shape):
+    """The shapes and acceptance criterion of vLLM PR #52204's GPU test:
+    cosine similarity > 0.98 against the unquantized product, output shape
+    (m, n) and contiguous; plus the oracle tolerance."""
+    m, n, k = shape
+    torch.manual_seed(0)
+    x = torch.randn((m, k), dtype=torch.bfloat16)
+    w = torch.randn((n, k), dtype=torch.bfloat16)
+    pw = lib.prepare_weight(w.cuda())
+    y = lib.linear(x.cuda(), pw)
+    ref = torch.mm(x.float(), w.float().t())
+    cos = F.cosine_similarity(y.float().cpu().flatten(), ref.flatten(), dim=0)
+    assert y.shape == (m, n) and y.is_contiguous()
+    assert cos.item() > 0.98
+    wq, wsf = oracle.quantize_rows(w.float().numpy())
+    assert_close_to_oracle(y, oracle.linear(x.float().numpy(), wq, wsf), "vllm%s" % (shape,))
+
+
+@pytest.mark.parametrize("tt,split", [(16, 1), (16, 4), (32, 2), (64, 1), (64, 8), (128, 1),
+                                      (128, 4), (256, 1)])
+def test_every_schedule(lib, tt, split):
+    """Each token-tile size and split-K factor on a shape with several weight
+    tiles, a ragged N (N_pad > N) and a ragged token tail."""
+    d = workloads.dense(m=300, n=390, k=1024, seed=30, bias=True)
+    _run_dense(lib, d, schedule=(tt, split))
+
+
+@pytest.mark.parametrize("m,n,k", [(1, 128, 256), (2, 130, 256), (17, 384, 512), (33, 260, 1024),
+                                   (100, 1000, 768), (257, 256, 256), (511, 640, 512)])
+def test_ragged_shapes(lib, m, n, k):
+    _run_dense(lib, workloads.dense(m=m, n=n, k=k, seed=m + n + k, bias=(m % 2 == 1)))
+
+
+def test_gemm_matches_linear_bitwise(lib):
+    d = workloads.dense(m=77, n=520, k=512, seed=31)
+    pw = lib.prepare_weight(to_dev_f32(d.w))
+    x = to_dev_bf16(d.x)
+    b = to_dev_bf16(d.bias)
+    y1 = lib.linear(x, pw, b)
+    q, sf = lib.quantize_act(x)
+    y2 = lib.gemm(q, sf, pw, b)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
+
+
+def test_deterministic(lib):
+    d = workloads.decode(m=16)
+    pw = lib.prepare_weight(to_dev_f32(d.w))
+    x = to_dev_bf16(d.x)
+    b = to_dev_bf16(d.bias)
+    ys = [lib.linear(x, pw, b) for _ in range(3)]
+    torch.cuda.synchronize()
+    assert all(torch.equal(ys[0], y) for y in ys[1:])
+
+
+def test_closed_form_all_ones(lib):
+    """x = W = 1: quantization is exact, y = K exactly (a power of two is
+    exact in BF16), plus an exactly representable bias."""
+    for k in (256, 2048):
+        m, n = 20, 200
+        pw = lib.prepare_weight(torch.ones((n, k), dtype=torch.float32, device="cuda"))
+        x = torch.ones((m, k), dtype=torch.bfloat16, device="cuda")
+        y = lib.linear(x, pw)
+        assert torch.equal(y, torch.full((m, n), float(k), dtype=torch.bfloat16, device="cuda"))
+        b = torch.arange(n, device="cuda", dtype=torch.float32).mul(0.5).to(torch.bfloat16)
+        yb = lib.linear(x, pw, b)
+        torch.cuda.synchronize()
+        # K + bias rounded once to BF16
+        ref = (float(k) + b.float()).to(torch.bfloat16).expand(m, n)
+        assert torch.equal(yb, ref)
+
+
+def test_leading_dims_and_m0(lib):
+    d = workloads.dense(m=12, n=256, k=256, seed=32)
+    pw = lib.prepare_weight(to_dev_f32(d.w))
+    x = to_dev_bf16(d.x).reshape(3, 4, 256)
+    y = lib.linear(x, pw, to_dev_bf16(d.bias))
+    assert y.shape == (3, 4, 256)
+    y0 = lib.linear(torch.empty((0, 256), dtype=torch.bfloat16, device="cuda"), pw)
+    assert y0.shape == (0, 256)
+
+
+def test_no_device_timeout_recorded(lib):
+    assert lib.device_error() == 0
