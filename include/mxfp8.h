@@ -167,9 +167,13 @@ int mxfp8_last_cuda_error(void);
  * device.  Returns MXFP8_OK or MXFP8_ERR_DEVICE_TIMEOUT. */
 mxfp8_status mxfp8_device_error(void);
 
-/* Testing hook: pin the GEMM schedule.  tokens_per_tile in {0 (automatic),
- * 16, 32, 64, 128, 256}; split_k in {0 (automatic), 1..8}.  Process-wide. */
-void mxfp8_set_schedule(int tokens_per_tile, int split_k);
+/* Testing hook: pin the GEMM schedule, process-wide.
+ * tokens_per_tile: 0 (automatic) or 16, 32, 64, 128, 256 (256 needs split_k -1);
+ * split_k: 0 automatic, -1 persistent tiles, 1..8 one tile per cluster of
+ * split_k CTAs (K split among them, tokens_per_tile <= 128);
+ * fuse_quant: -1 automatic, 0 never, 1 whenever the schedule allows
+ * (one-tile schedules of mxfp8_linear) -- the GEMM then quantizes x itself. */
+void mxfp8_set_schedule(int tokens_per_tile, int split_k, int fuse_quant);
 
 #ifdef __cplusplus
 }

@@ -89,7 +89,7 @@ def library():
         "mxfp8_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "mxfp8_last_cuda_error": (ctypes.c_int, []),
         "mxfp8_device_error": (ctypes.c_int, []),
-        "mxfp8_set_schedule": (None, [ctypes.c_int, ctypes.c_int]),
+        "mxfp8_set_schedule": (None, [ctypes.c_int, ctypes.c_int, ctypes.c_int]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -243,9 +243,11 @@ def grouped_linear(x_sorted: torch.Tensor, offsets: torch.Tensor, pw: PreparedWe
 
 
 # ------------------------------------------------------------------ hooks
-def set_schedule(tokens_per_tile: int = 0, split_k: int = 0) -> None:
-    """Pin the GEMM schedule (testing/benchmarking); 0 = automatic."""
-    library().mxfp8_set_schedule(int(tokens_per_tile), int(split_k))
+def set_schedule(tokens_per_tile: int = 0, split_k: int = 0, fuse_quant: int = -1) -> None:
+    """Pin the GEMM schedule (testing/benchmarking).  tokens_per_tile 0 = auto;
+    split_k 0 = auto, -1 = persistent, >0 = one tile per cluster of split_k
+    CTAs; fuse_quant -1 = auto, 0 = off, 1 = on where possible."""
+    library().mxfp8_set_schedule(int(tokens_per_tile), int(split_k), int(fuse_quant))
 
 
 def device_error() -> int:

@@ -18,6 +18,7 @@ namespace {
 thread_local int t_last_cuda_error = 0;
 int g_force_tt = 0;
 int g_force_split = 0;
+int g_force_fuse = -1;
 
 struct DeviceInfo {
     int checked;  // 0 unknown, 1 supported, -1 unsupported
@@ -136,9 +137,8 @@ mxfp8_status mxfp8_quantize_act(const void* x, int64_t m, int64_t k, void* q, vo
     return e == cudaSuccess ? MXFP8_OK : cuda_fail(e);
 }
 
-static mxfp8_status run_gemm(const void* qa, const void* sfa, int64_t m, const mxfp8_weight* w,
-                             const void* bias, void* y, const int32_t* offsets, bool after_quant,
-                             int sms, cudaStream_t s) {
+static mxk::GemmProblem make_problem(const void* qa, const void* sfa, int64_t m, const mxfp8_weight* w,
+                                     const void* bias, void* y, const int32_t* offsets, const void* x) {
     mxk::GemmProblem p;
     p.qa = static_cast<const uint8_t*>(qa);
     p.sfa = static_cast<const uint8_t*>(sfa);
@@ -152,10 +152,11 @@ static mxfp8_status run_gemm(const void* qa, const void* sfa, int64_t m, const m
     p.bias = bias;
     p.y = y;
     p.offsets = offsets;
-    p.after_quant = after_quant;
-    const mxk::GemmSchedule sch = mxk::choose_schedule(p, sms, g_force_tt, g_force_split);
-    bool enc_fail = false;
-    cudaError_t e = mxk::launch_gemm(p, sch, sms, s, &enc_fail);
+    p.x = x;
+    return p;
+}
+
+static mxfp8_status launch_status(cudaError_t e, bool enc_fail) {
     if (enc_fail) return MXFP8_ERR_INVALID_ARG;
     return e == cudaSuccess ? MXFP8_OK : cuda_fail(e);
 }
@@ -172,7 +173,11 @@ mxfp8_status mxfp8_gemm(const void* qa, const void* sfa, int64_t m, const mxfp8_
         return MXFP8_ERR_MISALIGNED;
     int sms = 0;
     if ((st = device_sms(&sms)) != MXFP8_OK) return st;
-    return run_gemm(qa, sfa, m, w, bias, y, nullptr, false, sms, static_cast<cudaStream_t>(stream));
+    const mxk::GemmProblem p = make_problem(qa, sfa, m, w, bias, y, nullptr, nullptr);
+    const mxk::GemmSchedule sch = mxk::choose_schedule(p, sms, g_force_tt, g_force_split, g_force_fuse);
+    bool enc_fail = false;
+    cudaError_t e = mxk::launch_gemm(p, sch, sms, static_cast<cudaStream_t>(stream), &enc_fail);
+    return launch_status(e, enc_fail);
 }
 
 static mxfp8_status linear_common(const void* x, int64_t m, const int32_t* offsets,
@@ -192,9 +197,17 @@ static mxfp8_status linear_common(const void* x, int64_t m, const int32_t* offse
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t* qa = static_cast<uint8_t*>(workspace);
     uint8_t* sfa = qa + ceil_to(m * w->k, 256);
-    cudaError_t e = mxk::launch_quant_act(x, m, w->k, qa, sfa, sms, s);
-    if (e != cudaSuccess) return cuda_fail(e);
-    return run_gemm(qa, sfa, m, w, bias, y, offsets, true, sms, s);
+    // Small M: the GEMM quantizes its own K slices of x (no separate launch,
+    // the workspace stays unused).  Otherwise quantize into the workspace.
+    const mxk::GemmProblem p = make_problem(qa, sfa, m, w, bias, y, offsets, offsets ? nullptr : x);
+    const mxk::GemmSchedule sch = mxk::choose_schedule(p, sms, g_force_tt, g_force_split, g_force_fuse);
+    if (!sch.fuse_quant) {
+        cudaError_t e = mxk::launch_quant_act(x, m, w->k, qa, sfa, sms, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    bool enc_fail = false;
+    cudaError_t e = mxk::launch_gemm(p, sch, sms, s, &enc_fail);
+    return launch_status(e, enc_fail);
 }
 
 mxfp8_status mxfp8_linear(const void* x, int64_t m, const mxfp8_weight* w, const void* bias, void* y,
@@ -236,11 +249,12 @@ mxfp8_status mxfp8_device_error(void) {
     return v ? MXFP8_ERR_DEVICE_TIMEOUT : MXFP8_OK;
 }
 
-void mxfp8_set_schedule(int tokens_per_tile, int split_k) {
+void mxfp8_set_schedule(int tokens_per_tile, int split_k, int fuse_quant) {
     const bool tt_ok = tokens_per_tile == 0 || tokens_per_tile == 16 || tokens_per_tile == 32 ||
                        tokens_per_tile == 64 || tokens_per_tile == 128 || tokens_per_tile == 256;
     g_force_tt = tt_ok ? tokens_per_tile : 0;
-    g_force_split = (split_k >= 0 && split_k <= 8) ? split_k : 0;
+    g_force_split = (split_k >= -1 && split_k <= 8) ? split_k : 0;
+    g_force_fuse = (fuse_quant >= -1 && fuse_quant <= 1) ? fuse_quant : -1;
 }
 
 }  // extern "C"

@@ -9,28 +9,42 @@
 // tile) and the tokens its B operand (N = 16..256 tokens per tile): the
 // accumulator D^T[n, token] lives in TMEM with one weight row per lane.  This
 // is why N is padded to 128 and why the small-M case needs no padding of the
-// token count beyond 16 (the "shuffling for transposed MMA outputs" of
-// FlashInfer PR #1214 names the same choice).
+// token count beyond 16 (FlashInfer PR #1214 names the same choice:
+// "shuffling for transposed MMA outputs").
 //
-// Per CTA (320 threads, 10 warps):
+// Per CTA (352 threads, 11 warps):
 //   warp 0      TMA producer: per 128-wide K block, one 128x128 weight tile,
-//               the token tile (TMA boxes of <= 32 rows), the weight scales
-//               (one 512-byte bulk copy, already in TMEM-copy order) and the
-//               raw 8x4 activation-scale groups (one TMA box).
-//   warp 1      TMEM allocator and MMA issuer: re-orders the activation scales
-//               into the 32x16-byte TMEM-copy order in shared memory, copies
+//               the weight scales (one 512-byte bulk copy, already in
+//               TMEM-copy order) and -- unless quantization is fused -- the
+//               token tile (TMA boxes of <= 32 rows) and the raw 8x4
+//               activation-scale groups (one TMA box).
+//   warp 1      TMEM allocator; its lane 0 alone is the MMA issuer: copies
 //               both scale tiles into TMEM (tcgen05.cp 32x128b.warpx4), issues
 //               four tcgen05.mma kind::mxf8f6f4 block_scale (K = 32 each) and
-//               commits the stage back to the producer.
+//               commits the stage back to the producer.  The issue path holds no
+//               warp-wide synchronisation: its cost per stage bounds the whole
+//               kernel at small N.
 //   warps 2..9  epilogue: two warps per TMEM lane quadrant, each half of the
 //               token columns; tcgen05.ld, release the accumulator, then
 //               + bias, BF16 rounding and masked stores (j < N, token < M).
+//               With fused quantization they first quantize the BF16 token
+//               rows of each K block straight into the swizzled B tile and
+//               the TMEM-copy scale order (same arithmetic as quant.cu).
+//   warp 10     scale re-order (unfused only): token j of the raw 8x4 groups
+//               goes to word (j%32)*4 + (j%128)/32 of its 128-token chunk,
+//               the order tcgen05.cp 32x128b.warpx4 expects.
 // Schedules:
-//   split_k == 1  persistent: grid <= #SMs, tiles strided over CTAs.
-//   split_k  > 1  a cluster of split_k CTAs per tile, each a K range; FP32
-//                 partials meet in distributed shared memory and are summed in
-//                 rank order (deterministic), each rank finishing a slice of
-//                 the tokens.
+//   persistent   grid <= #SMs x occupancy, tiles strided over CTAs (large M,
+//                grouped).
+//   one tile     one output tile per cluster of `splits` CTAs, each a K range
+//                (small M).  With splits > 1 every rank pushes its FP32
+//                partials into the owning rank's shared memory (DSMEM stores),
+//                one cluster barrier, and each owner sums its token slice in
+//                rank order (deterministic).
+// Programmatic dependent launch: the kernel lets the next grid start at once;
+// it reads nothing a previous grid may write before griddepcontrol.wait,
+// except the weights, their scales and the grouped offsets, which are written
+// before the layer's first kernel.
 // Every wait is bounded (kWaitNs); a timeout sets g_gemm_error, every role
 // unwinds, in-flight copies and MMAs are drained (again bounded), TMEM is
 // freed and the kernel returns.
@@ -42,6 +56,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "quant_block.cuh"
 
 namespace mxk {
 
@@ -51,7 +66,7 @@ namespace {
 
 constexpr uint64_t kWaitNs = 4000000000ull;   // 4 s per wait, then give up
 constexpr uint64_t kDrainNs = 200000000ull;   // 0.2 s per drain wait
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kEpilogueWarps = 8;
 constexpr int kMaxExperts = 1024;
 
@@ -63,11 +78,12 @@ struct GemmArgs {
     const __nv_bfloat16* bias;
     __nv_bfloat16* y;
     const int32_t* offsets;  // grouped segment offsets, or null (dense)
-    int m, n, n_pad, kq;     // kq = k / 128
+    const __nv_bfloat16* x;  // fused quantization: BF16 activations [m, k], else null
+    int m, n, n_pad, k, kq;  // kq = k / 128
     int experts, n_tiles;
     int box_rows, sf_groups;
-    int stages, splits;
-    int num_tiles;           // dense only (grouped counts tiles on the device)
+    int stages, splits, persistent;
+    int num_tiles;           // dense (grouped counts tiles on the device)
     uint32_t tmem_cols;
 };
 
@@ -81,8 +97,11 @@ struct Geometry {
     static constexpr int kOffAsfT = kOffAsfRaw + 1152;            // 36 groups x 32 B max
     static constexpr int kStageBytes = ((kOffAsfT + 512 * kSfChunks) + 1023) / 1024 * 1024;
     static constexpr int kSfSlotCols = 4 + 4 * kSfChunks;         // TMEM columns per stage
-    static constexpr int kPartialBytes = 128 * TT * 4;
 };
+
+__host__ __device__ constexpr int tokens_per_owner(int tt, int splits) {
+    return (tt + splits - 1) / splits;
+}
 
 struct TileInfo {
     int e, n_tile, tok0, count;
@@ -129,26 +148,40 @@ __device__ __forceinline__ void record_timeout(volatile uint32_t* abort_flag) {
     *abort_flag = 1u;
 }
 
+__device__ __forceinline__ void st_shared_v2(void* p, uint2 v) {
+    asm volatile("st.shared.v2.u32 [%0], {%1,%2};" ::"r"(smem_addr(p)), "r"(v.x), "r"(v.y) : "memory");
+}
+
+// Small token tiles keep registers low enough for two CTAs per SM.
 template <int TT>
-__global__ void __launch_bounds__(kThreads, 1) mxfp8_gemm_kernel(const __grid_constant__ GemmArgs p) {
+__global__ void __launch_bounds__(kThreads, (TT <= 64 ? 2 : 1)) mxfp8_gemm_kernel(const __grid_constant__ GemmArgs p) {
     using G = Geometry<TT>;
     extern __shared__ uint8_t smem_dyn[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~static_cast<uintptr_t>(1023));
 
+    // Dependent grids may launch now; they wait for this grid before reading
+    // anything it writes.
+    pdl_launch_dependents();
+
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int stages = p.stages;
-    const bool split = p.splits > 1;
+    const int splits = p.splits;
+    const bool reduce = splits > 1;
+    const bool fused = p.x != nullptr;
+    const int per = tokens_per_owner(TT, splits);
 
-    uint8_t* partial = smem + stages * G::kStageBytes;  // split-K partials [TT][128] f32
-    uint8_t* ctrl = partial + (split ? G::kPartialBytes : 0);
+    uint8_t* partial = smem + stages * G::kStageBytes;  // split-K partials [splits][per][128] f32
+    uint8_t* ctrl = partial + (reduce ? splits * per * 512 : 0);
     uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
     uint64_t* empty = full + stages;
     uint64_t* acc_full = empty + stages;
     uint64_t* acc_empty = acc_full + 1;
     uint64_t* drain = acc_empty + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* sfraw = drain + 1;          // raw activation scales landed
+    uint64_t* sfok = sfraw + stages;      // re-ordered scales written
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sfok + stages);
     volatile uint32_t* abort_flag = tmem_slot + 1;
     int* prefix = reinterpret_cast<int*>(tmem_slot + 2);   // [experts + 1]
     int* offs = prefix + (kMaxExperts + 1);                 // [experts + 1]
@@ -156,11 +189,15 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp8_gemm_kernel(const __grid_co
     // ---------------------------------------------------------------- setup
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&p.map_w);
-        tma_prefetch_desc(&p.map_a);
-        tma_prefetch_desc(&p.map_asf);
+        if (!fused) {
+            tma_prefetch_desc(&p.map_a);
+            tma_prefetch_desc(&p.map_asf);
+        }
         for (int s = 0; s < stages; ++s) {
-            mbar_init(&full[s], 1);
+            mbar_init(&full[s], fused ? 1 + kEpilogueWarps : 1);
             mbar_init(&empty[s], 1);
+            mbar_init(&sfraw[s], 1);
+            mbar_init(&sfok[s], 1);
         }
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, kEpilogueWarps);
@@ -200,16 +237,20 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp8_gemm_kernel(const __grid_co
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // Peers must have started before any DSMEM store: arrive now, wait just
+    // before the first remote access.
+    if (reduce) cluster_arrive_relaxed();
+    bool cluster_waited = false;
 
     // Work assignment: a list of (tile, K range).
-    int tile_first, tile_stride, num_tiles, kb_begin, kb_end;
-    if (split) {
-        const int r = static_cast<int>(cluster_rank());
-        tile_first = static_cast<int>(cluster_id_x());
+    int tile_first, tile_stride, num_tiles, kb_begin, kb_end, rank = 0;
+    if (!p.persistent) {
+        rank = reduce ? static_cast<int>(cluster_rank()) : 0;
+        tile_first = reduce ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
         tile_stride = 1 << 30;
         num_tiles = tile_first + 1;
-        kb_begin = (r * p.kq) / p.splits;
-        kb_end = ((r + 1) * p.kq) / p.splits;
+        kb_begin = (rank * p.kq) / splits;
+        kb_end = ((rank + 1) * p.kq) / splits;
     } else {
         tile_first = blockIdx.x;
         tile_stride = gridDim.x;
@@ -223,22 +264,19 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp8_gemm_kernel(const __grid_co
         if (lane == 0) {
             const uint64_t pol_w = policy_evict_normal();
             const uint64_t pol_a = policy_evict_last();
-            int job = 0;
             // Weight bytes of the first `stages` jobs are issued before waiting
-            // for the activation quantizer (programmatic dependent launch):
-            // only the activations and their scales depend on it.
+            // for the previous grid: only the activations depend on it.
             int pre = 0;
             {
                 int t = tile_first;
                 for (; pre < stages && t < num_tiles;) {
                     const TileInfo ti = decode_tile<TT>(t, p, prefix, offs);
+                    const int nloads = (ti.count + p.box_rows - 1) / p.box_rows;
+                    const uint32_t bytes = 16384u + 512u +
+                        (fused ? 0u : static_cast<uint32_t>(nloads * p.box_rows * 128));
                     for (int kb = kb_begin; kb < kb_end && pre < stages; ++kb, ++pre) {
                         const int s = pre;
                         uint8_t* st = smem + s * G::kStageBytes;
-                        const int nloads = (ti.count + p.box_rows - 1) / p.box_rows;
-                        const uint32_t bytes = 16384u + 512u +
-                                               static_cast<uint32_t>(nloads * p.box_rows * 128) +
-                                               static_cast<uint32_t>(p.sf_groups * 32);
                         mbar_arrive_expect_tx(&full[s], bytes);
                         tma_load_2d(st + G::kOffW, &p.map_w, kb * 128,
                                     ti.e * p.n_pad + ti.n_tile * 128, &full[s], pol_w);
@@ -249,33 +287,33 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp8_gemm_kernel(const __grid_co
                     if (pre < stages) t += tile_stride;
                 }
             }
-            pdl_wait();
-            {
+            if (!fused) {
+                pdl_wait();
                 int t = tile_first, issued = 0;
                 for (; issued < pre;) {
                     const TileInfo ti = decode_tile<TT>(t, p, prefix, offs);
+                    const int nloads = (ti.count + p.box_rows - 1) / p.box_rows;
                     for (int kb = kb_begin; kb < kb_end && issued < pre; ++kb, ++issued) {
                         const int s = issued;
                         uint8_t* st = smem + s * G::kStageBytes;
-                        const int nloads = (ti.count + p.box_rows - 1) / p.box_rows;
                         for (int l = 0; l < nloads; ++l)
                             tma_load_2d(st + G::kOffA + l * p.box_rows * 128, &p.map_a, kb * 128,
                                         ti.tok0 + l * p.box_rows, &full[s], pol_a);
-                        tma_load_2d(st + G::kOffAsfRaw, &p.map_asf, kb * 32, ti.tok0 >> 3, &full[s],
+                        mbar_arrive_expect_tx(&sfraw[s], static_cast<uint32_t>(p.sf_groups * 32));
+                        tma_load_2d(st + G::kOffAsfRaw, &p.map_asf, kb * 32, ti.tok0 >> 3, &sfraw[s],
                                     pol_a);
                     }
                     t += tile_stride;
                 }
             }
             // Steady state.
-            job = 0;
+            int job = 0;
             bool stop = false;
             for (int t = tile_first; t < num_tiles && !stop; t += tile_stride) {
                 const TileInfo ti = decode_tile<TT>(t, p, prefix, offs);
                 const int nloads = (ti.count + p.box_rows - 1) / p.box_rows;
                 const uint32_t bytes = 16384u + 512u +
-                                       static_cast<uint32_t>(nloads * p.box_rows * 128) +
-                                       static_cast<uint32_t>(p.sf_groups * 32);
+                    (fused ? 0u : static_cast<uint32_t>(nloads * p.box_rows * 128));
                 for (int kb = kb_begin; kb < kb_end; ++kb, ++job) {
                     if (job < pre) continue;
                     if (*abort_flag) { stop = true; break; }
@@ -293,91 +331,177 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp8_gemm_kernel(const __grid_co
                     bulk_load(st + G::kOffWsf,
                               p.wsf + ((static_cast<size_t>(ti.e) * p.n_tiles + ti.n_tile) * p.kq + kb) * 512,
                               512, &full[s], pol_w);
-                    for (int l = 0; l < nloads; ++l)
-                        tma_load_2d(st + G::kOffA + l * p.box_rows * 128, &p.map_a, kb * 128,
-                                    ti.tok0 + l * p.box_rows, &full[s], pol_a);
-                    tma_load_2d(st + G::kOffAsfRaw, &p.map_asf, kb * 32, ti.tok0 >> 3, &full[s], pol_a);
+                    if (!fused) {
+                        for (int l = 0; l < nloads; ++l)
+                            tma_load_2d(st + G::kOffA + l * p.box_rows * 128, &p.map_a, kb * 128,
+                                        ti.tok0 + l * p.box_rows, &full[s], pol_a);
+                        mbar_arrive_expect_tx(&sfraw[s], static_cast<uint32_t>(p.sf_groups * 32));
+                        tma_load_2d(st + G::kOffAsfRaw, &p.map_asf, kb * 32, ti.tok0 >> 3, &sfraw[s], pol_a);
+                    }
                 }
             }
             // Drain: the last use of each stage must have landed before exit.
             const int issued_jobs = job > pre ? job : pre;
-            for (int j = issued_jobs - 1; j >= 0 && j >= issued_jobs - stages; --j)
+            for (int j = issued_jobs - 1; j >= 0 && j >= issued_jobs - stages; --j) {
                 (void)mbar_wait(&full[j % stages], (j / stages) & 1, kDrainNs);
+                if (!fused) (void)mbar_wait(&sfraw[j % stages], (j / stages) & 1, kDrainNs);
+            }
         }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
-        int job = 0, tile_iter = 0;
-        bool stop = false;
-        for (int t = tile_first; t < num_tiles && !stop; t += tile_stride, ++tile_iter) {
-            const TileInfo ti = decode_tile<TT>(t, p, prefix, offs);
-            const uint32_t n_mma = static_cast<uint32_t>((ti.count + 15) & ~15);
-            const int off8 = ti.tok0 & 7;
-            if (tile_iter > 0) {
-                bool ok = true;
-                if (lane == 0) ok = mbar_wait(acc_empty, (tile_iter - 1) & 1, kWaitNs);
-                ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
-                if (!ok) { if (lane == 0) record_timeout(abort_flag); break; }
-            }
-            for (int kb = kb_begin; kb < kb_end; ++kb, ++job) {
-                const int s = job % stages;
-                bool ok = mbar_wait(&full[s], (job / stages) & 1, kWaitNs);
-                ok = __all_sync(0xFFFFFFFFu, ok ? 1 : 0) != 0;
-                if (!ok || *abort_flag) {
-                    if (lane == 0 && !ok) record_timeout(abort_flag);
-                    stop = true;
+        if (lane == 0) {
+            // Descriptors of stage 0; stage s adds s * kStageBytes (the start
+            // address field is address >> 4 and never carries: smem < 256 KB).
+            const uint64_t a_desc0 = desc_kmajor_sw128(smem_addr(smem + G::kOffW));
+            const uint64_t b_desc0 = desc_kmajor_sw128(smem_addr(smem + G::kOffA));
+            const uint64_t wsf_desc0 = desc_sf_32x16(smem_addr(smem + G::kOffWsf));
+            const uint64_t asf_desc0 = desc_sf_32x16(smem_addr(smem + G::kOffAsfT));
+            constexpr uint64_t kStageStep = static_cast<uint64_t>(G::kStageBytes >> 4);
+            int s = 0;
+            uint32_t phase = 0;
+            int tile_iter = 0;
+            bool stop = false;
+            for (int t = tile_first; t < num_tiles && !stop; t += tile_stride, ++tile_iter) {
+                const TileInfo ti = decode_tile<TT>(t, p, prefix, offs);
+                const uint32_t n_mma = static_cast<uint32_t>((ti.count + 15) & ~15);
+                uint32_t idesc[4];
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) idesc[kk] = idesc_mxf8(128, n_mma, kk, kk);
+                if (tile_iter > 0 && !mbar_wait(acc_empty, (tile_iter - 1) & 1, kWaitNs)) {
+                    record_timeout(abort_flag);
                     break;
                 }
-                uint8_t* st = smem + s * G::kStageBytes;
-                // Activation scales: token j of the tile is word (off8 + j) of
-                // the raw 8x4 groups; the TMEM-copy order puts token j of each
-                // 128-chunk at word (j%32)*4 + (j%128)/32.
-                const uint32_t* raw = reinterpret_cast<const uint32_t*>(st + G::kOffAsfRaw);
-#pragma unroll
-                for (int c = 0; c < G::kSfChunks; ++c) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int jq = 0; jq < 4; ++jq) {
-                        const int j = c * 128 + jq * 32 + lane;
-                        w[jq] = (j < TT) ? raw[off8 + j] : 0u;
+                for (int kb = kb_begin; kb < kb_end; ++kb) {
+                    if (!mbar_wait(&full[s], phase, kWaitNs) ||
+                        (!fused && !mbar_wait(&sfok[s], phase, kWaitNs))) {
+                        record_timeout(abort_flag);
+                        stop = true;
+                        break;
                     }
-                    *reinterpret_cast<uint4*>(st + G::kOffAsfT + c * 512 + lane * 16) =
-                        make_uint4(w[0], w[1], w[2], w[3]);
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
                     tc_fence_after();
+                    const uint64_t sd = static_cast<uint64_t>(s) * kStageStep;
                     const uint32_t sfa = tmem_base + TT + s * G::kSfSlotCols;
                     const uint32_t sfb = sfa + 4;
-                    tmem_copy_sf(sfa, desc_sf_32x16(smem_addr(st + G::kOffWsf)));
+                    tmem_copy_sf(sfa, wsf_desc0 + sd);
 #pragma unroll
-                    for (int c = 0; c < G::kSfChunks; ++c)
-                        tmem_copy_sf(sfb + 4 * c, desc_sf_32x16(smem_addr(st + G::kOffAsfT + c * 512)));
-                    const uint32_t a_base = smem_addr(st + G::kOffW);
-                    const uint32_t b_base = smem_addr(st + G::kOffA);
+                    for (int c = 0; c < G::kSfChunks; ++c) tmem_copy_sf(sfb + 4 * c, asf_desc0 + sd + c * 32);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint32_t idesc = idesc_mxf8(128, n_mma, kk, kk);
-                        mma_mxf8(tmem_base, desc_kmajor_sw128(a_base + kk * 32),
-                                 desc_kmajor_sw128(b_base + kk * 32), idesc, sfa, sfb,
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_mxf8(tmem_base, a_desc0 + sd + 2 * kk, b_desc0 + sd + 2 * kk, idesc[kk], sfa, sfb,
                                  (kb > kb_begin || kk > 0) ? 1u : 0u);
-                    }
                     mma_commit(&empty[s]);
                     if (kb == kb_end - 1) mma_commit(acc_full);
+                    if (++s == stages) { s = 0; phase ^= 1u; }
                 }
-                __syncwarp();
             }
-        }
-        // Drain every MMA this thread issued before TMEM is released.
-        if (lane == 0) {
+            // Drain every MMA this thread issued before TMEM is released.
             mma_commit(drain);
             (void)mbar_wait(drain, 0, kDrainNs);
         }
         __syncwarp();
+    } else if (warp == 10) {
+        // ------------------------------------------- activation-scale reorder
+        if (!fused) {
+            int s = 0;
+            uint32_t phase = 0;
+            bool stop = false;
+            for (int t = tile_first; t < num_tiles && !stop; t += tile_stride) {
+                const TileInfo ti = decode_tile<TT>(t, p, prefix, offs);
+                const int off8 = ti.tok0 & 7;
+                for (int kb = kb_begin; kb < kb_end; ++kb) {
+                    bool ok = mbar_wait(&sfraw[s], phase, kWaitNs);
+                    ok = __all_sync(0xFFFFFFFFu, ok ? 1 : 0) != 0;
+                    if (!ok) {
+                        if (lane == 0) record_timeout(abort_flag);
+                        stop = true;
+                        break;
+                    }
+                    uint8_t* st = smem + s * G::kStageBytes;
+                    const uint32_t* raw = reinterpret_cast<const uint32_t*>(st + G::kOffAsfRaw);
+#pragma unroll
+                    for (int c = 0; c < G::kSfChunks; ++c) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int jq = 0; jq < 4; ++jq) {
+                            const int j = c * 128 + jq * 32 + lane;
+                            w[jq] = (j < TT) ? raw[off8 + j] : 0u;
+                        }
+                        *reinterpret_cast<uint4*>(st + G::kOffAsfT + c * 512 + lane * 16) =
+                            make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sfok[s]);
+                    if (++s == stages) { s = 0; phase ^= 1u; }
+                }
+            }
+        }
+        __syncwarp();
     } else {
+        const int ew = warp - 2;  // warps 2..9
+        // ---------------------------------------- fused activation quantizer
+        if (fused) {
+            // One tile per CTA.  Each pass of a warp quantizes 8 (row, block)
+            // pairs: lanes 4g..4g+3 hold the 32 values of one block.  Passes
+            // of all K blocks are flattened and their loads issued in batches
+            // of 8 before any is quantized.
+            pdl_wait();
+            const TileInfo ti = decode_tile<TT>(tile_first, p, prefix, offs);
+            constexpr int kPasses = TT / 16;  // passes per K block per warp
+            const int total = (kb_end - kb_begin) * kPasses;
+            bool ok = true;
+            for (int p0 = 0; p0 < total && ok; p0 += 8) {
+                uint4 raw[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int ps = p0 + u;
+                    const int job = ps / kPasses;
+                    const int pr = ((ps - job * kPasses) * kEpilogueWarps + ew) * 8 + (lane >> 2);
+                    const int row = pr >> 2;
+                    const int col = (kb_begin + job) * 128 + (pr & 3) * 32 + (lane & 3) * 8;
+                    raw[u] = make_uint4(0, 0, 0, 0);
+                    if (ps < total && row < ti.count)
+                        raw[u] = *reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(ti.tok0 + row) * p.k + col);
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int ps = p0 + u;
+                    if (ps >= total) break;  // warp-uniform
+                    const int job = ps / kPasses;
+                    const int pass = ps - job * kPasses;
+                    const int s = job % stages;
+                    if (pass == 0 && job >= stages) {
+                        ok = mbar_wait(&empty[s], ((job / stages) & 1) ^ 1, kWaitNs);
+                        ok = __all_sync(0xFFFFFFFFu, ok ? 1 : 0) != 0;
+                        if (!ok) { if (lane == 0) record_timeout(abort_flag); break; }
+                    }
+                    uint8_t* st = smem + s * G::kStageBytes;
+                    const int pr = (pass * kEpilogueWarps + ew) * 8 + (lane >> 2);
+                    const int row = pr >> 2;
+                    const int byte = (pr & 3) * 32 + (lane & 3) * 8;  // within the 128-byte K block
+                    float v[8];
+                    bf16x8_to_float(raw[u], v);
+                    uint2 q8;
+                    uint32_t sc;
+                    quantize_lane8(v, q8, sc);
+                    const int chunk = byte >> 4;  // 128-byte swizzle: chunk ^= row % 8
+                    st_shared_v2(st + G::kOffA + row * 128 + ((chunk ^ (row & 7)) << 4) + (byte & 15), q8);
+                    const uint32_t word = gather_scale_word(sc);
+                    if ((lane & 15) == 0) {
+                        const int rr = row & 127;
+                        *reinterpret_cast<uint32_t*>(st + G::kOffAsfT + (row >> 7) * 512 + (rr & 31) * 16 +
+                                                     (rr >> 5) * 4) = word;
+                    }
+                    if (pass == kPasses - 1) {
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&full[s]);
+                    }
+                }
+            }
+        }
         // ------------------------------------------------------- epilogue
-        const int ew = warp - 2;
         const int quad = warp & 3;             // TMEM lanes [32*quad, 32*quad + 32)
         const int half = ew >> 2;              // token columns [half*TT/2, (half+1)*TT/2)
         constexpr int kCols = TT / 2;
@@ -399,14 +523,16 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp8_gemm_kernel(const __grid_co
 #pragma unroll
                     for (int i = 0; i < 32; ++i) acc[c * 32 + i] = r[i];
                 }
+            } else if constexpr (kCols == 16) {
+                uint32_t r[16];
+                tmem_load_16(taddr, r);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) acc[i] = r[i];
             } else {
+                uint32_t r[8];
+                tmem_load_8(taddr, r);
 #pragma unroll
-                for (int c = 0; c < kCols / 8; ++c) {
-                    uint32_t r[8];
-                    tmem_load_8(taddr + c * 8, r);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) acc[c * 8 + i] = r[i];
-                }
+                for (int i = 0; i < 8; ++i) acc[i] = r[i];
             }
             tmem_load_wait();
             tc_fence_before();
@@ -414,10 +540,20 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp8_gemm_kernel(const __grid_co
             if (lane == 0) mbar_arrive(acc_empty);
 
             const int nl = quad * 32 + lane;  // weight row within the tile
-            if (split) {
-                float* part = reinterpret_cast<float*>(partial);
+            if (reduce) {
+                // Push: token column c goes to rank c / per, slot [rank][c % per].
+                __syncwarp();
+                cluster_wait();
+                cluster_waited = true;
+                const uint32_t pbase = smem_addr(partial);
 #pragma unroll
-                for (int j = 0; j < kCols; ++j) part[(col0 + j) * 128 + nl] = __uint_as_float(acc[j]);
+                for (int j = 0; j < kCols; ++j) {
+                    const int c = col0 + j;
+                    const int owner = c / per;
+                    const int jj = c - owner * per;
+                    const uint32_t a = pbase + static_cast<uint32_t>(((rank * per + jj) * 128 + nl) * 4);
+                    st_cluster_f32(map_to_rank(a, static_cast<uint32_t>(owner)), __uint_as_float(acc[j]));
+                }
             } else {
                 const int n = ti.n_tile * 128 + nl;
                 if (n < p.n) {
@@ -434,30 +570,30 @@ __global__ void __launch_bounds__(kThreads, 1) mxfp8_gemm_kernel(const __grid_co
     }
 
     // ------------------------------------------------- split-K reduction
-    if (split) {
-        cluster_sync();  // every rank's partial tile is in its shared memory
-        if (warp >= 2 && !*abort_flag) {
-            const TileInfo ti = decode_tile<TT>(tile_first, p, prefix, offs);
-            const int rank = static_cast<int>(cluster_rank());
-            const int per = (TT + p.splits - 1) / p.splits;
+    if (reduce) {
+        const int et = threadIdx.x - 64;
+        const TileInfo ti = decode_tile<TT>(tile_first, p, prefix, offs);
+        const int nl = et & 127;
+        const int n = ti.n_tile * 128 + nl;
+        float b = 0.0f;
+        __syncwarp();
+        if (!__all_sync(0xFFFFFFFFu, cluster_waited ? 1 : 0)) cluster_wait();
+        const bool epi = warp >= 2 && warp < 2 + kEpilogueWarps;
+        if (epi && p.bias && n < p.n) b = __bfloat162float(p.bias[static_cast<size_t>(ti.e) * p.n + n]);
+        cluster_sync();  // every rank's pushes have landed
+        if (epi && !*abort_flag) {
+            const float* part = reinterpret_cast<const float*>(partial);
             const int j0 = rank * per;
-            const int j1 = min(TT, j0 + per);
-            const int et = threadIdx.x - 64;
-            const uint32_t pbase = smem_addr(partial);
-            for (int o = et; o < (j1 - j0) * 128; o += kEpilogueWarps * 32) {
-                const int j = j0 + (o >> 7);
-                const int nl = o & 127;
-                const int n = ti.n_tile * 128 + nl;
-                if (j < ti.count && n < p.n) {
-                    const uint32_t a = pbase + static_cast<uint32_t>((j * 128 + nl) * 4);
+            for (int o = et; o < per * 128; o += kEpilogueWarps * 32) {
+                const int jj = o >> 7;
+                const int j = j0 + jj;
+                if (j < ti.count && j < TT && n < p.n) {
                     float sum = 0.0f;
-                    for (int r = 0; r < p.splits; ++r) sum += ld_cluster_f32(map_to_rank(a, r));
-                    if (p.bias) sum += __bfloat162float(p.bias[static_cast<size_t>(ti.e) * p.n + n]);
-                    p.y[static_cast<size_t>(ti.tok0 + j) * p.n + n] = __float2bfloat16_rn(sum);
+                    for (int r = 0; r < splits; ++r) sum += part[(r * per + jj) * 128 + nl];
+                    p.y[static_cast<size_t>(ti.tok0 + j) * p.n + n] = __float2bfloat16_rn(sum + b);
                 }
             }
         }
-        cluster_sync();  // no CTA leaves while another still reads its partials
     }
 
     // -------------------------------------------------------------- teardown
@@ -509,59 +645,121 @@ uint32_t pow2_cols(int need) {
 }
 
 template <int TT>
-cudaError_t launch_tt(const GemmProblem& pr, int splits, int num_sms, cudaStream_t s,
+struct LaunchPlan {
+    int stages;
+    uint32_t tmem_cols;
+    size_t smem;
+    int partial;
+};
+
+template <int TT>
+LaunchPlan<TT> plan_for(int splits, bool persistent, int kq) {
+    using G = Geometry<TT>;
+    LaunchPlan<TT> lp;
+    // Pipeline depth: as many stages as fit next to the partial buffer and
+    // control block (a one-tile CTA never needs more than its K blocks).
+    const int ctrl = 8 * 64 + 8 + 4 * 2 * (kMaxExperts + 1) + 64;  // barriers, slots, prefix/offsets
+    lp.partial = splits > 1 ? splits * tokens_per_owner(TT, splits) * 512 : 0;
+    const int budget = 227 * 1024 - 1024 - ctrl - lp.partial;
+    int stages = budget / G::kStageBytes;
+    if (stages > 8) stages = 8;
+    if (!persistent) {
+        const int nk = (kq + splits - 1) / splits;
+        if (stages > nk) stages = nk;
+    }
+    lp.stages = stages;
+    lp.tmem_cols = pow2_cols(TT + stages * G::kSfSlotCols);
+    lp.smem = 1024 + static_cast<size_t>(stages) * G::kStageBytes + lp.partial + ctrl;
+    return lp;
+}
+
+// Clusters of `splits` CTAs that can be resident at once (one wave), cached.
+template <int TT>
+int max_active_clusters(int splits, size_t smem, cudaStream_t s) {
+    static int cache[9][64];
+    const int key = static_cast<int>(smem >> 12) & 63;
+    if (cache[splits][key] > 0) return cache[splits][key];
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(splits * 64, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = splits;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaFuncSetAttribute(mxfp8_gemm_kernel<TT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess ||
+        cudaOccupancyMaxActiveClusters(&n, mxfp8_gemm_kernel<TT>, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    cache[splits][key] = n;
+    return n;
+}
+
+template <int TT>
+cudaError_t launch_tt(const GemmProblem& pr, const GemmSchedule& sch, int num_sms, cudaStream_t s,
                       bool* encode_failed) {
     using G = Geometry<TT>;
     GemmArgs a;
     memset(&a, 0, sizeof(a));
     const int64_t m8 = (pr.m + 7) / 8 * 8;
+    const bool fused = sch.fuse_quant && pr.x != nullptr;
     a.box_rows = TT < 32 ? TT : 32;
     a.sf_groups = TT / 8 + 1;
-    bool ok = encode_2d_u8(&a.map_w, pr.wq, pr.k, pr.experts * pr.n_pad, pr.k, 128, 128, true) &&
-              encode_2d_u8(&a.map_a, pr.qa, pr.k, pr.m, pr.k, 128, a.box_rows, true) &&
-              encode_2d_u8(&a.map_asf, pr.sfa, pr.k / 4, m8 / 8, pr.k / 4, 32, a.sf_groups, false);
+    bool ok = encode_2d_u8(&a.map_w, pr.wq, pr.k, pr.experts * pr.n_pad, pr.k, 128, 128, true);
+    if (ok && !fused)
+        ok = encode_2d_u8(&a.map_a, pr.qa, pr.k, pr.m, pr.k, 128, a.box_rows, true) &&
+             encode_2d_u8(&a.map_asf, pr.sfa, pr.k / 4, m8 / 8, pr.k / 4, 32, a.sf_groups, false);
     if (!ok) {
         *encode_failed = true;
         return cudaErrorInvalidValue;
     }
+    const int kq = static_cast<int>(pr.k / 128);
+    const int tok_tiles = static_cast<int>((pr.m + TT - 1) / TT);
+    const int n_tiles = static_cast<int>(pr.n_pad / 128);
+    int splits = sch.persistent ? 1 : sch.split_k;
+    if (!sch.persistent && !sch.split_forced) {
+        // Largest split whose clusters all fit in one wave.
+        const int tiles = n_tiles * tok_tiles;
+        int chosen = 1;
+        for (int c = splits; c > 1; --c) {
+            const LaunchPlan<TT> lp = plan_for<TT>(c, false, kq);
+            if (lp.stages >= 1 && tiles <= max_active_clusters<TT>(c, lp.smem, s)) { chosen = c; break; }
+        }
+        splits = chosen;
+    }
+    const LaunchPlan<TT> lp = plan_for<TT>(splits, sch.persistent, kq);
+    if (lp.stages < 1) return cudaErrorInvalidConfiguration;
+
     a.wsf = pr.wsf;
     a.bias = static_cast<const __nv_bfloat16*>(pr.bias);
     a.y = static_cast<__nv_bfloat16*>(pr.y);
     a.offsets = pr.offsets;
+    a.x = fused ? static_cast<const __nv_bfloat16*>(pr.x) : nullptr;
     a.m = static_cast<int>(pr.m);
     a.n = static_cast<int>(pr.n);
     a.n_pad = static_cast<int>(pr.n_pad);
-    a.kq = static_cast<int>(pr.k / 128);
+    a.k = static_cast<int>(pr.k);
+    a.kq = kq;
     a.experts = static_cast<int>(pr.experts);
-    a.n_tiles = static_cast<int>(pr.n_pad / 128);
+    a.n_tiles = n_tiles;
     a.splits = splits;
-
-    // Pipeline depth: as many stages as fit next to the partial buffer and
-    // control block (the split-K schedule never needs more than its K blocks).
-    const int ctrl = 8 * 64 + 8 + 4 * 2 * (kMaxExperts + 1) + 64;
-    const int partial = splits > 1 ? G::kPartialBytes : 0;
-    const int budget = 227 * 1024 - 1024 - ctrl - partial;
-    int stages = budget / G::kStageBytes;
-    if (stages > 8) stages = 8;
-    if (splits > 1) {
-        const int nk = (a.kq + splits - 1) / splits;
-        if (stages > nk) stages = nk;
-        // small tiles: leave room for a second CTA on the SM
-        if (TT <= 32 && stages > 4) stages = 4;
-    }
-    if (stages < 2) stages = 2;
-    a.stages = stages;
-    a.tmem_cols = pow2_cols(TT + stages * G::kSfSlotCols);
-    const size_t smem = 1024 + static_cast<size_t>(stages) * G::kStageBytes + partial + ctrl;
+    a.persistent = sch.persistent ? 1 : 0;
+    a.stages = lp.stages;
+    a.tmem_cols = lp.tmem_cols;
+    const size_t smem = lp.smem;
 
     cudaError_t err = cudaFuncSetAttribute(mxfp8_gemm_kernel<TT>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;
-    if (splits > 1) {
-        err = cudaFuncSetAttribute(mxfp8_gemm_kernel<TT>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (err != cudaSuccess) return err;
-    }
 
     // TMEM is never oversubscribed: co-resident CTAs x columns <= 512.
     int per_sm = 1;
@@ -571,13 +769,11 @@ cudaError_t launch_tt(const GemmProblem& pr, int splits, int num_sms, cudaStream
     if (static_cast<uint32_t>(per_sm) * a.tmem_cols > 512u) return cudaErrorInvalidConfiguration;
 
     int grid;
-    if (splits > 1) {
-        const int tok_tiles = static_cast<int>((pr.m + TT - 1) / TT);
-        a.num_tiles = a.n_tiles * tok_tiles;
+    if (!sch.persistent) {
+        a.num_tiles = n_tiles * tok_tiles;
         grid = a.num_tiles * splits;
     } else if (pr.offsets == nullptr) {
-        const int tok_tiles = static_cast<int>((pr.m + TT - 1) / TT);
-        a.num_tiles = a.n_tiles * tok_tiles;
+        a.num_tiles = n_tiles * tok_tiles;
         grid = a.num_tiles < num_sms * per_sm ? a.num_tiles : num_sms * per_sm;
     } else {
         a.num_tiles = 0;  // counted on the device from the offsets
@@ -599,11 +795,9 @@ cudaError_t launch_tt(const GemmProblem& pr, int splits, int num_sms, cudaStream
         attrs[na].val.clusterDim.z = 1;
         ++na;
     }
-    if (pr.after_quant) {
-        attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attrs[na].val.programmaticStreamSerializationAllowed = 1;
-        ++na;
-    }
+    attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
     cfg.attrs = attrs;
     cfg.numAttrs = na;
     return cudaLaunchKernelEx(&cfg, mxfp8_gemm_kernel<TT>, a);
@@ -611,8 +805,10 @@ cudaError_t launch_tt(const GemmProblem& pr, int splits, int num_sms, cudaStream
 
 }  // namespace
 
-GemmSchedule choose_schedule(const GemmProblem& p, int num_sms, int force_tt, int force_split) {
+GemmSchedule choose_schedule(const GemmProblem& p, int num_sms, int force_tt, int force_split,
+                             int force_fuse) {
     GemmSchedule sch;
+    const int64_t kq = p.k / 128;
     int tt;
     if (p.offsets != nullptr) {
         // grouped: size the token tile to the mean segment (rounded up)
@@ -622,23 +818,34 @@ GemmSchedule choose_schedule(const GemmProblem& p, int num_sms, int force_tt, in
         tt = p.m <= 16 ? 16 : p.m <= 32 ? 32 : p.m <= 64 ? 64 : p.m <= 128 ? 128 : 256;
     }
     if (force_tt) tt = force_tt;
+    bool persistent = p.offsets != nullptr || tt > 128;
     int split = 1;
-    if (p.offsets == nullptr && tt <= 128) {
+    if (!persistent) {
         const int64_t tiles = (p.n_pad / 128) * ((p.m + tt - 1) / tt);
-        const int64_t kq = p.k / 128;
-        // enough CTAs to cover the SMs, at least two K blocks per CTA
-        int64_t want = (num_sms + tiles - 1) / tiles;
-        if (tt <= 32) want = (2 * num_sms + tiles - 1) / tiles;
+        // enough CTAs to cover the SMs (twice for the small tiles that fit two
+        // per SM), at least two K blocks per CTA
+        int64_t want = ((tt <= 32 ? 2 : 1) * num_sms + tiles - 1) / tiles;
         if (want > 8) want = 8;
         if (want > kq / 2) want = kq / 2;
         if (want < 1) want = 1;
         split = static_cast<int>(want);
     }
-    if (force_split) split = force_split;
-    if (p.offsets != nullptr) split = 1;
-    if (split > p.k / 128) split = static_cast<int>(p.k / 128);
+    if (force_split < 0 && p.offsets == nullptr && tt <= 256) {
+        persistent = true;
+        split = 1;
+    } else if (force_split > 0 && p.offsets == nullptr && tt <= 128) {
+        persistent = false;
+        split = force_split;
+    }
+    if (split > kq) split = static_cast<int>(kq);
+    bool fuse = !persistent && p.x != nullptr && tt <= 64;
+    if (force_fuse == 0) fuse = false;
+    if (force_fuse == 1) fuse = !persistent && p.x != nullptr;
     sch.tokens_per_tile = tt;
-    sch.split_k = split;
+    sch.split_k = persistent ? 1 : split;
+    sch.persistent = persistent;
+    sch.fuse_quant = fuse;
+    sch.split_forced = force_split != 0;
     return sch;
 }
 
@@ -646,11 +853,11 @@ cudaError_t launch_gemm(const GemmProblem& p, const GemmSchedule& sch, int num_s
                         bool* encode_failed) {
     *encode_failed = false;
     switch (sch.tokens_per_tile) {
-        case 16: return launch_tt<16>(p, sch.split_k, num_sms, s, encode_failed);
-        case 32: return launch_tt<32>(p, sch.split_k, num_sms, s, encode_failed);
-        case 64: return launch_tt<64>(p, sch.split_k, num_sms, s, encode_failed);
-        case 128: return launch_tt<128>(p, sch.split_k, num_sms, s, encode_failed);
-        case 256: return launch_tt<256>(p, sch.split_k, num_sms, s, encode_failed);
+        case 16: return launch_tt<16>(p, sch, num_sms, s, encode_failed);
+        case 32: return launch_tt<32>(p, sch, num_sms, s, encode_failed);
+        case 64: return launch_tt<64>(p, sch, num_sms, s, encode_failed);
+        case 128: return launch_tt<128>(p, sch, num_sms, s, encode_failed);
+        case 256: return launch_tt<256>(p, sch, num_sms, s, encode_failed);
         default: return cudaErrorInvalidValue;
     }
 }

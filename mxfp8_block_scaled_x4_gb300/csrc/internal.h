@@ -29,15 +29,21 @@ struct GemmProblem {
     const void* bias;          // bf16 [experts][n] or null
     void* y;                   // bf16 [m][n]
     const int32_t* offsets;    // grouped: device [experts + 1]; dense: null
-    bool after_quant;          // launch as a programmatic dependent of the previous kernel
+    const void* x;             // bf16 [m][k] activations when the GEMM may quantize them itself
 };
 
 struct GemmSchedule {
     int tokens_per_tile;       // 16, 32, 64, 128, 256
-    int split_k;               // 1 = persistent tiles, >1 = cluster split-K
+    int split_k;               // CTAs (a cluster) per output tile, K split among them
+    bool persistent;           // tiles strided over a persistent grid (split_k == 1)
+    bool fuse_quant;           // the GEMM quantizes x itself (one-tile schedules)
+    bool split_forced;         // keep split_k even if the clusters need two waves
 };
 
-GemmSchedule choose_schedule(const GemmProblem& p, int num_sms, int force_tt, int force_split);
+// force_tt: 0 or a token tile; force_split: 0 auto, -1 persistent, >0 split;
+// force_fuse: -1 auto, 0 off, 1 on where possible.
+GemmSchedule choose_schedule(const GemmProblem& p, int num_sms, int force_tt, int force_split,
+                             int force_fuse);
 
 // Returns cudaSuccess or the launch/encode error; sets *encode_failed when a
 // tensor map could not be encoded (reported as an invalid argument).

@@ -21,7 +21,7 @@ def _oracle_expert_weights(w):
     return wq, wsf
 
 
-def _run_grouped(mx, g, rows=None, schedule=(0, 0)):
+def _run_grouped(mx, g, rows=None, schedule=(0, 0, -1)):
     pw = mx.prepare_weight(to_dev_f32(g.w))
     x = to_dev_bf16(g.x_sorted)
     off = torch.from_numpy(g.offsets).cuda()
@@ -30,7 +30,7 @@ def _run_grouped(mx, g, rows=None, schedule=(0, 0)):
     try:
         y = mx.grouped_linear(x, off, pw, b)
     finally:
-        mx.set_schedule(0, 0)
+        mx.set_schedule(0, 0, -1)
     torch.cuda.synchronize()
     wq, wsf = _oracle_expert_weights(g.w)
     y_ref = oracle.grouped_linear(g.x_sorted, g.offsets, wq, wsf, g.bias, rows=rows)
@@ -56,7 +56,7 @@ def test_grouped_edge_segments(lib, tt):
     """Empty experts, one-row experts, a segment longer than the token tile,
     ragged N, bias."""
     g = workloads.grouped_from_counts([5, 0, 300, 1, 0, 17, 40, 0], n=260, k=512, seed=51, bias=True)
-    _run_grouped(lib, g, schedule=(tt, 0))
+    _run_grouped(lib, g, schedule=(tt, 0, -1))
 
 
 def test_grouped_all_rows_one_expert(lib):

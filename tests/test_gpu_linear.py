@@ -13,7 +13,7 @@ from gpu_common import assert_close_to_oracle, oracle_weight, to_dev_bf16, to_de
 pytestmark = pytest.mark.gpu
 
 
-def _run_dense(mx, d, rows=None, schedule=(0, 0)):
+def _run_dense(mx, d, rows=None, schedule=(0, 0, -1)):
     pw = mx.prepare_weight(to_dev_f32(d.w))
     x = to_dev_bf16(d.x)
     b = None if d.bias is None else to_dev_bf16(d.bias)
@@ -21,7 +21,7 @@ def _run_dense(mx, d, rows=None, schedule=(0, 0)):
     try:
         y = mx.linear(x, pw, b)
     finally:
-        mx.set_schedule(0, 0)
+        mx.set_schedule(0, 0, -1)
     torch.cuda.synchronize()
     assert y.shape == (d.m, d.n) and y.is_contiguous()
     wq, wsf = oracle_weight(d.w)
@@ -74,13 +74,16 @@ def test_vllm_shapes_cosine_and_oracle(lib, shape):
     assert_close_to_oracle(y, oracle.linear(x.float().numpy(), wq, wsf), "vllm%s" % (shape,))
 
 
-@pytest.mark.parametrize("tt,split", [(16, 1), (16, 4), (32, 2), (64, 1), (64, 8), (128, 1),
-                                      (128, 4), (256, 1)])
-def test_every_schedule(lib, tt, split):
-    """Each token-tile size and split-K factor on a shape with several weight
-    tiles, a ragged N (N_pad > N) and a ragged token tail."""
+@pytest.mark.parametrize("tt,split,fuse", [
+    (16, -1, 0), (16, 1, 1), (16, 4, 1), (16, 4, 0), (32, 2, 1), (32, 3, 0), (64, -1, 0),
+    (64, 8, 1), (64, 8, 0), (128, -1, 0), (128, 4, 0), (128, 2, 1), (256, -1, 0)])
+def test_every_schedule(lib, tt, split, fuse):
+    """Each token-tile size, persistent (-1) or one tile per cluster of `split`
+    CTAs, with the activation quantization fused into the GEMM or not, on a
+    shape with several weight tiles, a ragged N (N_pad > N) and a ragged token
+    tail."""
     d = workloads.dense(m=300, n=390, k=1024, seed=30, bias=True)
-    _run_dense(lib, d, schedule=(tt, split))
+    _run_dense(lib, d, schedule=(tt, split, fuse))
 
 
 @pytest.mark.parametrize("m,n,k", [(1, 128, 256), (2, 130, 256), (17, 384, 512), (33, 260, 1024),
