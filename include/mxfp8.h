@@ -157,6 +157,35 @@ mxfp8_status mxfp8_grouped_linear(const void* x_sorted, int64_t rows,
                                   void* y, void* workspace,
                                   size_t workspace_bytes, void* stream);
 
+/* ------------------------------------------------ scratch-free variant
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that cannot allocate device memory, so cannot hand mxfp8_linear a
+ * workspace: code inside a host framework that owns every device allocation
+ * (an allocation behind its back breaks its memory accounting), or serving
+ * paths that must never allocate once running.
+ *
+ * mxfp8_linear_static_scratch computes what mxfp8_linear computes, always by
+ * the unfused path (quantizer -> scratch -> GEMM), with the scratch in an
+ * array of MXFP8_STATIC_SCRATCH_BYTES inside the library: every GPU that
+ * loads the library holds that array until the process exits.  It allocates
+ * nothing and calls no allocating routine.  The caller still passes x, the
+ * weight, bias and y.
+ *  - Sizes: ceil(m*k/256)*256 + ceil(m/8)*8 * k/32 bytes must fit the array,
+ *    else MXFP8_ERR_WORKSPACE_TOO_SMALL and nothing is launched (at k = 2048
+ *    that is m <= 7943; at k = 8192, m <= 1985).
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress with that device current); make that first call
+ *    before any stream capture begins.
+ *  - All calls share the one array, which keeps the last call's contents
+ *    (nothing needs clearing: each call writes every byte it reads).  Calls
+ *    whose kernels overlap on the GPU race on it: serialise them.
+ *  - Errors and other conventions as mxfp8_linear; a failed CUDA call's code
+ *    is returned by mxfp8_static_scratch_last_cuda_error(). */
+#define MXFP8_STATIC_SCRATCH_BYTES (16u << 20)
+mxfp8_status mxfp8_linear_static_scratch(const void* x, int64_t m, const mxfp8_weight* w,
+                                         const void* bias, void* y, void* stream);
+int mxfp8_static_scratch_last_cuda_error(void);
+
 /* --------------------------------------------------------- status helpers */
 
 const char* mxfp8_status_string(mxfp8_status status);

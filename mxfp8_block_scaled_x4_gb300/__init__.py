@@ -90,6 +90,8 @@ def library():
         "mxfp8_last_cuda_error": (ctypes.c_int, []),
         "mxfp8_device_error": (ctypes.c_int, []),
         "mxfp8_set_schedule": (None, [ctypes.c_int, ctypes.c_int, ctypes.c_int]),
+        "mxfp8_linear_static_scratch": (ctypes.c_int, [vp, i64, W, vp, vp, vp]),
+        "mxfp8_static_scratch_last_cuda_error": (ctypes.c_int, []),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
