@@ -204,6 +204,11 @@ mxfp8_status mxfp8_device_error(void);
  * (one-tile schedules of mxfp8_linear) -- the GEMM then quantizes x itself. */
 void mxfp8_set_schedule(int tokens_per_tile, int split_k, int fuse_quant);
 
+/* Testing hook: the schedule of the calling thread's last GEMM launch, as
+ * out5[0..4] = {tokens per tile, split (-1 = persistent), fused quantization
+ * (0/1), grid size, pipeline stages}. */
+void mxfp8_last_schedule(int* out5);
+
 #ifdef __cplusplus
 }
 #endif

@@ -91,6 +91,7 @@ def library():
         "mxfp8_device_error": (ctypes.c_int, []),
         "mxfp8_set_schedule": (None, [ctypes.c_int, ctypes.c_int, ctypes.c_int]),
         "mxfp8_linear_static_scratch": (ctypes.c_int, [vp, i64, W, vp, vp, vp]),
+        "mxfp8_last_schedule": (None, [ctypes.POINTER(ctypes.c_int)]),
         "mxfp8_static_scratch_last_cuda_error": (ctypes.c_int, []),
     }
     for name, (res, args) in sig.items():
@@ -250,6 +251,14 @@ def set_schedule(tokens_per_tile: int = 0, split_k: int = 0, fuse_quant: int = -
     split_k 0 = auto, -1 = persistent, >0 = one tile per cluster of split_k
     CTAs; fuse_quant -1 = auto, 0 = off, 1 = on where possible."""
     library().mxfp8_set_schedule(int(tokens_per_tile), int(split_k), int(fuse_quant))
+
+
+def last_schedule() -> dict:
+    """Schedule of this thread's last GEMM launch (testing aid)."""
+    out = (ctypes.c_int * 5)()
+    library().mxfp8_last_schedule(out)
+    return {"tokens_per_tile": out[0], "split": out[1], "fused": bool(out[2]),
+            "grid": out[3], "stages": out[4]}
 
 
 def device_error() -> int:

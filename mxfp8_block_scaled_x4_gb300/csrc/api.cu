@@ -249,6 +249,10 @@ mxfp8_status mxfp8_device_error(void) {
     return v ? MXFP8_ERR_DEVICE_TIMEOUT : MXFP8_OK;
 }
 
+void mxfp8_last_schedule(int* out5) {
+    if (out5) mxk::last_schedule(out5);
+}
+
 void mxfp8_set_schedule(int tokens_per_tile, int split_k, int fuse_quant) {
     const bool tt_ok = tokens_per_tile == 0 || tokens_per_tile == 16 || tokens_per_tile == 32 ||
                        tokens_per_tile == 64 || tokens_per_tile == 128 || tokens_per_tile == 256;

@@ -43,8 +43,8 @@
 //                rank order (deterministic).
 // Programmatic dependent launch: the kernel lets the next grid start at once;
 // it reads nothing a previous grid may write before griddepcontrol.wait,
-// except the weights, their scales and the grouped offsets, which are written
-// before the layer's first kernel.
+// except the weights, their scales, the bias and the grouped offsets, which
+// are written before the layer's first kernel.
 // Every wait is bounded (kWaitNs); a timeout sets g_gemm_error, every role
 // unwinds, in-flight copies and MMAs are drained (again bounded), TMEM is
 // freed and the kernel returns.
@@ -61,6 +61,9 @@
 namespace mxk {
 
 __device__ unsigned int g_gemm_error;
+
+// Schedule of the last GEMM launch on the host (testing aid).
+thread_local int t_last_schedule[5];
 
 namespace {
 
@@ -99,8 +102,10 @@ struct Geometry {
     static constexpr int kSfSlotCols = 4 + 4 * kSfChunks;         // TMEM columns per stage
 };
 
+// Tokens whose split-K sum one rank owns: a multiple of 4 so partials move as
+// 16-byte vectors (some ranks may own none).
 __host__ __device__ constexpr int tokens_per_owner(int tt, int splits) {
-    return (tt + splits - 1) / splits;
+    return ((tt + splits - 1) / splits + 3) & ~3;
 }
 
 struct TileInfo {
@@ -172,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, (TT <= 64 ? 2 : 1)) mxfp8_gemm_kerne
     const bool fused = p.x != nullptr;
     const int per = tokens_per_owner(TT, splits);
 
-    uint8_t* partial = smem + stages * G::kStageBytes;  // split-K partials [splits][per][128] f32
+    uint8_t* partial = smem + stages * G::kStageBytes;  // split-K partials [splits][128][per] f32
     uint8_t* ctrl = partial + (reduce ? splits * per * 512 : 0);
     uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
     uint64_t* empty = full + stages;
@@ -241,6 +246,7 @@ __global__ void __launch_bounds__(kThreads, (TT <= 64 ? 2 : 1)) mxfp8_gemm_kerne
     // before the first remote access.
     if (reduce) cluster_arrive_relaxed();
     bool cluster_waited = false;
+    float b_red = 0.0f;  // split-K owners: bias of their output feature
 
     // Work assignment: a list of (tile, K range).
     int tile_first, tile_stride, num_tiles, kb_begin, kb_end, rank = 0;
@@ -440,6 +446,13 @@ __global__ void __launch_bounds__(kThreads, (TT <= 64 ? 2 : 1)) mxfp8_gemm_kerne
         __syncwarp();
     } else {
         const int ew = warp - 2;  // warps 2..9
+        // Bias of the output feature this thread finishes in the split-K
+        // reduction, fetched before anything else so its latency hides.
+        if (reduce && p.bias) {
+            const TileInfo t0 = decode_tile<TT>(tile_first, p, prefix, offs);
+            const int n_red = t0.n_tile * 128 + ((threadIdx.x - 64) & 127);
+            if (n_red < p.n) b_red = __bfloat162float(p.bias[static_cast<size_t>(t0.e) * p.n + n_red]);
+        }
         // ---------------------------------------- fused activation quantizer
         if (fused) {
             // One tile per CTA.  Each pass of a warp quantizes 8 (row, block)
@@ -509,6 +522,10 @@ __global__ void __launch_bounds__(kThreads, (TT <= 64 ? 2 : 1)) mxfp8_gemm_kerne
         int tile_iter = 0;
         for (int t = tile_first; t < num_tiles; t += tile_stride, ++tile_iter) {
             const TileInfo ti = decode_tile<TT>(t, p, prefix, offs);
+            const int nl = quad * 32 + lane;  // weight row within the tile
+            const int n = ti.n_tile * 128 + nl;
+            const float b = (!reduce && p.bias && n < p.n)
+                                ? __bfloat162float(p.bias[static_cast<size_t>(ti.e) * p.n + n]) : 0.0f;
             bool ok = mbar_wait(acc_full, tile_iter & 1, kWaitNs);
             ok = __all_sync(0xFFFFFFFFu, ok ? 1 : 0) != 0;
             if (!ok) { if (lane == 0) record_timeout(abort_flag); break; }
@@ -539,25 +556,22 @@ __global__ void __launch_bounds__(kThreads, (TT <= 64 ? 2 : 1)) mxfp8_gemm_kerne
             __syncwarp();
             if (lane == 0) mbar_arrive(acc_empty);
 
-            const int nl = quad * 32 + lane;  // weight row within the tile
             if (reduce) {
-                // Push: token column c goes to rank c / per, slot [rank][c % per].
+                // Push: token columns c..c+3 go to rank c / per as one 16-byte
+                // store into its slot [rank][nl][c % per].
                 __syncwarp();
                 cluster_wait();
                 cluster_waited = true;
                 const uint32_t pbase = smem_addr(partial);
 #pragma unroll
-                for (int j = 0; j < kCols; ++j) {
+                for (int j = 0; j < kCols; j += 4) {
                     const int c = col0 + j;
                     const int owner = c / per;
-                    const int jj = c - owner * per;
-                    const uint32_t a = pbase + static_cast<uint32_t>(((rank * per + jj) * 128 + nl) * 4);
-                    st_cluster_f32(map_to_rank(a, static_cast<uint32_t>(owner)), __uint_as_float(acc[j]));
+                    const uint32_t a = pbase + static_cast<uint32_t>(((rank * 128 + nl) * per + (c - owner * per)) * 4);
+                    st_cluster_v4(map_to_rank(a, static_cast<uint32_t>(owner)), acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
                 }
             } else {
-                const int n = ti.n_tile * 128 + nl;
                 if (n < p.n) {
-                    const float b = p.bias ? __bfloat162float(p.bias[static_cast<size_t>(ti.e) * p.n + n]) : 0.0f;
                     const int jmax = min(kCols, ti.count - col0);
                     __nv_bfloat16* yp = p.y + static_cast<size_t>(ti.tok0 + col0) * p.n + n;
 #pragma unroll
@@ -571,26 +585,33 @@ __global__ void __launch_bounds__(kThreads, (TT <= 64 ? 2 : 1)) mxfp8_gemm_kerne
 
     // ------------------------------------------------- split-K reduction
     if (reduce) {
-        const int et = threadIdx.x - 64;
-        const TileInfo ti = decode_tile<TT>(tile_first, p, prefix, offs);
-        const int nl = et & 127;
-        const int n = ti.n_tile * 128 + nl;
-        float b = 0.0f;
         __syncwarp();
         if (!__all_sync(0xFFFFFFFFu, cluster_waited ? 1 : 0)) cluster_wait();
-        const bool epi = warp >= 2 && warp < 2 + kEpilogueWarps;
-        if (epi && p.bias && n < p.n) b = __bfloat162float(p.bias[static_cast<size_t>(ti.e) * p.n + n]);
         cluster_sync();  // every rank's pushes have landed
+        const bool epi = warp >= 2 && warp < 2 + kEpilogueWarps;
         if (epi && !*abort_flag) {
+            // Owner: tokens [rank*per, rank*per + per), four per thread and step,
+            // summed over source ranks in rank order.
+            const TileInfo ti = decode_tile<TT>(tile_first, p, prefix, offs);
+            const int et = threadIdx.x - 64;
+            const int nl = et & 127;
+            const int n = ti.n_tile * 128 + nl;
             const float* part = reinterpret_cast<const float*>(partial);
             const int j0 = rank * per;
-            for (int o = et; o < per * 128; o += kEpilogueWarps * 32) {
-                const int jj = o >> 7;
-                const int j = j0 + jj;
-                if (j < ti.count && j < TT && n < p.n) {
-                    float sum = 0.0f;
-                    for (int r = 0; r < splits; ++r) sum += part[(r * per + jj) * 128 + nl];
-                    p.y[static_cast<size_t>(ti.tok0 + j) * p.n + n] = __float2bfloat16_rn(sum + b);
+            for (int q = et >> 7; q < per / 4; q += (kEpilogueWarps * 32) / 128) {
+                float4 sum = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                for (int r = 0; r < splits; ++r) {
+                    const float4 v = *reinterpret_cast<const float4*>(part + (r * 128 + nl) * per + q * 4);
+                    sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
+                }
+                const float sv[4] = {sum.x, sum.y, sum.z, sum.w};
+                if (n < p.n) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int j = j0 + q * 4 + i;
+                        if (j < ti.count && j < TT)
+                            p.y[static_cast<size_t>(ti.tok0 + j) * p.n + n] = __float2bfloat16_rn(sv[i] + b_red);
+                    }
                 }
             }
         }
@@ -673,36 +694,6 @@ LaunchPlan<TT> plan_for(int splits, bool persistent, int kq) {
     return lp;
 }
 
-// Clusters of `splits` CTAs that can be resident at once (one wave), cached.
-template <int TT>
-int max_active_clusters(int splits, size_t smem, cudaStream_t s) {
-    static int cache[9][64];
-    const int key = static_cast<int>(smem >> 12) & 63;
-    if (cache[splits][key] > 0) return cache[splits][key];
-    cudaLaunchConfig_t cfg;
-    memset(&cfg, 0, sizeof(cfg));
-    cfg.gridDim = dim3(splits * 64, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = splits;
-    attr.val.clusterDim.y = 1;
-    attr.val.clusterDim.z = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaFuncSetAttribute(mxfp8_gemm_kernel<TT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess ||
-        cudaOccupancyMaxActiveClusters(&n, mxfp8_gemm_kernel<TT>, &cfg) != cudaSuccess) {
-        cudaGetLastError();
-        return 0;
-    }
-    cache[splits][key] = n;
-    return n;
-}
-
 template <int TT>
 cudaError_t launch_tt(const GemmProblem& pr, const GemmSchedule& sch, int num_sms, cudaStream_t s,
                       bool* encode_failed) {
@@ -711,7 +702,10 @@ cudaError_t launch_tt(const GemmProblem& pr, const GemmSchedule& sch, int num_sm
     memset(&a, 0, sizeof(a));
     const int64_t m8 = (pr.m + 7) / 8 * 8;
     const bool fused = sch.fuse_quant && pr.x != nullptr;
-    a.box_rows = TT < 32 ? TT : 32;
+    // One TMA box per token tile: the producer is a single thread and every
+    // TMA instruction costs issue time.  Rows past M are zero-filled; rows past
+    // a grouped segment belong to the next expert and are never stored.
+    a.box_rows = TT;
     a.sf_groups = TT / 8 + 1;
     bool ok = encode_2d_u8(&a.map_w, pr.wq, pr.k, pr.experts * pr.n_pad, pr.k, 128, 128, true);
     if (ok && !fused)
@@ -724,17 +718,7 @@ cudaError_t launch_tt(const GemmProblem& pr, const GemmSchedule& sch, int num_sm
     const int kq = static_cast<int>(pr.k / 128);
     const int tok_tiles = static_cast<int>((pr.m + TT - 1) / TT);
     const int n_tiles = static_cast<int>(pr.n_pad / 128);
-    int splits = sch.persistent ? 1 : sch.split_k;
-    if (!sch.persistent && !sch.split_forced) {
-        // Largest split whose clusters all fit in one wave.
-        const int tiles = n_tiles * tok_tiles;
-        int chosen = 1;
-        for (int c = splits; c > 1; --c) {
-            const LaunchPlan<TT> lp = plan_for<TT>(c, false, kq);
-            if (lp.stages >= 1 && tiles <= max_active_clusters<TT>(c, lp.smem, s)) { chosen = c; break; }
-        }
-        splits = chosen;
-    }
+    const int splits = sch.persistent ? 1 : sch.split_k;
     const LaunchPlan<TT> lp = plan_for<TT>(splits, sch.persistent, kq);
     if (lp.stages < 1) return cudaErrorInvalidConfiguration;
 
@@ -800,6 +784,11 @@ cudaError_t launch_tt(const GemmProblem& pr, const GemmSchedule& sch, int num_sm
     ++na;
     cfg.attrs = attrs;
     cfg.numAttrs = na;
+    t_last_schedule[0] = TT;
+    t_last_schedule[1] = sch.persistent ? -1 : splits;
+    t_last_schedule[2] = fused ? 1 : 0;
+    t_last_schedule[3] = grid;
+    t_last_schedule[4] = lp.stages;
     return cudaLaunchKernelEx(&cfg, mxfp8_gemm_kernel<TT>, a);
 }
 
@@ -815,17 +804,21 @@ GemmSchedule choose_schedule(const GemmProblem& p, int num_sms, int force_tt, in
         const int64_t mean = (p.m + p.experts - 1) / (p.experts > 0 ? p.experts : 1);
         tt = mean <= 16 ? 16 : mean <= 32 ? 32 : mean <= 64 ? 64 : mean <= 128 ? 128 : 256;
     } else {
-        tt = p.m <= 16 ? 16 : p.m <= 32 ? 32 : p.m <= 64 ? 64 : p.m <= 128 ? 128 : 256;
+        // Up to 128 tokens the 64-token tile with split-K measured fastest
+        // (more CTAs stream weights at once); above, persistent 256-token tiles.
+        tt = p.m <= 16 ? 16 : p.m <= 32 ? 32 : p.m <= 128 ? 64 : 256;
     }
     if (force_tt) tt = force_tt;
     bool persistent = p.offsets != nullptr || tt > 128;
     int split = 1;
     if (!persistent) {
         const int64_t tiles = (p.n_pad / 128) * ((p.m + tt - 1) / tt);
-        // enough CTAs to cover the SMs (twice for the small tiles that fit two
-        // per SM), at least two K blocks per CTA
-        int64_t want = ((tt <= 32 ? 2 : 1) * num_sms + tiles - 1) / tiles;
-        if (want > 8) want = 8;
+        // Measured on the decode and mid-batch shapes: as many CTAs as fit
+        // two per SM (tiles of <= 64 tokens run two per SM), at least two K
+        // blocks per CTA, and at most 4 per cluster -- beyond that the cluster
+        // barrier and the reduction cost more than the extra streams save.
+        int64_t want = ((tt <= 64 ? 2 : 1) * num_sms) / tiles;
+        if (want > 4) want = 4;
         if (want > kq / 2) want = kq / 2;
         if (want < 1) want = 1;
         split = static_cast<int>(want);
@@ -838,14 +831,13 @@ GemmSchedule choose_schedule(const GemmProblem& p, int num_sms, int force_tt, in
         split = force_split;
     }
     if (split > kq) split = static_cast<int>(kq);
-    bool fuse = !persistent && p.x != nullptr && tt <= 64;
+    bool fuse = !persistent && p.x != nullptr && p.m <= 64;
     if (force_fuse == 0) fuse = false;
     if (force_fuse == 1) fuse = !persistent && p.x != nullptr;
     sch.tokens_per_tile = tt;
     sch.split_k = persistent ? 1 : split;
     sch.persistent = persistent;
     sch.fuse_quant = fuse;
-    sch.split_forced = force_split != 0;
     return sch;
 }
 
@@ -860,6 +852,10 @@ cudaError_t launch_gemm(const GemmProblem& p, const GemmSchedule& sch, int num_s
         case 256: return launch_tt<256>(p, sch, num_sms, s, encode_failed);
         default: return cudaErrorInvalidValue;
     }
+}
+
+void last_schedule(int* out5) {
+    for (int i = 0; i < 5; ++i) out5[i] = t_last_schedule[i];
 }
 
 cudaError_t read_and_clear_gemm_error(unsigned int* out) {

@@ -37,7 +37,6 @@ struct GemmSchedule {
     int split_k;               // CTAs (a cluster) per output tile, K split among them
     bool persistent;           // tiles strided over a persistent grid (split_k == 1)
     bool fuse_quant;           // the GEMM quantizes x itself (one-tile schedules)
-    bool split_forced;         // keep split_k even if the clusters need two waves
 };
 
 // force_tt: 0 or a token tile; force_split: 0 auto, -1 persistent, >0 split;
@@ -49,6 +48,10 @@ GemmSchedule choose_schedule(const GemmProblem& p, int num_sms, int force_tt, in
 // tensor map could not be encoded (reported as an invalid argument).
 cudaError_t launch_gemm(const GemmProblem& p, const GemmSchedule& sch, int num_sms,
                         cudaStream_t s, bool* encode_failed);
+
+// Schedule of this thread's last GEMM launch: {tokens per tile, split (-1 =
+// persistent), fused quantization, grid, stages}.
+void last_schedule(int* out5);
 
 // Reads and clears the device error word of the GEMM kernels.
 cudaError_t read_and_clear_gemm_error(unsigned int* out);
