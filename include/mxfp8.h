@@ -204,6 +204,13 @@ mxfp8_status mxfp8_device_error(void);
  * (one-tile schedules of mxfp8_linear) -- the GEMM then quantizes x itself. */
 void mxfp8_set_schedule(int tokens_per_tile, int split_k, int fuse_quant);
 
+/* Testing hook for failure detection: limit, in nanoseconds, of every
+ * pipeline wait of later GEMM launches (0 restores the default, 4 s).  A wait
+ * that runs out sets the device error word read by mxfp8_device_error(); the
+ * kernel then unwinds (in-flight copies and MMAs drained, TMEM freed) and
+ * returns, so the context stays usable.  Process-wide. */
+void mxfp8_set_wait_limit_ns(uint64_t ns);
+
 /* Testing hook: the schedule of the calling thread's last GEMM launch, as
  * out5[0..4] = {tokens per tile, split (-1 = persistent), fused quantization
  * (0/1), grid size, pipeline stages}. */

@@ -92,6 +92,7 @@ def library():
         "mxfp8_set_schedule": (None, [ctypes.c_int, ctypes.c_int, ctypes.c_int]),
         "mxfp8_linear_static_scratch": (ctypes.c_int, [vp, i64, W, vp, vp, vp]),
         "mxfp8_last_schedule": (None, [ctypes.POINTER(ctypes.c_int)]),
+        "mxfp8_set_wait_limit_ns": (None, [ctypes.c_uint64]),
         "mxfp8_static_scratch_last_cuda_error": (ctypes.c_int, []),
     }
     for name, (res, args) in sig.items():
@@ -165,9 +166,13 @@ class PreparedWeight:
         return self.q.device
 
 
-def prepare_weight(w: torch.Tensor) -> PreparedWeight:
+def prepare_weight(w: torch.Tensor, out: PreparedWeight = None) -> PreparedWeight:
     """Quantize + pad + lay out a weight [n, k] (or stacked experts
-    [e, n, k]) given as float32 or bfloat16 on the GPU."""
+    [e, n, k]) given as float32 or bfloat16 on the GPU.
+
+    out: an existing PreparedWeight of the same shape to re-prepare in place
+    (a weight refit: its buffers keep their addresses, so CUDA graphs that
+    captured calls on it stay valid and see the new weight on replay)."""
     _need(w.is_cuda, "weight must be a CUDA tensor")
     _need(w.dtype in (torch.float32, torch.bfloat16), "weight must be float32 or bfloat16")
     w3 = w.unsqueeze(0) if w.dim() == 2 else w
@@ -175,9 +180,13 @@ def prepare_weight(w: torch.Tensor) -> PreparedWeight:
     w3 = w3.contiguous()
     e, n, k = w3.shape
     n_pad = (n + 127) // 128 * 128
-    q = torch.empty((e, n_pad, k), dtype=torch.uint8, device=w.device)
-    sf = torch.empty((e, n_pad * (k // 32)), dtype=torch.uint8, device=w.device)
-    pw = PreparedWeight(q, sf, n)
+    if out is not None:
+        _need((out.num_experts, out.n, out.k) == (e, n, k), "refit needs a weight of the same shape")
+        pw = out
+    else:
+        q = torch.empty((e, n_pad, k), dtype=torch.uint8, device=w.device)
+        sf = torch.empty((e, n_pad * (k // 32)), dtype=torch.uint8, device=w.device)
+        pw = PreparedWeight(q, sf, n)
     dt = IN_BF16 if w3.dtype == torch.bfloat16 else IN_F32
     _check(library().mxfp8_prepare_weight(_ptr(w3), dt, ctypes.byref(pw.c), _stream(w)),
            "mxfp8_prepare_weight")
@@ -259,6 +268,12 @@ def last_schedule() -> dict:
     library().mxfp8_last_schedule(out)
     return {"tokens_per_tile": out[0], "split": out[1], "fused": bool(out[2]),
             "grid": out[3], "stages": out[4]}
+
+
+def set_wait_limit_ns(ns: int = 0) -> None:
+    """Limit of every pipeline wait in later GEMM launches (0 = default 4 s).
+    Testing aid for the timeout path."""
+    library().mxfp8_set_wait_limit_ns(int(ns))
 
 
 def device_error() -> int:

@@ -249,6 +249,8 @@ mxfp8_status mxfp8_device_error(void) {
     return v ? MXFP8_ERR_DEVICE_TIMEOUT : MXFP8_OK;
 }
 
+void mxfp8_set_wait_limit_ns(uint64_t ns) { mxk::set_wait_limit_ns(ns); }
+
 void mxfp8_last_schedule(int* out5) {
     if (out5) mxk::last_schedule(out5);
 }

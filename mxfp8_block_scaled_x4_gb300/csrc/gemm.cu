@@ -45,7 +45,7 @@
 // it reads nothing a previous grid may write before griddepcontrol.wait,
 // except the weights, their scales, the bias and the grouped offsets, which
 // are written before the layer's first kernel.
-// Every wait is bounded (kWaitNs); a timeout sets g_gemm_error, every role
+// Every wait is bounded (4 s by default); a timeout sets g_gemm_error, every role
 // unwinds, in-flight copies and MMAs are drained (again bounded), TMEM is
 // freed and the kernel returns.
 #include <cuda.h>
@@ -64,10 +64,11 @@ __device__ unsigned int g_gemm_error;
 
 // Schedule of the last GEMM launch on the host (testing aid).
 thread_local int t_last_schedule[5];
+uint64_t g_wait_limit_ns = 0;  // 0: kWaitNs
 
 namespace {
 
-constexpr uint64_t kWaitNs = 4000000000ull;   // 4 s per wait, then give up
+constexpr uint64_t kWaitNs = 4000000000ull;   // default: 4 s per wait, then give up
 constexpr uint64_t kDrainNs = 200000000ull;   // 0.2 s per drain wait
 constexpr int kThreads = 352;
 constexpr int kEpilogueWarps = 8;
@@ -88,6 +89,7 @@ struct GemmArgs {
     int stages, splits, persistent;
     int num_tiles;           // dense (grouped counts tiles on the device)
     uint32_t tmem_cols;
+    uint64_t wait_ns;        // limit of every pipeline wait
 };
 
 template <int TT>
@@ -325,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, (TT <= 64 ? 2 : 1)) mxfp8_gemm_kerne
                     if (*abort_flag) { stop = true; break; }
                     const int s = job % stages;
                     const int round = job / stages;
-                    if (!mbar_wait(&empty[s], (round & 1) ^ 1, kWaitNs)) {
+                    if (!mbar_wait(&empty[s], (round & 1) ^ 1, p.wait_ns)) {
                         record_timeout(abort_flag);
                         stop = true;
                         break;
@@ -374,13 +376,13 @@ __global__ void __launch_bounds__(kThreads, (TT <= 64 ? 2 : 1)) mxfp8_gemm_kerne
                 uint32_t idesc[4];
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) idesc[kk] = idesc_mxf8(128, n_mma, kk, kk);
-                if (tile_iter > 0 && !mbar_wait(acc_empty, (tile_iter - 1) & 1, kWaitNs)) {
+                if (tile_iter > 0 && !mbar_wait(acc_empty, (tile_iter - 1) & 1, p.wait_ns)) {
                     record_timeout(abort_flag);
                     break;
                 }
                 for (int kb = kb_begin; kb < kb_end; ++kb) {
-                    if (!mbar_wait(&full[s], phase, kWaitNs) ||
-                        (!fused && !mbar_wait(&sfok[s], phase, kWaitNs))) {
+                    if (!mbar_wait(&full[s], phase, p.wait_ns) ||
+                        (!fused && !mbar_wait(&sfok[s], phase, p.wait_ns))) {
                         record_timeout(abort_flag);
                         stop = true;
                         break;
@@ -416,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, (TT <= 64 ? 2 : 1)) mxfp8_gemm_kerne
                 const TileInfo ti = decode_tile<TT>(t, p, prefix, offs);
                 const int off8 = ti.tok0 & 7;
                 for (int kb = kb_begin; kb < kb_end; ++kb) {
-                    bool ok = mbar_wait(&sfraw[s], phase, kWaitNs);
+                    bool ok = mbar_wait(&sfraw[s], phase, p.wait_ns);
                     ok = __all_sync(0xFFFFFFFFu, ok ? 1 : 0) != 0;
                     if (!ok) {
                         if (lane == 0) record_timeout(abort_flag);
@@ -485,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, (TT <= 64 ? 2 : 1)) mxfp8_gemm_kerne
                     const int pass = ps - job * kPasses;
                     const int s = job % stages;
                     if (pass == 0 && job >= stages) {
-                        ok = mbar_wait(&empty[s], ((job / stages) & 1) ^ 1, kWaitNs);
+                        ok = mbar_wait(&empty[s], ((job / stages) & 1) ^ 1, p.wait_ns);
                         ok = __all_sync(0xFFFFFFFFu, ok ? 1 : 0) != 0;
                         if (!ok) { if (lane == 0) record_timeout(abort_flag); break; }
                     }
@@ -526,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, (TT <= 64 ? 2 : 1)) mxfp8_gemm_kerne
             const int n = ti.n_tile * 128 + nl;
             const float b = (!reduce && p.bias && n < p.n)
                                 ? __bfloat162float(p.bias[static_cast<size_t>(ti.e) * p.n + n]) : 0.0f;
-            bool ok = mbar_wait(acc_full, tile_iter & 1, kWaitNs);
+            bool ok = mbar_wait(acc_full, tile_iter & 1, p.wait_ns);
             ok = __all_sync(0xFFFFFFFFu, ok ? 1 : 0) != 0;
             if (!ok) { if (lane == 0) record_timeout(abort_flag); break; }
             tc_fence_after();
@@ -738,6 +740,7 @@ cudaError_t launch_tt(const GemmProblem& pr, const GemmSchedule& sch, int num_sm
     a.persistent = sch.persistent ? 1 : 0;
     a.stages = lp.stages;
     a.tmem_cols = lp.tmem_cols;
+    a.wait_ns = g_wait_limit_ns ? g_wait_limit_ns : kWaitNs;
     const size_t smem = lp.smem;
 
     cudaError_t err = cudaFuncSetAttribute(mxfp8_gemm_kernel<TT>,
@@ -853,6 +856,8 @@ cudaError_t launch_gemm(const GemmProblem& p, const GemmSchedule& sch, int num_s
         default: return cudaErrorInvalidValue;
     }
 }
+
+void set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns = ns; }
 
 void last_schedule(int* out5) {
     for (int i = 0; i < 5; ++i) out5[i] = t_last_schedule[i];

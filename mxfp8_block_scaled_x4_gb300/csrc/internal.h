@@ -53,6 +53,9 @@ cudaError_t launch_gemm(const GemmProblem& p, const GemmSchedule& sch, int num_s
 // persistent), fused quantization, grid, stages}.
 void last_schedule(int* out5);
 
+// Limit of every pipeline wait of later GEMM launches (0 = the default).
+void set_wait_limit_ns(uint64_t ns);
+
 // Reads and clears the device error word of the GEMM kernels.
 cudaError_t read_and_clear_gemm_error(unsigned int* out);
 

@@ -61,13 +61,13 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
 // Waits for phase `parity` of `bar` to complete, giving up after `limit_ns`
 // of wall time.  Returns false on timeout (the caller records the error and
 // unwinds); never spins forever.
+// (try_wait itself suspends the thread for a bounded, system-dependent time,
+// so the clock is read after every unsuccessful attempt.)
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
     if (mbar_test(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (;;) {
-#pragma unroll 1
-        for (int i = 0; i < 32; ++i)
-            if (mbar_test(bar, parity)) return true;
+        if (mbar_test(bar, parity)) return true;
         if (global_timer_ns() - t0 > limit_ns) return false;
     }
 }
