@@ -211,9 +211,16 @@ void mxfp8_set_schedule(int tokens_per_tile, int split_k, int fuse_quant);
  * returns, so the context stays usable.  Process-wide. */
 void mxfp8_set_wait_limit_ns(uint64_t ns);
 
+/* Testing hook: MMA pipelines per CTA for later launches (0 = automatic, 1,
+ * 2, or 4; more than one only for tiles of <= 64 tokens, 4 only for 16).
+ * Each pipeline has its own producer and MMA-issuing thread, owns every
+ * pipes-th K block of a tile and accumulates in its own TMEM columns; the
+ * epilogue sums them in pipeline order.  Process-wide. */
+void mxfp8_set_pipes(int pipes);
+
 /* Testing hook: the schedule of the calling thread's last GEMM launch, as
- * out5[0..4] = {tokens per tile, split (-1 = persistent), fused quantization
- * (0/1), grid size, pipeline stages}. */
+ * out5[0..4] = {tokens per tile + 1000 * (pipelines - 1), split (-1 =
+ * persistent), fused quantization (0/1), grid size, stages per pipeline}. */
 void mxfp8_last_schedule(int* out5);
 
 #ifdef __cplusplus

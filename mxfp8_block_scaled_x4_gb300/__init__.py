@@ -93,6 +93,7 @@ def library():
         "mxfp8_linear_static_scratch": (ctypes.c_int, [vp, i64, W, vp, vp, vp]),
         "mxfp8_last_schedule": (None, [ctypes.POINTER(ctypes.c_int)]),
         "mxfp8_set_wait_limit_ns": (None, [ctypes.c_uint64]),
+        "mxfp8_set_pipes": (None, [ctypes.c_int]),
         "mxfp8_static_scratch_last_cuda_error": (ctypes.c_int, []),
     }
     for name, (res, args) in sig.items():
@@ -262,12 +263,17 @@ def set_schedule(tokens_per_tile: int = 0, split_k: int = 0, fuse_quant: int = -
     library().mxfp8_set_schedule(int(tokens_per_tile), int(split_k), int(fuse_quant))
 
 
+def set_pipes(pipes: int = 0) -> None:
+    """MMA pipelines per CTA for later launches (0 = automatic; testing aid)."""
+    library().mxfp8_set_pipes(int(pipes))
+
+
 def last_schedule() -> dict:
     """Schedule of this thread's last GEMM launch (testing aid)."""
     out = (ctypes.c_int * 5)()
     library().mxfp8_last_schedule(out)
-    return {"tokens_per_tile": out[0], "split": out[1], "fused": bool(out[2]),
-            "grid": out[3], "stages": out[4]}
+    return {"tokens_per_tile": out[0] % 1000, "pipes": out[0] // 1000 + 1, "split": out[1],
+            "fused": bool(out[2]), "grid": out[3], "stages": out[4]}
 
 
 def set_wait_limit_ns(ns: int = 0) -> None:

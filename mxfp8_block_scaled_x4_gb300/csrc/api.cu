@@ -251,6 +251,8 @@ mxfp8_status mxfp8_device_error(void) {
 
 void mxfp8_set_wait_limit_ns(uint64_t ns) { mxk::set_wait_limit_ns(ns); }
 
+void mxfp8_set_pipes(int pipes) { mxk::set_pipes(pipes); }
+
 void mxfp8_last_schedule(int* out5) {
     if (out5) mxk::last_schedule(out5);
 }

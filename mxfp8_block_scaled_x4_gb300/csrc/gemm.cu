@@ -70,7 +70,6 @@ namespace {
 
 constexpr uint64_t kWaitNs = 4000000000ull;   // default: 4 s per wait, then give up
 constexpr uint64_t kDrainNs = 200000000ull;   // 0.2 s per drain wait
-constexpr int kThreads = 352;
 constexpr int kEpilogueWarps = 8;
 constexpr int kMaxExperts = 1024;
 
@@ -159,9 +158,278 @@ __device__ __forceinline__ void st_shared_v2(void* p, uint2 v) {
     asm volatile("st.shared.v2.u32 [%0], {%1,%2};" ::"r"(smem_addr(p)), "r"(v.x), "r"(v.y) : "memory");
 }
 
-// Small token tiles keep registers low enough for two CTAs per SM.
-template <int TT>
-__global__ void __launch_bounds__(kThreads, (TT <= 64 ? 2 : 1)) mxfp8_gemm_kernel(const __grid_constant__ GemmArgs p) {
+// ----------------------------------------------------------------- kernel
+// Warp roles for PIPES pipelines:
+//   0                      producer of pipe 0      (lane 0)
+//   1                      MMA issuer of pipe 0    (lane 0); TMEM alloc/free
+//   2 .. 9                 epilogue (and fused activation quantizer)
+//   10                     activation-scale re-order (unfused)
+//   11 .. 9+PIPES          producers of pipes 1..PIPES-1
+//   10+PIPES .. 8+2*PIPES  MMA issuers of pipes 1..PIPES-1
+// Pipe q owns the local K blocks i with i % PIPES == q of every tile, its own
+// ring of `stages` shared-memory stages and its own TMEM accumulator; the
+// epilogue sums the accumulators in pipe order.
+__host__ __device__ constexpr int num_warps(int pipes) { return 11 + 2 * (pipes - 1); }
+
+struct Ctx {
+    uint8_t* smem;
+    uint64_t* full;
+    uint64_t* empty;
+    uint64_t* sfraw;
+    uint64_t* acc_full;
+    uint64_t* acc_empty;
+    uint64_t* drain;
+    volatile uint32_t* abort_flag;
+    const int* prefix;
+    const int* offs;
+    uint32_t tmem_base;
+    int stages;        // per pipe
+    int tile_first, tile_stride, num_tiles, kb_begin, kb_end;
+    bool fused;
+};
+
+// Jobs of pipe q in one tile of nk K blocks, and the stage/phase of a job.
+template <int PIPES>
+__device__ __forceinline__ int pipe_jobs(int q, int nk) {
+    return q < nk ? (nk - q + PIPES - 1) / PIPES : 0;
+}
+
+template <int TT, int PIPES>
+__device__ __forceinline__ void run_producer(const GemmArgs& p, const Ctx& c, int q) {
+    using G = Geometry<TT>;
+    const uint64_t pol_w = policy_evict_normal();
+    const uint64_t pol_a = policy_evict_last();
+    const int nk = c.kb_end - c.kb_begin;
+    const int nq = pipe_jobs<PIPES>(q, nk);
+    if (nq == 0) return;
+    const int S = c.stages;
+    auto stage_of = [&](int jq) { return q * S + jq % S; };
+    const uint32_t a_bytes = c.fused ? 0u : static_cast<uint32_t>(TT * 128);
+    auto issue_w = [&](const TileInfo& ti, int kb, int s) {
+        uint8_t* st = c.smem + s * G::kStageBytes;
+        mbar_arrive_expect_tx(&c.full[s], 16384u + 512u + a_bytes);
+        tma_load_2d(st + G::kOffW, &p.map_w, kb * 128, ti.e * p.n_pad + ti.n_tile * 128, &c.full[s], pol_w);
+        bulk_load(st + G::kOffWsf,
+                  p.wsf + ((static_cast<size_t>(ti.e) * p.n_tiles + ti.n_tile) * p.kq + kb) * 512, 512,
+                  &c.full[s], pol_w);
+    };
+    auto issue_a = [&](const TileInfo& ti, int kb, int s) {
+        uint8_t* st = c.smem + s * G::kStageBytes;
+        tma_load_2d(st + G::kOffA, &p.map_a, kb * 128, ti.tok0, &c.full[s], pol_a);
+        mbar_arrive_expect_tx(&c.sfraw[s], static_cast<uint32_t>(p.sf_groups * 32));
+        tma_load_2d(st + G::kOffAsfRaw, &p.map_asf, kb * 32, ti.tok0 >> 3, &c.sfraw[s], pol_a);
+    };
+    // Weight bytes of the first S jobs go out before waiting for the previous
+    // grid: only the activations depend on it.
+    int pre = 0;
+    for (int t = c.tile_first; t < c.num_tiles && pre < S; t += c.tile_stride) {
+        const TileInfo ti = decode_tile<TT>(t, p, c.prefix, c.offs);
+        for (int i = q; i < nk && pre < S; i += PIPES, ++pre) issue_w(ti, c.kb_begin + i, stage_of(pre));
+    }
+    if (!c.fused) {
+        pdl_wait();
+        int j = 0;
+        for (int t = c.tile_first; t < c.num_tiles && j < pre; t += c.tile_stride) {
+            const TileInfo ti = decode_tile<TT>(t, p, c.prefix, c.offs);
+            for (int i = q; i < nk && j < pre; i += PIPES, ++j) issue_a(ti, c.kb_begin + i, stage_of(j));
+        }
+    }
+    int jq = 0;
+    bool stop = false;
+    for (int t = c.tile_first; t < c.num_tiles && !stop; t += c.tile_stride) {
+        const TileInfo ti = decode_tile<TT>(t, p, c.prefix, c.offs);
+        for (int i = q; i < nk; i += PIPES, ++jq) {
+            if (jq < pre) continue;
+            const int s = stage_of(jq);
+            if (!mbar_wait(&c.empty[s], ((jq / S) & 1) ^ 1, p.wait_ns)) {
+                record_timeout(c.abort_flag);
+                stop = true;
+                break;
+            }
+            issue_w(ti, c.kb_begin + i, s);
+            if (!c.fused) issue_a(ti, c.kb_begin + i, s);
+        }
+    }
+    // Drain: the last use of each stage must have landed before exit.
+    const int issued = jq > pre ? jq : pre;
+    for (int j = issued - 1; j >= 0 && j >= issued - S; --j) {
+        (void)mbar_wait(&c.full[stage_of(j)], (j / S) & 1, kDrainNs);
+        if (!c.fused) (void)mbar_wait(&c.sfraw[stage_of(j)], (j / S) & 1, kDrainNs);
+    }
+}
+
+template <int TT, int PIPES>
+__device__ __forceinline__ void run_mma(const GemmArgs& p, const Ctx& c, int q) {
+    using G = Geometry<TT>;
+    // Descriptors of stage 0; stage s adds s * kStageBytes (the start address
+    // field is address >> 4 and never carries: shared memory < 256 KB).
+    const uint64_t a_desc0 = desc_kmajor_sw128(smem_addr(c.smem + G::kOffW));
+    const uint64_t b_desc0 = desc_kmajor_sw128(smem_addr(c.smem + G::kOffA));
+    const uint64_t wsf_desc0 = desc_sf_32x16(smem_addr(c.smem + G::kOffWsf));
+    const uint64_t asf_desc0 = desc_sf_32x16(smem_addr(c.smem + G::kOffAsfT));
+    constexpr uint64_t kStageStep = static_cast<uint64_t>(G::kStageBytes >> 4);
+    const int nk = c.kb_end - c.kb_begin;
+    const int S = c.stages;
+    const uint32_t acc = c.tmem_base + q * TT;
+    int jq = 0;
+    int tile_iter = 0;
+    for (int t = c.tile_first; t < c.num_tiles; t += c.tile_stride, ++tile_iter) {
+        const TileInfo ti = decode_tile<TT>(t, p, c.prefix, c.offs);
+        const uint32_t n_mma = static_cast<uint32_t>((ti.count + 15) & ~15);
+        uint32_t idesc[4];
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) idesc[kk] = idesc_mxf8(128, n_mma, kk, kk);
+        // Every pipe waits for the epilogue to drain the previous tile, so the
+        // accumulator barrier can never run two phases ahead of any pipe.
+        if (tile_iter > 0 && !mbar_wait(c.acc_empty, (tile_iter - 1) & 1, p.wait_ns)) {
+            record_timeout(c.abort_flag);
+            break;
+        }
+        tc_fence_after();
+        bool stop = false;
+        for (int i = q; i < nk; i += PIPES, ++jq) {
+            const int s = q * S + jq % S;
+            if (!mbar_wait(&c.full[s], (jq / S) & 1, p.wait_ns)) {
+                record_timeout(c.abort_flag);
+                stop = true;
+                break;
+            }
+            const uint64_t sd = static_cast<uint64_t>(s) * kStageStep;
+            const uint32_t sfa = c.tmem_base + PIPES * TT + s * G::kSfSlotCols;
+            const uint32_t sfb = sfa + 4;
+            tmem_copy_sf(sfa, wsf_desc0 + sd);
+#pragma unroll
+            for (int ch = 0; ch < G::kSfChunks; ++ch) tmem_copy_sf(sfb + 4 * ch, asf_desc0 + sd + ch * 32);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                mma_mxf8(acc, a_desc0 + sd + 2 * kk, b_desc0 + sd + 2 * kk, idesc[kk], sfa, sfb,
+                         (i > q || kk > 0) ? 1u : 0u);
+            mma_commit(&c.empty[s]);
+        }
+        if (stop) break;
+        mma_commit(c.acc_full);  // also for a pipe with no K block in this tile
+    }
+    // Drain every MMA this thread issued before TMEM is released.
+    mma_commit(&c.drain[q]);
+    (void)mbar_wait(&c.drain[q], 0, kDrainNs);
+}
+
+template <int TT, int PIPES>
+__device__ __forceinline__ void run_reorder(const GemmArgs& p, const Ctx& c, int lane) {
+    using G = Geometry<TT>;
+    const int nk = c.kb_end - c.kb_begin;
+    const int S = c.stages;
+    int tile_iter = 0;
+    for (int t = c.tile_first; t < c.num_tiles; t += c.tile_stride, ++tile_iter) {
+        const TileInfo ti = decode_tile<TT>(t, p, c.prefix, c.offs);
+        const int off8 = ti.tok0 & 7;
+        for (int i = 0; i < nk; ++i) {
+            const int q = i % PIPES;
+            const int jq = tile_iter * pipe_jobs<PIPES>(q, nk) + i / PIPES;
+            const int s = q * S + jq % S;
+            bool ok = mbar_wait(&c.sfraw[s], (jq / S) & 1, p.wait_ns);
+            ok = __all_sync(0xFFFFFFFFu, ok ? 1 : 0) != 0;
+            if (!ok) {
+                if (lane == 0) record_timeout(c.abort_flag);
+                return;
+            }
+            uint8_t* st = c.smem + s * G::kStageBytes;
+            // Token j of the tile is word (off8 + j) of the raw 8x4 groups; the
+            // TMEM-copy order puts token j of each 128-chunk at word
+            // (j%32)*4 + (j%128)/32.
+            const uint32_t* raw = reinterpret_cast<const uint32_t*>(st + G::kOffAsfRaw);
+#pragma unroll
+            for (int ch = 0; ch < G::kSfChunks; ++ch) {
+                uint32_t w[4];
+#pragma unroll
+                for (int jq4 = 0; jq4 < 4; ++jq4) {
+                    const int j = ch * 128 + jq4 * 32 + lane;
+                    w[jq4] = (j < TT) ? raw[off8 + j] : 0u;
+                }
+                *reinterpret_cast<uint4*>(st + G::kOffAsfT + ch * 512 + lane * 16) =
+                    make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&c.full[s]);
+        }
+    }
+}
+
+// Fused activation quantizer (one tile per CTA): each pass of a warp
+// quantizes 8 (row, block) pairs; lanes 4g..4g+3 hold the 32 values of one
+// block.  Passes of all K blocks are flattened and their loads issued in
+// batches of 8 before any is quantized.
+template <int TT, int PIPES>
+__device__ __forceinline__ void run_fused_quant(const GemmArgs& p, const Ctx& c, int ew, int lane) {
+    using G = Geometry<TT>;
+    pdl_wait();
+    const TileInfo ti = decode_tile<TT>(c.tile_first, p, c.prefix, c.offs);
+    const int nk = c.kb_end - c.kb_begin;
+    const int S = c.stages;
+    constexpr int kPasses = TT / 16;  // passes per K block per warp
+    const int total = nk * kPasses;
+    for (int p0 = 0; p0 < total; p0 += 8) {
+        uint4 raw[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int ps = p0 + u;
+            const int i = ps / kPasses;
+            const int pr = ((ps - i * kPasses) * kEpilogueWarps + ew) * 8 + (lane >> 2);
+            const int row = pr >> 2;
+            const int col = (c.kb_begin + i) * 128 + (pr & 3) * 32 + (lane & 3) * 8;
+            raw[u] = make_uint4(0, 0, 0, 0);
+            if (ps < total && row < ti.count)
+                raw[u] = *reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(ti.tok0 + row) * p.k + col);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int ps = p0 + u;
+            if (ps >= total) break;  // warp-uniform
+            const int i = ps / kPasses;
+            const int pass = ps - i * kPasses;
+            const int q = i % PIPES;
+            const int jq = i / PIPES;
+            const int s = q * S + jq % S;
+            if (pass == 0 && jq >= S) {
+                bool ok = mbar_wait(&c.empty[s], ((jq / S) & 1) ^ 1, p.wait_ns);
+                ok = __all_sync(0xFFFFFFFFu, ok ? 1 : 0) != 0;
+                if (!ok) {
+                    if (lane == 0) record_timeout(c.abort_flag);
+                    return;
+                }
+            }
+            uint8_t* st = c.smem + s * G::kStageBytes;
+            const int pr = (pass * kEpilogueWarps + ew) * 8 + (lane >> 2);
+            const int row = pr >> 2;
+            const int byte = (pr & 3) * 32 + (lane & 3) * 8;  // within the 128-byte K block
+            float v[8];
+            bf16x8_to_float(raw[u], v);
+            uint2 q8;
+            uint32_t sc;
+            quantize_lane8(v, q8, sc);
+            const int chunk = byte >> 4;  // 128-byte swizzle: chunk ^= row % 8
+            st_shared_v2(st + G::kOffA + row * 128 + ((chunk ^ (row & 7)) << 4) + (byte & 15), q8);
+            const uint32_t word = gather_scale_word(sc);
+            if ((lane & 15) == 0) {
+                const int rr = row & 127;
+                *reinterpret_cast<uint32_t*>(st + G::kOffAsfT + (row >> 7) * 512 + (rr & 31) * 16 +
+                                             (rr >> 5) * 4) = word;
+            }
+            if (pass == kPasses - 1) {
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&c.full[s]);
+            }
+        }
+    }
+}
+
+// Small token tiles with one pipe keep registers low enough for two CTAs
+// per SM.
+template <int TT, int PIPES>
+__global__ void __launch_bounds__(32 * num_warps(PIPES), (TT <= 64 && PIPES == 1 ? 2 : 1))
+    mxfp8_gemm_kernel(const __grid_constant__ GemmArgs p) {
     using G = Geometry<TT>;
     extern __shared__ uint8_t smem_dyn[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -173,25 +441,31 @@ __global__ void __launch_bounds__(kThreads, (TT <= 64 ? 2 : 1)) mxfp8_gemm_kerne
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int stages = p.stages;
+    const int S = p.stages;          // per pipe
+    const int ST = PIPES * S;        // all stages
     const int splits = p.splits;
     const bool reduce = splits > 1;
     const bool fused = p.x != nullptr;
     const int per = tokens_per_owner(TT, splits);
 
-    uint8_t* partial = smem + stages * G::kStageBytes;  // split-K partials [splits][128][per] f32
+    uint8_t* partial = smem + ST * G::kStageBytes;  // split-K partials [splits][128][per] f32
     uint8_t* ctrl = partial + (reduce ? splits * per * 512 : 0);
-    uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
-    uint64_t* empty = full + stages;
-    uint64_t* acc_full = empty + stages;
-    uint64_t* acc_empty = acc_full + 1;
-    uint64_t* drain = acc_empty + 1;
-    uint64_t* sfraw = drain + 1;          // raw activation scales landed
-    uint64_t* sfok = sfraw + stages;      // re-ordered scales written
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sfok + stages);
-    volatile uint32_t* abort_flag = tmem_slot + 1;
+    Ctx c;
+    c.smem = smem;
+    c.full = reinterpret_cast<uint64_t*>(ctrl);
+    c.empty = c.full + ST;
+    c.sfraw = c.empty + ST;
+    c.acc_full = c.sfraw + ST;
+    c.acc_empty = c.acc_full + 1;
+    c.drain = c.acc_empty + 1;  // [PIPES]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(c.drain + PIPES);
+    c.abort_flag = tmem_slot + 1;
     int* prefix = reinterpret_cast<int*>(tmem_slot + 2);   // [experts + 1]
     int* offs = prefix + (kMaxExperts + 1);                 // [experts + 1]
+    c.prefix = prefix;
+    c.offs = offs;
+    c.stages = S;
+    c.fused = fused;
 
     // ---------------------------------------------------------------- setup
     if (warp == 0 && lane == 0) {
@@ -200,16 +474,17 @@ __global__ void __launch_bounds__(kThreads, (TT <= 64 ? 2 : 1)) mxfp8_gemm_kerne
             tma_prefetch_desc(&p.map_a);
             tma_prefetch_desc(&p.map_asf);
         }
-        for (int s = 0; s < stages; ++s) {
-            mbar_init(&full[s], fused ? 1 + kEpilogueWarps : 1);
-            mbar_init(&empty[s], 1);
-            mbar_init(&sfraw[s], 1);
-            mbar_init(&sfok[s], 1);
+        for (int s = 0; s < ST; ++s) {
+            // full: the producer's arrival (+ TMA bytes) and either the eight
+            // fused-quantizer warps or the scale re-order warp.
+            mbar_init(&c.full[s], fused ? 1 + kEpilogueWarps : 2);
+            mbar_init(&c.empty[s], 1);
+            mbar_init(&c.sfraw[s], 1);
         }
-        mbar_init(acc_full, 1);
-        mbar_init(acc_empty, kEpilogueWarps);
-        mbar_init(drain, 1);
-        *abort_flag = 0u;
+        mbar_init(c.acc_full, PIPES);
+        mbar_init(c.acc_empty, kEpilogueWarps);
+        for (int q = 0; q < PIPES; ++q) mbar_init(&c.drain[q], 1);
+        *c.abort_flag = 0u;
         fence_barrier_init();
     }
     if (warp == 1) tmem_alloc(tmem_slot, p.tmem_cols);
@@ -243,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, (TT <= 64 ? 2 : 1)) mxfp8_gemm_kerne
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem_base = *tmem_slot;
+    c.tmem_base = *tmem_slot;
     // Peers must have started before any DSMEM store: arrive now, wait just
     // before the first remote access.
     if (reduce) cluster_arrive_relaxed();
@@ -251,335 +526,108 @@ __global__ void __launch_bounds__(kThreads, (TT <= 64 ? 2 : 1)) mxfp8_gemm_kerne
     float b_red = 0.0f;  // split-K owners: bias of their output feature
 
     // Work assignment: a list of (tile, K range).
-    int tile_first, tile_stride, num_tiles, kb_begin, kb_end, rank = 0;
+    int rank = 0;
     if (!p.persistent) {
         rank = reduce ? static_cast<int>(cluster_rank()) : 0;
-        tile_first = reduce ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
-        tile_stride = 1 << 30;
-        num_tiles = tile_first + 1;
-        kb_begin = (rank * p.kq) / splits;
-        kb_end = ((rank + 1) * p.kq) / splits;
+        c.tile_first = reduce ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
+        c.tile_stride = 1 << 30;
+        c.num_tiles = c.tile_first + 1;
+        c.kb_begin = (rank * p.kq) / splits;
+        c.kb_end = ((rank + 1) * p.kq) / splits;
     } else {
-        tile_first = blockIdx.x;
-        tile_stride = gridDim.x;
-        num_tiles = (p.offsets == nullptr) ? p.num_tiles : prefix[p.experts];
-        kb_begin = 0;
-        kb_end = p.kq;
+        c.tile_first = blockIdx.x;
+        c.tile_stride = gridDim.x;
+        c.num_tiles = (p.offsets == nullptr) ? p.num_tiles : prefix[p.experts];
+        c.kb_begin = 0;
+        c.kb_end = p.kq;
     }
+    const int nk = c.kb_end - c.kb_begin;
 
-    if (warp == 0) {
-        // ------------------------------------------------------- producer
-        if (lane == 0) {
-            const uint64_t pol_w = policy_evict_normal();
-            const uint64_t pol_a = policy_evict_last();
-            // Weight bytes of the first `stages` jobs are issued before waiting
-            // for the previous grid: only the activations depend on it.
-            int pre = 0;
-            {
-                int t = tile_first;
-                for (; pre < stages && t < num_tiles;) {
-                    const TileInfo ti = decode_tile<TT>(t, p, prefix, offs);
-                    const int nloads = (ti.count + p.box_rows - 1) / p.box_rows;
-                    const uint32_t bytes = 16384u + 512u +
-                        (fused ? 0u : static_cast<uint32_t>(nloads * p.box_rows * 128));
-                    for (int kb = kb_begin; kb < kb_end && pre < stages; ++kb, ++pre) {
-                        const int s = pre;
-                        uint8_t* st = smem + s * G::kStageBytes;
-                        mbar_arrive_expect_tx(&full[s], bytes);
-                        tma_load_2d(st + G::kOffW, &p.map_w, kb * 128,
-                                    ti.e * p.n_pad + ti.n_tile * 128, &full[s], pol_w);
-                        bulk_load(st + G::kOffWsf,
-                                  p.wsf + ((static_cast<size_t>(ti.e) * p.n_tiles + ti.n_tile) * p.kq + kb) * 512,
-                                  512, &full[s], pol_w);
-                    }
-                    if (pre < stages) t += tile_stride;
-                }
-            }
-            if (!fused) {
-                pdl_wait();
-                int t = tile_first, issued = 0;
-                for (; issued < pre;) {
-                    const TileInfo ti = decode_tile<TT>(t, p, prefix, offs);
-                    const int nloads = (ti.count + p.box_rows - 1) / p.box_rows;
-                    for (int kb = kb_begin; kb < kb_end && issued < pre; ++kb, ++issued) {
-                        const int s = issued;
-                        uint8_t* st = smem + s * G::kStageBytes;
-                        for (int l = 0; l < nloads; ++l)
-                            tma_load_2d(st + G::kOffA + l * p.box_rows * 128, &p.map_a, kb * 128,
-                                        ti.tok0 + l * p.box_rows, &full[s], pol_a);
-                        mbar_arrive_expect_tx(&sfraw[s], static_cast<uint32_t>(p.sf_groups * 32));
-                        tma_load_2d(st + G::kOffAsfRaw, &p.map_asf, kb * 32, ti.tok0 >> 3, &sfraw[s],
-                                    pol_a);
-                    }
-                    t += tile_stride;
-                }
-            }
-            // Steady state.
-            int job = 0;
-            bool stop = false;
-            for (int t = tile_first; t < num_tiles && !stop; t += tile_stride) {
-                const TileInfo ti = decode_tile<TT>(t, p, prefix, offs);
-                const int nloads = (ti.count + p.box_rows - 1) / p.box_rows;
-                const uint32_t bytes = 16384u + 512u +
-                    (fused ? 0u : static_cast<uint32_t>(nloads * p.box_rows * 128));
-                for (int kb = kb_begin; kb < kb_end; ++kb, ++job) {
-                    if (job < pre) continue;
-                    if (*abort_flag) { stop = true; break; }
-                    const int s = job % stages;
-                    const int round = job / stages;
-                    if (!mbar_wait(&empty[s], (round & 1) ^ 1, p.wait_ns)) {
-                        record_timeout(abort_flag);
-                        stop = true;
-                        break;
-                    }
-                    uint8_t* st = smem + s * G::kStageBytes;
-                    mbar_arrive_expect_tx(&full[s], bytes);
-                    tma_load_2d(st + G::kOffW, &p.map_w, kb * 128, ti.e * p.n_pad + ti.n_tile * 128,
-                                &full[s], pol_w);
-                    bulk_load(st + G::kOffWsf,
-                              p.wsf + ((static_cast<size_t>(ti.e) * p.n_tiles + ti.n_tile) * p.kq + kb) * 512,
-                              512, &full[s], pol_w);
-                    if (!fused) {
-                        for (int l = 0; l < nloads; ++l)
-                            tma_load_2d(st + G::kOffA + l * p.box_rows * 128, &p.map_a, kb * 128,
-                                        ti.tok0 + l * p.box_rows, &full[s], pol_a);
-                        mbar_arrive_expect_tx(&sfraw[s], static_cast<uint32_t>(p.sf_groups * 32));
-                        tma_load_2d(st + G::kOffAsfRaw, &p.map_asf, kb * 32, ti.tok0 >> 3, &sfraw[s], pol_a);
-                    }
-                }
-            }
-            // Drain: the last use of each stage must have landed before exit.
-            const int issued_jobs = job > pre ? job : pre;
-            for (int j = issued_jobs - 1; j >= 0 && j >= issued_jobs - stages; --j) {
-                (void)mbar_wait(&full[j % stages], (j / stages) & 1, kDrainNs);
-                if (!fused) (void)mbar_wait(&sfraw[j % stages], (j / stages) & 1, kDrainNs);
-            }
-        }
+    if (warp == 0 || (warp >= 11 && warp < 10 + PIPES)) {
+        if (lane == 0) run_producer<TT, PIPES>(p, c, warp == 0 ? 0 : warp - 10);
         __syncwarp();
-    } else if (warp == 1) {
-        // ------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            // Descriptors of stage 0; stage s adds s * kStageBytes (the start
-            // address field is address >> 4 and never carries: smem < 256 KB).
-            const uint64_t a_desc0 = desc_kmajor_sw128(smem_addr(smem + G::kOffW));
-            const uint64_t b_desc0 = desc_kmajor_sw128(smem_addr(smem + G::kOffA));
-            const uint64_t wsf_desc0 = desc_sf_32x16(smem_addr(smem + G::kOffWsf));
-            const uint64_t asf_desc0 = desc_sf_32x16(smem_addr(smem + G::kOffAsfT));
-            constexpr uint64_t kStageStep = static_cast<uint64_t>(G::kStageBytes >> 4);
-            int s = 0;
-            uint32_t phase = 0;
-            int tile_iter = 0;
-            bool stop = false;
-            for (int t = tile_first; t < num_tiles && !stop; t += tile_stride, ++tile_iter) {
-                const TileInfo ti = decode_tile<TT>(t, p, prefix, offs);
-                const uint32_t n_mma = static_cast<uint32_t>((ti.count + 15) & ~15);
-                uint32_t idesc[4];
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) idesc[kk] = idesc_mxf8(128, n_mma, kk, kk);
-                if (tile_iter > 0 && !mbar_wait(acc_empty, (tile_iter - 1) & 1, p.wait_ns)) {
-                    record_timeout(abort_flag);
-                    break;
-                }
-                for (int kb = kb_begin; kb < kb_end; ++kb) {
-                    if (!mbar_wait(&full[s], phase, p.wait_ns) ||
-                        (!fused && !mbar_wait(&sfok[s], phase, p.wait_ns))) {
-                        record_timeout(abort_flag);
-                        stop = true;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint64_t sd = static_cast<uint64_t>(s) * kStageStep;
-                    const uint32_t sfa = tmem_base + TT + s * G::kSfSlotCols;
-                    const uint32_t sfb = sfa + 4;
-                    tmem_copy_sf(sfa, wsf_desc0 + sd);
-#pragma unroll
-                    for (int c = 0; c < G::kSfChunks; ++c) tmem_copy_sf(sfb + 4 * c, asf_desc0 + sd + c * 32);
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_mxf8(tmem_base, a_desc0 + sd + 2 * kk, b_desc0 + sd + 2 * kk, idesc[kk], sfa, sfb,
-                                 (kb > kb_begin || kk > 0) ? 1u : 0u);
-                    mma_commit(&empty[s]);
-                    if (kb == kb_end - 1) mma_commit(acc_full);
-                    if (++s == stages) { s = 0; phase ^= 1u; }
-                }
-            }
-            // Drain every MMA this thread issued before TMEM is released.
-            mma_commit(drain);
-            (void)mbar_wait(drain, 0, kDrainNs);
-        }
+    } else if (warp == 1 || (warp >= 10 + PIPES && warp < num_warps(PIPES))) {
+        if (lane == 0) run_mma<TT, PIPES>(p, c, warp == 1 ? 0 : warp - (10 + PIPES) + 1);
         __syncwarp();
     } else if (warp == 10) {
-        // ------------------------------------------- activation-scale reorder
-        if (!fused) {
-            int s = 0;
-            uint32_t phase = 0;
-            bool stop = false;
-            for (int t = tile_first; t < num_tiles && !stop; t += tile_stride) {
-                const TileInfo ti = decode_tile<TT>(t, p, prefix, offs);
-                const int off8 = ti.tok0 & 7;
-                for (int kb = kb_begin; kb < kb_end; ++kb) {
-                    bool ok = mbar_wait(&sfraw[s], phase, p.wait_ns);
-                    ok = __all_sync(0xFFFFFFFFu, ok ? 1 : 0) != 0;
-                    if (!ok) {
-                        if (lane == 0) record_timeout(abort_flag);
-                        stop = true;
-                        break;
-                    }
-                    uint8_t* st = smem + s * G::kStageBytes;
-                    const uint32_t* raw = reinterpret_cast<const uint32_t*>(st + G::kOffAsfRaw);
-#pragma unroll
-                    for (int c = 0; c < G::kSfChunks; ++c) {
-                        uint32_t w[4];
-#pragma unroll
-                        for (int jq = 0; jq < 4; ++jq) {
-                            const int j = c * 128 + jq * 32 + lane;
-                            w[jq] = (j < TT) ? raw[off8 + j] : 0u;
-                        }
-                        *reinterpret_cast<uint4*>(st + G::kOffAsfT + c * 512 + lane * 16) =
-                            make_uint4(w[0], w[1], w[2], w[3]);
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&sfok[s]);
-                    if (++s == stages) { s = 0; phase ^= 1u; }
-                }
-            }
-        }
+        if (!fused) run_reorder<TT, PIPES>(p, c, lane);
         __syncwarp();
     } else {
         const int ew = warp - 2;  // warps 2..9
         // Bias of the output feature this thread finishes in the split-K
         // reduction, fetched before anything else so its latency hides.
         if (reduce && p.bias) {
-            const TileInfo t0 = decode_tile<TT>(tile_first, p, prefix, offs);
+            const TileInfo t0 = decode_tile<TT>(c.tile_first, p, prefix, offs);
             const int n_red = t0.n_tile * 128 + ((threadIdx.x - 64) & 127);
             if (n_red < p.n) b_red = __bfloat162float(p.bias[static_cast<size_t>(t0.e) * p.n + n_red]);
         }
-        // ---------------------------------------- fused activation quantizer
-        if (fused) {
-            // One tile per CTA.  Each pass of a warp quantizes 8 (row, block)
-            // pairs: lanes 4g..4g+3 hold the 32 values of one block.  Passes
-            // of all K blocks are flattened and their loads issued in batches
-            // of 8 before any is quantized.
-            pdl_wait();
-            const TileInfo ti = decode_tile<TT>(tile_first, p, prefix, offs);
-            constexpr int kPasses = TT / 16;  // passes per K block per warp
-            const int total = (kb_end - kb_begin) * kPasses;
-            bool ok = true;
-            for (int p0 = 0; p0 < total && ok; p0 += 8) {
-                uint4 raw[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int ps = p0 + u;
-                    const int job = ps / kPasses;
-                    const int pr = ((ps - job * kPasses) * kEpilogueWarps + ew) * 8 + (lane >> 2);
-                    const int row = pr >> 2;
-                    const int col = (kb_begin + job) * 128 + (pr & 3) * 32 + (lane & 3) * 8;
-                    raw[u] = make_uint4(0, 0, 0, 0);
-                    if (ps < total && row < ti.count)
-                        raw[u] = *reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(ti.tok0 + row) * p.k + col);
-                }
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int ps = p0 + u;
-                    if (ps >= total) break;  // warp-uniform
-                    const int job = ps / kPasses;
-                    const int pass = ps - job * kPasses;
-                    const int s = job % stages;
-                    if (pass == 0 && job >= stages) {
-                        ok = mbar_wait(&empty[s], ((job / stages) & 1) ^ 1, p.wait_ns);
-                        ok = __all_sync(0xFFFFFFFFu, ok ? 1 : 0) != 0;
-                        if (!ok) { if (lane == 0) record_timeout(abort_flag); break; }
-                    }
-                    uint8_t* st = smem + s * G::kStageBytes;
-                    const int pr = (pass * kEpilogueWarps + ew) * 8 + (lane >> 2);
-                    const int row = pr >> 2;
-                    const int byte = (pr & 3) * 32 + (lane & 3) * 8;  // within the 128-byte K block
-                    float v[8];
-                    bf16x8_to_float(raw[u], v);
-                    uint2 q8;
-                    uint32_t sc;
-                    quantize_lane8(v, q8, sc);
-                    const int chunk = byte >> 4;  // 128-byte swizzle: chunk ^= row % 8
-                    st_shared_v2(st + G::kOffA + row * 128 + ((chunk ^ (row & 7)) << 4) + (byte & 15), q8);
-                    const uint32_t word = gather_scale_word(sc);
-                    if ((lane & 15) == 0) {
-                        const int rr = row & 127;
-                        *reinterpret_cast<uint32_t*>(st + G::kOffAsfT + (row >> 7) * 512 + (rr & 31) * 16 +
-                                                     (rr >> 5) * 4) = word;
-                    }
-                    if (pass == kPasses - 1) {
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&full[s]);
-                    }
-                }
-            }
-        }
+        if (fused) run_fused_quant<TT, PIPES>(p, c, ew, lane);
         // ------------------------------------------------------- epilogue
         const int quad = warp & 3;             // TMEM lanes [32*quad, 32*quad + 32)
         const int half = ew >> 2;              // token columns [half*TT/2, (half+1)*TT/2)
         constexpr int kCols = TT / 2;
         const int col0 = half * kCols;
+        const int n_active = nk < PIPES ? nk : PIPES;
         int tile_iter = 0;
-        for (int t = tile_first; t < num_tiles; t += tile_stride, ++tile_iter) {
+        for (int t = c.tile_first; t < c.num_tiles; t += c.tile_stride, ++tile_iter) {
             const TileInfo ti = decode_tile<TT>(t, p, prefix, offs);
             const int nl = quad * 32 + lane;  // weight row within the tile
             const int n = ti.n_tile * 128 + nl;
             const float b = (!reduce && p.bias && n < p.n)
                                 ? __bfloat162float(p.bias[static_cast<size_t>(ti.e) * p.n + n]) : 0.0f;
-            bool ok = mbar_wait(acc_full, tile_iter & 1, p.wait_ns);
+            bool ok = mbar_wait(c.acc_full, tile_iter & 1, p.wait_ns);
             ok = __all_sync(0xFFFFFFFFu, ok ? 1 : 0) != 0;
-            if (!ok) { if (lane == 0) record_timeout(abort_flag); break; }
+            if (!ok) { if (lane == 0) record_timeout(c.abort_flag); break; }
             tc_fence_after();
-            uint32_t acc[kCols];
-            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + col0;
-            if constexpr (kCols >= 32) {
+            float acc[kCols];
 #pragma unroll
-                for (int c = 0; c < kCols / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_load_32(taddr + c * 32, r);
+            for (int i = 0; i < kCols; ++i) acc[i] = 0.0f;
+            for (int q = 0; q < n_active; ++q) {  // pipe order: deterministic sums
+                const uint32_t taddr = c.tmem_base + q * TT + (static_cast<uint32_t>(quad * 32) << 16) + col0;
+                uint32_t r[kCols];
+                if constexpr (kCols >= 32) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) acc[c * 32 + i] = r[i];
+                    for (int cc = 0; cc < kCols / 32; ++cc) {
+                        uint32_t r32[32];
+                        tmem_load_32(taddr + cc * 32, r32);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) r[cc * 32 + i] = r32[i];
+                    }
+                } else if constexpr (kCols == 16) {
+                    tmem_load_16(taddr, r);
+                } else {
+                    tmem_load_8(taddr, r);
                 }
-            } else if constexpr (kCols == 16) {
-                uint32_t r[16];
-                tmem_load_16(taddr, r);
+                tmem_load_wait();
 #pragma unroll
-                for (int i = 0; i < 16; ++i) acc[i] = r[i];
-            } else {
-                uint32_t r[8];
-                tmem_load_8(taddr, r);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) acc[i] = r[i];
+                for (int i = 0; i < kCols; ++i) acc[i] += __uint_as_float(r[i]);
             }
-            tmem_load_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(acc_empty);
+            if (lane == 0) mbar_arrive(c.acc_empty);
 
             if (reduce) {
-                // Push: token columns c..c+3 go to rank c / per as one 16-byte
-                // store into its slot [rank][nl][c % per].
+                // Push: token columns j..j+3 go to rank j / per as one 16-byte
+                // store into its slot [rank][nl][j % per].
                 __syncwarp();
                 cluster_wait();
                 cluster_waited = true;
                 const uint32_t pbase = smem_addr(partial);
 #pragma unroll
                 for (int j = 0; j < kCols; j += 4) {
-                    const int c = col0 + j;
-                    const int owner = c / per;
-                    const uint32_t a = pbase + static_cast<uint32_t>(((rank * 128 + nl) * per + (c - owner * per)) * 4);
-                    st_cluster_v4(map_to_rank(a, static_cast<uint32_t>(owner)), acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+                    const int col = col0 + j;
+                    const int owner = col / per;
+                    const uint32_t a = pbase + static_cast<uint32_t>(((rank * 128 + nl) * per + (col - owner * per)) * 4);
+                    st_cluster_v4(map_to_rank(a, static_cast<uint32_t>(owner)), __float_as_uint(acc[j]),
+                                  __float_as_uint(acc[j + 1]), __float_as_uint(acc[j + 2]),
+                                  __float_as_uint(acc[j + 3]));
                 }
-            } else {
-                if (n < p.n) {
-                    const int jmax = min(kCols, ti.count - col0);
-                    __nv_bfloat16* yp = p.y + static_cast<size_t>(ti.tok0 + col0) * p.n + n;
+            } else if (n < p.n) {
+                const int jmax = min(kCols, ti.count - col0);
+                __nv_bfloat16* yp = p.y + static_cast<size_t>(ti.tok0 + col0) * p.n + n;
 #pragma unroll
-                    for (int j = 0; j < kCols; ++j)
-                        if (j < jmax) yp[static_cast<size_t>(j) * p.n] = __float2bfloat16_rn(__uint_as_float(acc[j]) + b);
-                }
+                for (int j = 0; j < kCols; ++j)
+                    if (j < jmax) yp[static_cast<size_t>(j) * p.n] = __float2bfloat16_rn(acc[j] + b);
             }
         }
         __syncwarp();
@@ -591,26 +639,26 @@ __global__ void __launch_bounds__(kThreads, (TT <= 64 ? 2 : 1)) mxfp8_gemm_kerne
         if (!__all_sync(0xFFFFFFFFu, cluster_waited ? 1 : 0)) cluster_wait();
         cluster_sync();  // every rank's pushes have landed
         const bool epi = warp >= 2 && warp < 2 + kEpilogueWarps;
-        if (epi && !*abort_flag) {
+        if (epi && !*c.abort_flag) {
             // Owner: tokens [rank*per, rank*per + per), four per thread and step,
             // summed over source ranks in rank order.
-            const TileInfo ti = decode_tile<TT>(tile_first, p, prefix, offs);
+            const TileInfo ti = decode_tile<TT>(c.tile_first, p, prefix, offs);
             const int et = threadIdx.x - 64;
             const int nl = et & 127;
             const int n = ti.n_tile * 128 + nl;
             const float* part = reinterpret_cast<const float*>(partial);
             const int j0 = rank * per;
-            for (int q = et >> 7; q < per / 4; q += (kEpilogueWarps * 32) / 128) {
+            for (int qq = et >> 7; qq < per / 4; qq += (kEpilogueWarps * 32) / 128) {
                 float4 sum = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
                 for (int r = 0; r < splits; ++r) {
-                    const float4 v = *reinterpret_cast<const float4*>(part + (r * 128 + nl) * per + q * 4);
+                    const float4 v = *reinterpret_cast<const float4*>(part + (r * 128 + nl) * per + qq * 4);
                     sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
                 }
                 const float sv[4] = {sum.x, sum.y, sum.z, sum.w};
                 if (n < p.n) {
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        const int j = j0 + q * 4 + i;
+                        const int j = j0 + qq * 4 + i;
                         if (j < ti.count && j < TT)
                             p.y[static_cast<size_t>(ti.tok0 + j) * p.n + n] = __float2bfloat16_rn(sv[i] + b_red);
                     }
@@ -624,7 +672,7 @@ __global__ void __launch_bounds__(kThreads, (TT <= 64 ? 2 : 1)) mxfp8_gemm_kerne
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, p.tmem_cols);
+        tmem_dealloc(c.tmem_base, p.tmem_cols);
     }
 }
 
@@ -667,38 +715,40 @@ uint32_t pow2_cols(int need) {
     return c;
 }
 
-template <int TT>
 struct LaunchPlan {
-    int stages;
+    int stages;  // per pipe
     uint32_t tmem_cols;
     size_t smem;
     int partial;
 };
 
-template <int TT>
-LaunchPlan<TT> plan_for(int splits, bool persistent, int kq) {
+template <int TT, int PIPES>
+LaunchPlan plan_for(int splits, bool persistent, int kq) {
     using G = Geometry<TT>;
-    LaunchPlan<TT> lp;
+    LaunchPlan lp;
     // Pipeline depth: as many stages as fit next to the partial buffer and
-    // control block (a one-tile CTA never needs more than its K blocks).
+    // control block, at most 8 in all, split evenly between the pipes (a
+    // one-tile CTA never needs more than its K blocks).
     const int ctrl = 8 * 64 + 8 + 4 * 2 * (kMaxExperts + 1) + 64;  // barriers, slots, prefix/offsets
     lp.partial = splits > 1 ? splits * tokens_per_owner(TT, splits) * 512 : 0;
     const int budget = 227 * 1024 - 1024 - ctrl - lp.partial;
-    int stages = budget / G::kStageBytes;
-    if (stages > 8) stages = 8;
+    int stages = budget / (PIPES * G::kStageBytes);
+    if (stages * PIPES > 8) stages = 8 / PIPES;
     if (!persistent) {
         const int nk = (kq + splits - 1) / splits;
-        if (stages > nk) stages = nk;
+        const int nq = (nk + PIPES - 1) / PIPES;
+        if (stages > nq) stages = nq;
     }
     lp.stages = stages;
-    lp.tmem_cols = pow2_cols(TT + stages * G::kSfSlotCols);
-    lp.smem = 1024 + static_cast<size_t>(stages) * G::kStageBytes + lp.partial + ctrl;
+    lp.tmem_cols = pow2_cols(PIPES * TT + PIPES * stages * G::kSfSlotCols);
+    lp.smem = 1024 + static_cast<size_t>(PIPES * stages) * G::kStageBytes + lp.partial + ctrl;
     return lp;
 }
 
-template <int TT>
+template <int TT, int PIPES>
 cudaError_t launch_tt(const GemmProblem& pr, const GemmSchedule& sch, int num_sms, cudaStream_t s,
                       bool* encode_failed) {
+    constexpr int kThreads = 32 * num_warps(PIPES);
     using G = Geometry<TT>;
     GemmArgs a;
     memset(&a, 0, sizeof(a));
@@ -721,7 +771,7 @@ cudaError_t launch_tt(const GemmProblem& pr, const GemmSchedule& sch, int num_sm
     const int tok_tiles = static_cast<int>((pr.m + TT - 1) / TT);
     const int n_tiles = static_cast<int>(pr.n_pad / 128);
     const int splits = sch.persistent ? 1 : sch.split_k;
-    const LaunchPlan<TT> lp = plan_for<TT>(splits, sch.persistent, kq);
+    const LaunchPlan lp = plan_for<TT, PIPES>(splits, sch.persistent, kq);
     if (lp.stages < 1) return cudaErrorInvalidConfiguration;
 
     a.wsf = pr.wsf;
@@ -743,14 +793,14 @@ cudaError_t launch_tt(const GemmProblem& pr, const GemmSchedule& sch, int num_sm
     a.wait_ns = g_wait_limit_ns ? g_wait_limit_ns : kWaitNs;
     const size_t smem = lp.smem;
 
-    cudaError_t err = cudaFuncSetAttribute(mxfp8_gemm_kernel<TT>,
+    cudaError_t err = cudaFuncSetAttribute(mxfp8_gemm_kernel<TT, PIPES>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;
 
     // TMEM is never oversubscribed: co-resident CTAs x columns <= 512.
     int per_sm = 1;
-    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mxfp8_gemm_kernel<TT>, kThreads, smem);
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mxfp8_gemm_kernel<TT, PIPES>, kThreads, smem);
     if (err != cudaSuccess) return err;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     if (static_cast<uint32_t>(per_sm) * a.tmem_cols > 512u) return cudaErrorInvalidConfiguration;
@@ -787,15 +837,19 @@ cudaError_t launch_tt(const GemmProblem& pr, const GemmSchedule& sch, int num_sm
     ++na;
     cfg.attrs = attrs;
     cfg.numAttrs = na;
-    t_last_schedule[0] = TT;
+    t_last_schedule[0] = TT + 1000 * (PIPES - 1);
     t_last_schedule[1] = sch.persistent ? -1 : splits;
     t_last_schedule[2] = fused ? 1 : 0;
     t_last_schedule[3] = grid;
     t_last_schedule[4] = lp.stages;
-    return cudaLaunchKernelEx(&cfg, mxfp8_gemm_kernel<TT>, a);
+    return cudaLaunchKernelEx(&cfg, mxfp8_gemm_kernel<TT, PIPES>, a);
 }
 
 }  // namespace
+
+int g_force_pipes = 0;
+
+void set_pipes(int pipes) { g_force_pipes = (pipes == 1 || pipes == 2 || pipes == 4) ? pipes : 0; }
 
 GemmSchedule choose_schedule(const GemmProblem& p, int num_sms, int force_tt, int force_split,
                              int force_fuse) {
@@ -803,9 +857,11 @@ GemmSchedule choose_schedule(const GemmProblem& p, int num_sms, int force_tt, in
     const int64_t kq = p.k / 128;
     int tt;
     if (p.offsets != nullptr) {
-        // grouped: size the token tile to the mean segment (rounded up)
+        // Grouped: a token tile of at least twice the mean segment, so that
+        // most experts' weights stream once (measured on the 128-expert
+        // gate_up workload: 32-token tiles for a mean of 16 rows).
         const int64_t mean = (p.m + p.experts - 1) / (p.experts > 0 ? p.experts : 1);
-        tt = mean <= 16 ? 16 : mean <= 32 ? 32 : mean <= 64 ? 64 : mean <= 128 ? 128 : 256;
+        tt = 2 * mean <= 16 ? 16 : 2 * mean <= 32 ? 32 : 2 * mean <= 64 ? 64 : mean <= 128 ? 128 : 256;
     } else {
         // Up to 128 tokens the 64-token tile with split-K measured fastest
         // (more CTAs stream weights at once); above, persistent 256-token tiles.
@@ -841,18 +897,43 @@ GemmSchedule choose_schedule(const GemmProblem& p, int num_sms, int force_tt, in
     sch.split_k = persistent ? 1 : split;
     sch.persistent = persistent;
     sch.fuse_quant = fuse;
+    // Two MMA pipelines per CTA where the per-thread issue cost bounds the
+    // stream of weights: grouped tiles of <= 64 tokens, and 64-token one-tile
+    // schedules that still fit one CTA per SM (measured; at 16 tokens the
+    // two-CTA-per-SM single-pipe schedule is as fast).
+    int pipes = 1;
+    if (p.offsets != nullptr && tt <= 64) pipes = 2;
+    if (p.offsets == nullptr && !persistent && tt == 64 &&
+        (p.n_pad / 128) * ((p.m + tt - 1) / tt) * split <= num_sms)
+        pipes = 2;
+    if (g_force_pipes) pipes = g_force_pipes;
+    if (pipes == 2 && tt > 64) pipes = 1;
+    if (pipes == 4 && tt != 16) pipes = tt <= 64 ? 2 : 1;
+    sch.pipes = pipes;
     return sch;
 }
 
 cudaError_t launch_gemm(const GemmProblem& p, const GemmSchedule& sch, int num_sms, cudaStream_t s,
                         bool* encode_failed) {
     *encode_failed = false;
+    if (sch.pipes == 2) {
+        switch (sch.tokens_per_tile) {
+            case 16: return launch_tt<16, 2>(p, sch, num_sms, s, encode_failed);
+            case 32: return launch_tt<32, 2>(p, sch, num_sms, s, encode_failed);
+            case 64: return launch_tt<64, 2>(p, sch, num_sms, s, encode_failed);
+            default: return cudaErrorInvalidValue;
+        }
+    }
+    if (sch.pipes == 4) {
+        if (sch.tokens_per_tile == 16) return launch_tt<16, 4>(p, sch, num_sms, s, encode_failed);
+        return cudaErrorInvalidValue;
+    }
     switch (sch.tokens_per_tile) {
-        case 16: return launch_tt<16>(p, sch, num_sms, s, encode_failed);
-        case 32: return launch_tt<32>(p, sch, num_sms, s, encode_failed);
-        case 64: return launch_tt<64>(p, sch, num_sms, s, encode_failed);
-        case 128: return launch_tt<128>(p, sch, num_sms, s, encode_failed);
-        case 256: return launch_tt<256>(p, sch, num_sms, s, encode_failed);
+        case 16: return launch_tt<16, 1>(p, sch, num_sms, s, encode_failed);
+        case 32: return launch_tt<32, 1>(p, sch, num_sms, s, encode_failed);
+        case 64: return launch_tt<64, 1>(p, sch, num_sms, s, encode_failed);
+        case 128: return launch_tt<128, 1>(p, sch, num_sms, s, encode_failed);
+        case 256: return launch_tt<256, 1>(p, sch, num_sms, s, encode_failed);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -37,7 +37,11 @@ struct GemmSchedule {
     int split_k;               // CTAs (a cluster) per output tile, K split among them
     bool persistent;           // tiles strided over a persistent grid (split_k == 1)
     bool fuse_quant;           // the GEMM quantizes x itself (one-tile schedules)
+    int pipes;                 // MMA pipelines per CTA (1, 2 or 4; >1 only for <= 64 tokens)
 };
+
+// Testing hook: pipelines per CTA for later launches (0 = automatic).
+void set_pipes(int pipes);
 
 // force_tt: 0 or a token tile; force_split: 0 auto, -1 persistent, >0 split;
 // force_fuse: -1 auto, 0 off, 1 on where possible.

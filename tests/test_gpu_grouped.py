@@ -21,16 +21,18 @@ def _oracle_expert_weights(w):
     return wq, wsf
 
 
-def _run_grouped(mx, g, rows=None, schedule=(0, 0, -1)):
+def _run_grouped(mx, g, rows=None, schedule=(0, 0, -1), pipes=0):
     pw = mx.prepare_weight(to_dev_f32(g.w))
     x = to_dev_bf16(g.x_sorted)
     off = torch.from_numpy(g.offsets).cuda()
     b = None if g.bias is None else to_dev_bf16(g.bias)
     mx.set_schedule(*schedule)
+    mx.set_pipes(pipes)
     try:
         y = mx.grouped_linear(x, off, pw, b)
     finally:
         mx.set_schedule(0, 0, -1)
+        mx.set_pipes(0)
     torch.cuda.synchronize()
     wq, wsf = _oracle_expert_weights(g.w)
     y_ref = oracle.grouped_linear(g.x_sorted, g.offsets, wq, wsf, g.bias, rows=rows)
@@ -57,6 +59,12 @@ def test_grouped_edge_segments(lib, tt):
     ragged N, bias."""
     g = workloads.grouped_from_counts([5, 0, 300, 1, 0, 17, 40, 0], n=260, k=512, seed=51, bias=True)
     _run_grouped(lib, g, schedule=(tt, 0, -1))
+
+
+@pytest.mark.parametrize("tt,pipes", [(16, 2), (16, 4), (32, 2), (64, 2)])
+def test_grouped_multi_pipe(lib, tt, pipes):
+    g = workloads.grouped_from_counts([5, 0, 300, 1, 0, 17, 40, 0], n=260, k=512, seed=53, bias=True)
+    _run_grouped(lib, g, schedule=(tt, 0, -1), pipes=pipes)
 
 
 def test_grouped_all_rows_one_expert(lib):

@@ -13,15 +13,19 @@ from gpu_common import assert_close_to_oracle, oracle_weight, to_dev_bf16, to_de
 pytestmark = pytest.mark.gpu
 
 
-def _run_dense(mx, d, rows=None, schedule=(0, 0, -1)):
+def _run_dense(mx, d, rows=None, schedule=(0, 0, -1), pipes=0):
     pw = mx.prepare_weight(to_dev_f32(d.w))
     x = to_dev_bf16(d.x)
     b = None if d.bias is None else to_dev_bf16(d.bias)
     mx.set_schedule(*schedule)
+    mx.set_pipes(pipes)
     try:
         y = mx.linear(x, pw, b)
+        if pipes:
+            assert mx.last_schedule()["pipes"] == pipes
     finally:
         mx.set_schedule(0, 0, -1)
+        mx.set_pipes(0)
     torch.cuda.synchronize()
     assert y.shape == (d.m, d.n) and y.is_contiguous()
     wq, wsf = oracle_weight(d.w)
@@ -84,6 +88,24 @@ def test_every_schedule(lib, tt, split, fuse):
     tail."""
     d = workloads.dense(m=300, n=390, k=1024, seed=30, bias=True)
     _run_dense(lib, d, schedule=(tt, split, fuse))
+
+
+@pytest.mark.parametrize("tt,split,fuse,pipes", [
+    (16, -1, 0, 2), (16, -1, 0, 4), (16, 2, 1, 2), (16, 4, 1, 4), (16, 1, 0, 4), (32, 2, 1, 2),
+    (32, -1, 0, 2), (64, 4, 0, 2), (64, -1, 0, 2), (64, 2, 1, 2)])
+def test_multi_pipe_schedules(lib, tt, split, fuse, pipes):
+    """Several MMA pipelines per CTA (each every pipes-th K block, own
+    accumulator, summed in pipe order), persistent and split-K, fused or not;
+    K = 1024 gives 8 K blocks, also fewer than one per pipe under split 4."""
+    d = workloads.dense(m=300, n=390, k=1024, seed=33, bias=True)
+    _run_dense(lib, d, schedule=(tt, split, fuse), pipes=pipes)
+
+
+def test_multi_pipe_fewer_k_blocks_than_pipes(lib):
+    """K = 256 is 2 K blocks: with 4 pipelines two of them idle."""
+    d = workloads.dense(m=40, n=256, k=256, seed=34, bias=True)
+    _run_dense(lib, d, schedule=(16, -1, 0), pipes=4)
+    _run_dense(lib, d, schedule=(16, 1, 1), pipes=4)
 
 
 @pytest.mark.parametrize("m,n,k", [(1, 128, 256), (2, 130, 256), (17, 384, 512), (33, 260, 1024),
