@@ -70,7 +70,6 @@ namespace {
 
 constexpr uint64_t kWaitNs = 4000000000ull;   // default: 4 s per wait, then give up
 constexpr uint64_t kDrainNs = 200000000ull;   // 0.2 s per drain wait
-constexpr int kEpilogueWarps = 8;
 constexpr int kMaxExperts = 1024;
 
 struct GemmArgs {
@@ -159,17 +158,20 @@ __device__ __forceinline__ void st_shared_v2(void* p, uint2 v) {
 }
 
 // ----------------------------------------------------------------- kernel
-// Warp roles for PIPES pipelines:
-//   0                      producer of pipe 0      (lane 0)
-//   1                      MMA issuer of pipe 0    (lane 0); TMEM alloc/free
-//   2 .. 9                 epilogue (and fused activation quantizer)
-//   10                     activation-scale re-order (unfused)
-//   11 .. 9+PIPES          producers of pipes 1..PIPES-1
-//   10+PIPES .. 8+2*PIPES  MMA issuers of pipes 1..PIPES-1
+// Warp roles for PIPES pipelines and E = epi_warps(TT) epilogue warps:
+//   0                          producer of pipe 0      (lane 0)
+//   1                          MMA issuer of pipe 0    (lane 0); TMEM alloc/free
+//   2 .. 1+E                   epilogue (and fused activation quantizer)
+//   2+E                        activation-scale re-order (unfused)
+//   3+E .. 1+E+PIPES           producers of pipes 1..PIPES-1
+//   2+E+PIPES .. E+2*PIPES     MMA issuers of pipes 1..PIPES-1
 // Pipe q owns the local K blocks i with i % PIPES == q of every tile, its own
 // ring of `stages` shared-memory stages and its own TMEM accumulator; the
 // epilogue sums the accumulators in pipe order.
-__host__ __device__ constexpr int num_warps(int pipes) { return 11 + 2 * (pipes - 1); }
+// Epilogue warps: one per TMEM lane quadrant for tiles of <= 32 tokens (so
+// that two CTAs with two pipelines fit one SM), two per quadrant above.
+__host__ __device__ constexpr int epi_warps(int tt) { return tt <= 32 ? 4 : 8; }
+__host__ __device__ constexpr int num_warps(int tt, int pipes) { return 3 + epi_warps(tt) + 2 * (pipes - 1); }
 
 struct Ctx {
     uint8_t* smem;
@@ -367,7 +369,8 @@ __device__ __forceinline__ void run_fused_quant(const GemmArgs& p, const Ctx& c,
     const TileInfo ti = decode_tile<TT>(c.tile_first, p, c.prefix, c.offs);
     const int nk = c.kb_end - c.kb_begin;
     const int S = c.stages;
-    constexpr int kPasses = TT / 16;  // passes per K block per warp
+    constexpr int kEpi = epi_warps(TT);
+    constexpr int kPasses = TT * 4 / (kEpi * 8);  // passes per K block per warp
     const int total = nk * kPasses;
     for (int p0 = 0; p0 < total; p0 += 8) {
         uint4 raw[8];
@@ -375,7 +378,7 @@ __device__ __forceinline__ void run_fused_quant(const GemmArgs& p, const Ctx& c,
         for (int u = 0; u < 8; ++u) {
             const int ps = p0 + u;
             const int i = ps / kPasses;
-            const int pr = ((ps - i * kPasses) * kEpilogueWarps + ew) * 8 + (lane >> 2);
+            const int pr = ((ps - i * kPasses) * kEpi + ew) * 8 + (lane >> 2);
             const int row = pr >> 2;
             const int col = (c.kb_begin + i) * 128 + (pr & 3) * 32 + (lane & 3) * 8;
             raw[u] = make_uint4(0, 0, 0, 0);
@@ -400,7 +403,7 @@ __device__ __forceinline__ void run_fused_quant(const GemmArgs& p, const Ctx& c,
                 }
             }
             uint8_t* st = c.smem + s * G::kStageBytes;
-            const int pr = (pass * kEpilogueWarps + ew) * 8 + (lane >> 2);
+            const int pr = (pass * kEpi + ew) * 8 + (lane >> 2);
             const int row = pr >> 2;
             const int byte = (pr & 3) * 32 + (lane & 3) * 8;  // within the 128-byte K block
             float v[8];
@@ -428,9 +431,12 @@ __device__ __forceinline__ void run_fused_quant(const GemmArgs& p, const Ctx& c,
 // Small token tiles with one pipe keep registers low enough for two CTAs
 // per SM.
 template <int TT, int PIPES>
-__global__ void __launch_bounds__(32 * num_warps(PIPES), (TT <= 64 && PIPES == 1 ? 2 : 1))
+__global__ void __launch_bounds__(32 * num_warps(TT, PIPES),
+                                  ((TT <= 64 && PIPES == 1) || (TT <= 32 && PIPES == 2)) ? 2 : 1)
     mxfp8_gemm_kernel(const __grid_constant__ GemmArgs p) {
     using G = Geometry<TT>;
+    constexpr int kEpi = epi_warps(TT);
+    constexpr int kReorderWarp = 2 + kEpi;
     extern __shared__ uint8_t smem_dyn[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -477,12 +483,12 @@ __global__ void __launch_bounds__(32 * num_warps(PIPES), (TT <= 64 && PIPES == 1
         for (int s = 0; s < ST; ++s) {
             // full: the producer's arrival (+ TMA bytes) and either the eight
             // fused-quantizer warps or the scale re-order warp.
-            mbar_init(&c.full[s], fused ? 1 + kEpilogueWarps : 2);
+            mbar_init(&c.full[s], fused ? 1 + kEpi : 2);
             mbar_init(&c.empty[s], 1);
             mbar_init(&c.sfraw[s], 1);
         }
         mbar_init(c.acc_full, PIPES);
-        mbar_init(c.acc_empty, kEpilogueWarps);
+        mbar_init(c.acc_empty, kEpi);
         for (int q = 0; q < PIPES; ++q) mbar_init(&c.drain[q], 1);
         *c.abort_flag = 0u;
         fence_barrier_init();
@@ -543,17 +549,17 @@ __global__ void __launch_bounds__(32 * num_warps(PIPES), (TT <= 64 && PIPES == 1
     }
     const int nk = c.kb_end - c.kb_begin;
 
-    if (warp == 0 || (warp >= 11 && warp < 10 + PIPES)) {
-        if (lane == 0) run_producer<TT, PIPES>(p, c, warp == 0 ? 0 : warp - 10);
+    if (warp == 0 || (warp > kReorderWarp && warp < kReorderWarp + PIPES)) {
+        if (lane == 0) run_producer<TT, PIPES>(p, c, warp == 0 ? 0 : warp - kReorderWarp);
         __syncwarp();
-    } else if (warp == 1 || (warp >= 10 + PIPES && warp < num_warps(PIPES))) {
-        if (lane == 0) run_mma<TT, PIPES>(p, c, warp == 1 ? 0 : warp - (10 + PIPES) + 1);
+    } else if (warp == 1 || (warp >= kReorderWarp + PIPES && warp < num_warps(TT, PIPES))) {
+        if (lane == 0) run_mma<TT, PIPES>(p, c, warp == 1 ? 0 : warp - (kReorderWarp + PIPES) + 1);
         __syncwarp();
-    } else if (warp == 10) {
+    } else if (warp == kReorderWarp) {
         if (!fused) run_reorder<TT, PIPES>(p, c, lane);
         __syncwarp();
     } else {
-        const int ew = warp - 2;  // warps 2..9
+        const int ew = warp - 2;  // warps 2 .. 1+kEpi
         // Bias of the output feature this thread finishes in the split-K
         // reduction, fetched before anything else so its latency hides.
         if (reduce && p.bias) {
@@ -564,8 +570,8 @@ __global__ void __launch_bounds__(32 * num_warps(PIPES), (TT <= 64 && PIPES == 1
         if (fused) run_fused_quant<TT, PIPES>(p, c, ew, lane);
         // ------------------------------------------------------- epilogue
         const int quad = warp & 3;             // TMEM lanes [32*quad, 32*quad + 32)
-        const int half = ew >> 2;              // token columns [half*TT/2, (half+1)*TT/2)
-        constexpr int kCols = TT / 2;
+        const int half = ew >> 2;              // token columns [half*kCols, (half+1)*kCols)
+        constexpr int kCols = TT * 4 / kEpi;
         const int col0 = half * kCols;
         const int n_active = nk < PIPES ? nk : PIPES;
         int tile_iter = 0;
@@ -638,7 +644,7 @@ __global__ void __launch_bounds__(32 * num_warps(PIPES), (TT <= 64 && PIPES == 1
         __syncwarp();
         if (!__all_sync(0xFFFFFFFFu, cluster_waited ? 1 : 0)) cluster_wait();
         cluster_sync();  // every rank's pushes have landed
-        const bool epi = warp >= 2 && warp < 2 + kEpilogueWarps;
+        const bool epi = warp >= 2 && warp < 2 + kEpi;
         if (epi && !*c.abort_flag) {
             // Owner: tokens [rank*per, rank*per + per), four per thread and step,
             // summed over source ranks in rank order.
@@ -648,7 +654,7 @@ __global__ void __launch_bounds__(32 * num_warps(PIPES), (TT <= 64 && PIPES == 1
             const int n = ti.n_tile * 128 + nl;
             const float* part = reinterpret_cast<const float*>(partial);
             const int j0 = rank * per;
-            for (int qq = et >> 7; qq < per / 4; qq += (kEpilogueWarps * 32) / 128) {
+            for (int qq = et >> 7; qq < per / 4; qq += (kEpi * 32) / 128) {
                 float4 sum = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
                 for (int r = 0; r < splits; ++r) {
                     const float4 v = *reinterpret_cast<const float4*>(part + (r * 128 + nl) * per + qq * 4);
@@ -748,7 +754,7 @@ LaunchPlan plan_for(int splits, bool persistent, int kq) {
 template <int TT, int PIPES>
 cudaError_t launch_tt(const GemmProblem& pr, const GemmSchedule& sch, int num_sms, cudaStream_t s,
                       bool* encode_failed) {
-    constexpr int kThreads = 32 * num_warps(PIPES);
+    constexpr int kThreads = 32 * num_warps(TT, PIPES);
     using G = Geometry<TT>;
     GemmArgs a;
     memset(&a, 0, sizeof(a));
@@ -898,11 +904,12 @@ GemmSchedule choose_schedule(const GemmProblem& p, int num_sms, int force_tt, in
     sch.persistent = persistent;
     sch.fuse_quant = fuse;
     // Two MMA pipelines per CTA where the per-thread issue cost bounds the
-    // stream of weights: grouped tiles of <= 64 tokens, and 64-token one-tile
-    // schedules that still fit one CTA per SM (measured; at 16 tokens the
-    // two-CTA-per-SM single-pipe schedule is as fast).
+    // stream of weights (measured): grouped tiles of <= 64 tokens; one-tile
+    // schedules of <= 32 tokens (two such CTAs fit an SM); 64-token one-tile
+    // schedules that still fit one CTA per SM.
     int pipes = 1;
     if (p.offsets != nullptr && tt <= 64) pipes = 2;
+    if (p.offsets == nullptr && !persistent && tt <= 32) pipes = 2;
     if (p.offsets == nullptr && !persistent && tt == 64 &&
         (p.n_pad / 128) * ((p.m + tt - 1) / tt) * split <= num_sms)
         pipes = 2;
