@@ -682,6 +682,289 @@ __global__ void __launch_bounds__(32 * num_warps(TT, PIPES),
     }
 }
 
+// ------------------------------------------------------- dual-tile kernel
+// Large-M dense schedule.  A CTA tile is two adjacent 128-row weight tiles
+// (256 output features) x TT tokens.  The token tile and its scales are loaded
+// once per K block and serve both weight tiles; one MMA-issuing thread per
+// weight tile runs over all K blocks into its own TMEM accumulator.  Both
+// issuers feed the same tensor core, so together they keep it busy although
+// each pays a fixed cost per tcgen05 instruction.
+//   warp 0       producer (lane 0): both weight tiles, both scale tiles, the
+//                token tile, the raw 8x4 token scales
+//   warps 1, 11  MMA issuers of weight tile 0 / 1 (lane 0); warp 1 owns TMEM
+//   warps 2..9   epilogue: warp 2+e serves accumulator e/4, lane quadrant
+//                warp%4, 32 token columns at a time
+//   warp 10      token-scale re-order into the TMEM-copy order
+template <int TT>
+struct DualGeometry {
+    static constexpr int kSfChunks = (TT + 127) / 128;
+    static constexpr int kOffW0 = 0;
+    static constexpr int kOffW1 = 16384;
+    static constexpr int kOffA = 32768;
+    static constexpr int kOffWsf0 = kOffA + TT * 128;
+    static constexpr int kOffWsf1 = kOffWsf0 + 512;
+    static constexpr int kOffAsfRaw = kOffWsf1 + 512;
+    static constexpr int kOffAsfT = kOffAsfRaw + 1152;
+    static constexpr int kStageBytes = ((kOffAsfT + 512 * kSfChunks) + 1023) / 1024 * 1024;
+    static constexpr int kSlotCols = 4 + 4 * kSfChunks;  // per pipe per stage
+};
+
+constexpr int kDualThreads = 12 * 32;
+
+// Dense tiles over (weight-tile pair, token tile), token tiles banded by 8 so
+// a band's weights stay in L2.
+template <int TT>
+__device__ __forceinline__ TileInfo decode_dual(int t, const GemmArgs& p) {
+    const int pairs = (p.n_tiles + 1) >> 1;
+    const int tok_tiles = (p.m + TT - 1) / TT;
+    constexpr int kBand = 8;
+    const int band_size = kBand * pairs;
+    const int band = t / band_size;
+    const int r = t - band * band_size;
+    const int g = min(kBand, tok_tiles - band * kBand);
+    const int tt = band * kBand + r % g;
+    TileInfo ti;
+    ti.e = 0;
+    ti.n_tile = 2 * (r / g);  // first of the pair
+    ti.tok0 = tt * TT;
+    ti.count = min(TT, p.m - ti.tok0);
+    return ti;
+}
+
+template <int TT>
+__global__ void __launch_bounds__(kDualThreads, 1) mxfp8_gemm_dual_kernel(const __grid_constant__ GemmArgs p) {
+    using G = DualGeometry<TT>;
+    extern __shared__ uint8_t smem_dyn[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~static_cast<uintptr_t>(1023));
+    pdl_launch_dependents();
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int S = p.stages;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * G::kStageBytes);
+    uint64_t* empty = full + S;
+    uint64_t* sfraw = empty + S;
+    uint64_t* acc_full = sfraw + S;
+    uint64_t* acc_empty = acc_full + 1;
+    uint64_t* drain = acc_empty + 1;  // [2]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 2);
+    volatile uint32_t* abort_flag = tmem_slot + 1;
+
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&p.map_w);
+        tma_prefetch_desc(&p.map_a);
+        tma_prefetch_desc(&p.map_asf);
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 2);   // producer (+ bytes), re-order warp
+            mbar_init(&empty[s], 2);  // both MMA issuers
+            mbar_init(&sfraw[s], 1);
+        }
+        mbar_init(acc_full, 2);
+        mbar_init(acc_empty, 8);
+        mbar_init(&drain[0], 1);
+        mbar_init(&drain[1], 1);
+        *abort_flag = 0u;
+        fence_barrier_init();
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, p.tmem_cols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int tile_first = blockIdx.x;
+    const int tile_stride = gridDim.x;
+    const int num_tiles = p.num_tiles;
+    const int nk = p.kq;
+
+    if (warp == 0) {
+        // ------------------------------------------------------- producer
+        if (lane == 0) {
+            const uint64_t pol_w = policy_evict_normal();
+            const uint64_t pol_a = policy_evict_last();
+            auto issue_w = [&](const TileInfo& ti, int kb, int s) {
+                uint8_t* st = smem + s * G::kStageBytes;
+                const bool has1 = ti.n_tile + 1 < p.n_tiles;
+                mbar_arrive_expect_tx(&full[s], 2u * 16384u + (has1 ? 1024u : 512u) +
+                                                    static_cast<uint32_t>(TT * 128));
+                tma_load_2d(st + G::kOffW0, &p.map_w, kb * 128, ti.n_tile * 128, &full[s], pol_w);
+                tma_load_2d(st + G::kOffW1, &p.map_w, kb * 128, (ti.n_tile + 1) * 128, &full[s], pol_w);
+                bulk_load(st + G::kOffWsf0, p.wsf + (static_cast<size_t>(ti.n_tile) * p.kq + kb) * 512, 512,
+                          &full[s], pol_w);
+                if (has1)
+                    bulk_load(st + G::kOffWsf1, p.wsf + (static_cast<size_t>(ti.n_tile + 1) * p.kq + kb) * 512,
+                              512, &full[s], pol_w);
+            };
+            auto issue_a = [&](const TileInfo& ti, int kb, int s) {
+                uint8_t* st = smem + s * G::kStageBytes;
+                tma_load_2d(st + G::kOffA, &p.map_a, kb * 128, ti.tok0, &full[s], pol_a);
+                mbar_arrive_expect_tx(&sfraw[s], static_cast<uint32_t>(p.sf_groups * 32));
+                tma_load_2d(st + G::kOffAsfRaw, &p.map_asf, kb * 32, ti.tok0 >> 3, &sfraw[s], pol_a);
+            };
+            int pre = 0;
+            for (int t = tile_first; t < num_tiles && pre < S; t += tile_stride) {
+                const TileInfo ti = decode_dual<TT>(t, p);
+                for (int kb = 0; kb < nk && pre < S; ++kb, ++pre) issue_w(ti, kb, pre);
+            }
+            pdl_wait();
+            {
+                int j = 0;
+                for (int t = tile_first; t < num_tiles && j < pre; t += tile_stride) {
+                    const TileInfo ti = decode_dual<TT>(t, p);
+                    for (int kb = 0; kb < nk && j < pre; ++kb, ++j) issue_a(ti, kb, j);
+                }
+            }
+            int job = 0;
+            bool stop = false;
+            for (int t = tile_first; t < num_tiles && !stop; t += tile_stride) {
+                const TileInfo ti = decode_dual<TT>(t, p);
+                for (int kb = 0; kb < nk; ++kb, ++job) {
+                    if (job < pre) continue;
+                    const int s = job % S;
+                    if (!mbar_wait(&empty[s], ((job / S) & 1) ^ 1, p.wait_ns)) {
+                        record_timeout(abort_flag);
+                        stop = true;
+                        break;
+                    }
+                    issue_w(ti, kb, s);
+                    issue_a(ti, kb, s);
+                }
+            }
+            const int issued = job > pre ? job : pre;
+            for (int j = issued - 1; j >= 0 && j >= issued - S; --j) {
+                (void)mbar_wait(&full[j % S], (j / S) & 1, kDrainNs);
+                (void)mbar_wait(&sfraw[j % S], (j / S) & 1, kDrainNs);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1 || warp == 11) {
+        // ------------------------------------------------------- MMA issuers
+        if (lane == 0) {
+            const int q = warp == 1 ? 0 : 1;
+            const uint64_t a_desc0 = desc_kmajor_sw128(smem_addr(smem + (q ? G::kOffW1 : G::kOffW0)));
+            const uint64_t b_desc0 = desc_kmajor_sw128(smem_addr(smem + G::kOffA));
+            const uint64_t wsf_desc0 = desc_sf_32x16(smem_addr(smem + (q ? G::kOffWsf1 : G::kOffWsf0)));
+            const uint64_t asf_desc0 = desc_sf_32x16(smem_addr(smem + G::kOffAsfT));
+            constexpr uint64_t kStageStep = static_cast<uint64_t>(G::kStageBytes >> 4);
+            const uint32_t acc = tmem_base + q * TT;
+            int job = 0, tile_iter = 0;
+            for (int t = tile_first; t < num_tiles; t += tile_stride, ++tile_iter) {
+                const TileInfo ti = decode_dual<TT>(t, p);
+                const uint32_t n_mma = static_cast<uint32_t>((ti.count + 15) & ~15);
+                uint32_t idesc[4];
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) idesc[kk] = idesc_mxf8(128, n_mma, kk, kk);
+                if (tile_iter > 0 && !mbar_wait(acc_empty, (tile_iter - 1) & 1, p.wait_ns)) {
+                    record_timeout(abort_flag);
+                    break;
+                }
+                tc_fence_after();
+                bool stop = false;
+                for (int kb = 0; kb < nk; ++kb, ++job) {
+                    const int s = job % S;
+                    if (!mbar_wait(&full[s], (job / S) & 1, p.wait_ns)) {
+                        record_timeout(abort_flag);
+                        stop = true;
+                        break;
+                    }
+                    const uint64_t sd = static_cast<uint64_t>(s) * kStageStep;
+                    const uint32_t sfa = tmem_base + 2 * TT + (s * 2 + q) * G::kSlotCols;
+                    const uint32_t sfb = sfa + 4;
+                    tmem_copy_sf(sfa, wsf_desc0 + sd);
+#pragma unroll
+                    for (int ch = 0; ch < G::kSfChunks; ++ch) tmem_copy_sf(sfb + 4 * ch, asf_desc0 + sd + ch * 32);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_mxf8(acc, a_desc0 + sd + 2 * kk, b_desc0 + sd + 2 * kk, idesc[kk], sfa, sfb,
+                                 (kb > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(&empty[s]);
+                }
+                if (stop) break;
+                mma_commit(acc_full);
+            }
+            mma_commit(&drain[q]);
+            (void)mbar_wait(&drain[q], 0, kDrainNs);
+        }
+        __syncwarp();
+    } else if (warp == 10) {
+        // ------------------------------------------- token-scale re-order
+        int job = 0;
+        bool stop = false;
+        for (int t = tile_first; t < num_tiles && !stop; t += tile_stride) {
+            const TileInfo ti = decode_dual<TT>(t, p);
+            const int off8 = ti.tok0 & 7;
+            for (int kb = 0; kb < nk; ++kb, ++job) {
+                const int s = job % S;
+                bool ok = mbar_wait(&sfraw[s], (job / S) & 1, p.wait_ns);
+                ok = __all_sync(0xFFFFFFFFu, ok ? 1 : 0) != 0;
+                if (!ok) {
+                    if (lane == 0) record_timeout(abort_flag);
+                    stop = true;
+                    break;
+                }
+                uint8_t* st = smem + s * G::kStageBytes;
+                const uint32_t* raw = reinterpret_cast<const uint32_t*>(st + G::kOffAsfRaw);
+#pragma unroll
+                for (int ch = 0; ch < G::kSfChunks; ++ch) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int jq = 0; jq < 4; ++jq) {
+                        const int j = ch * 128 + jq * 32 + lane;
+                        w[jq] = (j < TT) ? raw[off8 + j] : 0u;
+                    }
+                    *reinterpret_cast<uint4*>(st + G::kOffAsfT + ch * 512 + lane * 16) =
+                        make_uint4(w[0], w[1], w[2], w[3]);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&full[s]);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------- epilogue
+        const int ew = warp - 2;
+        const int q = ew >> 2;   // accumulator / weight tile of the pair
+        const int quad = warp & 3;
+        int tile_iter = 0;
+        for (int t = tile_first; t < num_tiles; t += tile_stride, ++tile_iter) {
+            const TileInfo ti = decode_dual<TT>(t, p);
+            const int n = (ti.n_tile + q) * 128 + quad * 32 + lane;
+            const float b = (p.bias && n < p.n) ? __bfloat162float(p.bias[n]) : 0.0f;
+            bool ok = mbar_wait(acc_full, tile_iter & 1, p.wait_ns);
+            ok = __all_sync(0xFFFFFFFFu, ok ? 1 : 0) != 0;
+            if (!ok) { if (lane == 0) record_timeout(abort_flag); break; }
+            tc_fence_after();
+            const uint32_t taddr = tmem_base + q * TT + (static_cast<uint32_t>(quad * 32) << 16);
+            __nv_bfloat16* yp = p.y + static_cast<size_t>(ti.tok0) * p.n + n;
+#pragma unroll 1
+            for (int c0 = 0; c0 < TT; c0 += 32) {
+                uint32_t r[32];
+                tmem_load_32(taddr + c0, r);
+                tmem_load_wait();
+                if (n < p.n) {
+                    const int jmax = min(32, ti.count - c0);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (j < jmax)
+                            yp[static_cast<size_t>(c0 + j) * p.n] = __float2bfloat16_rn(__uint_as_float(r[j]) + b);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty);
+        }
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, p.tmem_cols);
+    }
+}
+
 // ------------------------------------------------------------------- host
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -851,6 +1134,71 @@ cudaError_t launch_tt(const GemmProblem& pr, const GemmSchedule& sch, int num_sm
     return cudaLaunchKernelEx(&cfg, mxfp8_gemm_kernel<TT, PIPES>, a);
 }
 
+template <int TT>
+cudaError_t launch_dual(const GemmProblem& pr, int num_sms, cudaStream_t s, bool* encode_failed) {
+    using G = DualGeometry<TT>;
+    GemmArgs a;
+    memset(&a, 0, sizeof(a));
+    const int64_t m8 = (pr.m + 7) / 8 * 8;
+    a.box_rows = TT;
+    a.sf_groups = TT / 8 + 1;
+    const bool ok = encode_2d_u8(&a.map_w, pr.wq, pr.k, pr.n_pad, pr.k, 128, 128, true) &&
+                    encode_2d_u8(&a.map_a, pr.qa, pr.k, pr.m, pr.k, 128, TT, true) &&
+                    encode_2d_u8(&a.map_asf, pr.sfa, pr.k / 4, m8 / 8, pr.k / 4, 32, a.sf_groups, false);
+    if (!ok) {
+        *encode_failed = true;
+        return cudaErrorInvalidValue;
+    }
+    a.wsf = pr.wsf;
+    a.bias = static_cast<const __nv_bfloat16*>(pr.bias);
+    a.y = static_cast<__nv_bfloat16*>(pr.y);
+    a.m = static_cast<int>(pr.m);
+    a.n = static_cast<int>(pr.n);
+    a.n_pad = static_cast<int>(pr.n_pad);
+    a.k = static_cast<int>(pr.k);
+    a.kq = static_cast<int>(pr.k / 128);
+    a.experts = 1;
+    a.n_tiles = static_cast<int>(pr.n_pad / 128);
+    a.splits = 1;
+    a.persistent = 1;
+    const int ctrl = 1024;
+    int stages = (227 * 1024 - 1024 - ctrl) / G::kStageBytes;
+    if (stages > 6) stages = 6;
+    if (stages < 2) return cudaErrorInvalidConfiguration;
+    a.stages = stages;
+    a.tmem_cols = pow2_cols(2 * TT + stages * 2 * G::kSlotCols);
+    if (a.tmem_cols > 512) return cudaErrorInvalidConfiguration;
+    a.wait_ns = g_wait_limit_ns ? g_wait_limit_ns : kWaitNs;
+    const size_t smem = 1024 + static_cast<size_t>(stages) * G::kStageBytes + ctrl;
+    cudaError_t err = cudaFuncSetAttribute(mxfp8_gemm_dual_kernel<TT>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    int per_sm = 1;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mxfp8_gemm_dual_kernel<TT>, kDualThreads, smem);
+    if (err != cudaSuccess) return err;
+    if (per_sm < 1 || static_cast<uint32_t>(per_sm) * a.tmem_cols > 512u) return cudaErrorInvalidConfiguration;
+    const int tok_tiles = static_cast<int>((pr.m + TT - 1) / TT);
+    a.num_tiles = ((a.n_tiles + 1) / 2) * tok_tiles;
+    const int grid = a.num_tiles < num_sms * per_sm ? a.num_tiles : num_sms * per_sm;
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(kDualThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    t_last_schedule[0] = TT + 1000;
+    t_last_schedule[1] = -2;  // persistent, two weight tiles per CTA tile
+    t_last_schedule[2] = 0;
+    t_last_schedule[3] = grid;
+    t_last_schedule[4] = stages;
+    return cudaLaunchKernelEx(&cfg, mxfp8_gemm_dual_kernel<TT>, a);
+}
+
 }  // namespace
 
 int g_force_pipes = 0;
@@ -874,6 +1222,14 @@ GemmSchedule choose_schedule(const GemmProblem& p, int num_sms, int force_tt, in
         tt = p.m <= 16 ? 16 : p.m <= 32 ? 32 : p.m <= 128 ? 64 : 256;
     }
     if (force_tt) tt = force_tt;
+    // Dense large M: two weight tiles x 192 tokens per CTA tile whenever
+    // that still gives every SM a tile (measured on 8192^3).
+    bool dual = false;
+    if (p.offsets == nullptr && tt == 256 && force_tt == 0 &&
+        ((p.n_pad / 128 + 1) / 2) * ((p.m + 191) / 192) >= num_sms)
+        dual = true;
+    if (p.offsets == nullptr && force_tt == 192) dual = true;
+    if (dual) tt = 192;
     bool persistent = p.offsets != nullptr || tt > 128;
     int split = 1;
     if (!persistent) {
@@ -902,7 +1258,8 @@ GemmSchedule choose_schedule(const GemmProblem& p, int num_sms, int force_tt, in
     sch.tokens_per_tile = tt;
     sch.split_k = persistent ? 1 : split;
     sch.persistent = persistent;
-    sch.fuse_quant = fuse;
+    sch.fuse_quant = fuse && !dual;
+    sch.dual = dual;
     // Two MMA pipelines per CTA where the per-thread issue cost bounds the
     // stream of weights (measured): grouped tiles of <= 64 tokens; one-tile
     // schedules of <= 32 tokens (two such CTAs fit an SM); 64-token one-tile
@@ -923,6 +1280,7 @@ GemmSchedule choose_schedule(const GemmProblem& p, int num_sms, int force_tt, in
 cudaError_t launch_gemm(const GemmProblem& p, const GemmSchedule& sch, int num_sms, cudaStream_t s,
                         bool* encode_failed) {
     *encode_failed = false;
+    if (sch.dual) return launch_dual<192>(p, num_sms, s, encode_failed);
     if (sch.pipes == 2) {
         switch (sch.tokens_per_tile) {
             case 16: return launch_tt<16, 2>(p, sch, num_sms, s, encode_failed);

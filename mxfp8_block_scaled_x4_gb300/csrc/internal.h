@@ -38,6 +38,7 @@ struct GemmSchedule {
     bool persistent;           // tiles strided over a persistent grid (split_k == 1)
     bool fuse_quant;           // the GEMM quantizes x itself (one-tile schedules)
     int pipes;                 // MMA pipelines per CTA (1, 2 or 4; >1 only for <= 64 tokens)
+    bool dual;                 // dense, persistent, two weight tiles x 192 tokens per CTA tile
 };
 
 // Testing hook: pipelines per CTA for later launches (0 = automatic).

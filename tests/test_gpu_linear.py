@@ -80,7 +80,7 @@ def test_vllm_shapes_cosine_and_oracle(lib, shape):
 
 @pytest.mark.parametrize("tt,split,fuse", [
     (16, -1, 0), (16, 1, 1), (16, 4, 1), (16, 4, 0), (32, 2, 1), (32, 3, 0), (64, -1, 0),
-    (64, 8, 1), (64, 8, 0), (128, -1, 0), (128, 4, 0), (128, 2, 1), (256, -1, 0)])
+    (64, 8, 1), (64, 8, 0), (128, -1, 0), (128, 4, 0), (128, 2, 1), (256, -1, 0), (192, -1, 0)])
 def test_every_schedule(lib, tt, split, fuse):
     """Each token-tile size, persistent (-1) or one tile per cluster of `split`
     CTAs, with the activation quantization fused into the GEMM or not, on a
@@ -99,6 +99,15 @@ def test_multi_pipe_schedules(lib, tt, split, fuse, pipes):
     K = 1024 gives 8 K blocks, also fewer than one per pipe under split 4."""
     d = workloads.dense(m=300, n=390, k=1024, seed=33, bias=True)
     _run_dense(lib, d, schedule=(tt, split, fuse), pipes=pipes)
+
+
+@pytest.mark.parametrize("m,n,k", [(300, 300, 1024), (1000, 640, 512), (193, 128, 256)])
+def test_dual_weight_tile_schedule(lib, m, n, k):
+    """Two weight tiles x 192 tokens per CTA tile (the large-M schedule):
+    odd numbers of weight tiles (the pair's second tile out of range), ragged
+    token tails, a single weight tile."""
+    d = workloads.dense(m=m, n=n, k=k, seed=m + n, bias=True)
+    _run_dense(lib, d, schedule=(192, -1, 0))
 
 
 def test_multi_pipe_fewer_k_blocks_than_pipes(lib):
