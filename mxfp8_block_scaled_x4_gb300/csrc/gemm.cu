@@ -742,12 +742,14 @@ __global__ void __launch_bounds__(kDualThreads, 1) mxfp8_gemm_dual_kernel(const 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int S = p.stages;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * G::kStageBytes);
+    // Epilogue staging: one 32 x 32 BF16 block per epilogue warp.
+    uint8_t* stage_out = smem + S * G::kStageBytes;
+    uint64_t* full = reinterpret_cast<uint64_t*>(stage_out + 8 * 2048);
     uint64_t* empty = full + S;
     uint64_t* sfraw = empty + S;
-    uint64_t* acc_full = sfraw + S;
-    uint64_t* acc_empty = acc_full + 1;
-    uint64_t* drain = acc_empty + 1;  // [2]
+    uint64_t* acc_full = sfraw + S;   // [2], one per accumulator
+    uint64_t* acc_empty = acc_full + 2;  // [2]
+    uint64_t* drain = acc_empty + 2;  // [2]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 2);
     volatile uint32_t* abort_flag = tmem_slot + 1;
 
@@ -760,8 +762,10 @@ __global__ void __launch_bounds__(kDualThreads, 1) mxfp8_gemm_dual_kernel(const 
             mbar_init(&empty[s], 2);  // both MMA issuers
             mbar_init(&sfraw[s], 1);
         }
-        mbar_init(acc_full, 2);
-        mbar_init(acc_empty, 8);
+        for (int q = 0; q < 2; ++q) {
+            mbar_init(&acc_full[q], 1);   // its MMA issuer
+            mbar_init(&acc_empty[q], 4);  // its four epilogue warps
+        }
         mbar_init(&drain[0], 1);
         mbar_init(&drain[1], 1);
         *abort_flag = 0u;
@@ -847,22 +851,23 @@ __global__ void __launch_bounds__(kDualThreads, 1) mxfp8_gemm_dual_kernel(const 
             const uint64_t asf_desc0 = desc_sf_32x16(smem_addr(smem + G::kOffAsfT));
             constexpr uint64_t kStageStep = static_cast<uint64_t>(G::kStageBytes >> 4);
             const uint32_t acc = tmem_base + q * TT;
-            int job = 0, tile_iter = 0;
+            int s = 0;
+            uint32_t phase = 0;
+            int tile_iter = 0;
             for (int t = tile_first; t < num_tiles; t += tile_stride, ++tile_iter) {
                 const TileInfo ti = decode_dual<TT>(t, p);
                 const uint32_t n_mma = static_cast<uint32_t>((ti.count + 15) & ~15);
                 uint32_t idesc[4];
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) idesc[kk] = idesc_mxf8(128, n_mma, kk, kk);
-                if (tile_iter > 0 && !mbar_wait(acc_empty, (tile_iter - 1) & 1, p.wait_ns)) {
+                if (tile_iter > 0 && !mbar_wait(&acc_empty[q], (tile_iter - 1) & 1, p.wait_ns)) {
                     record_timeout(abort_flag);
                     break;
                 }
                 tc_fence_after();
                 bool stop = false;
-                for (int kb = 0; kb < nk; ++kb, ++job) {
-                    const int s = job % S;
-                    if (!mbar_wait(&full[s], (job / S) & 1, p.wait_ns)) {
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!mbar_wait(&full[s], phase, p.wait_ns)) {
                         record_timeout(abort_flag);
                         stop = true;
                         break;
@@ -878,9 +883,10 @@ __global__ void __launch_bounds__(kDualThreads, 1) mxfp8_gemm_dual_kernel(const 
                         mma_mxf8(acc, a_desc0 + sd + 2 * kk, b_desc0 + sd + 2 * kk, idesc[kk], sfa, sfb,
                                  (kb > 0 || kk > 0) ? 1u : 0u);
                     mma_commit(&empty[s]);
+                    if (++s == S) { s = 0; phase ^= 1u; }
                 }
                 if (stop) break;
-                mma_commit(acc_full);
+                mma_commit(&acc_full[q]);
             }
             mma_commit(&drain[q]);
             (void)mbar_wait(&drain[q], 0, kDrainNs);
@@ -923,36 +929,56 @@ __global__ void __launch_bounds__(kDualThreads, 1) mxfp8_gemm_dual_kernel(const 
         __syncwarp();
     } else {
         // ------------------------------------------------------- epilogue
+        // 32 token columns at a time: TMEM -> registers (+ bias, BF16) ->
+        // this warp's 32 x 32 staging block transposed -> 16-byte stores of
+        // 64-byte output row segments (scalar stores when N is not a
+        // multiple of 8).
         const int ew = warp - 2;
         const int q = ew >> 2;   // accumulator / weight tile of the pair
         const int quad = warp & 3;
+        __nv_bfloat16* blk = reinterpret_cast<__nv_bfloat16*>(stage_out + ew * 2048);  // [32 tok][32 n]
+        const bool vec = (p.n & 7) == 0 && (reinterpret_cast<uintptr_t>(p.y) & 15) == 0;
         int tile_iter = 0;
         for (int t = tile_first; t < num_tiles; t += tile_stride, ++tile_iter) {
             const TileInfo ti = decode_dual<TT>(t, p);
-            const int n = (ti.n_tile + q) * 128 + quad * 32 + lane;
+            const int n0 = (ti.n_tile + q) * 128 + quad * 32;  // this warp's 32 output features
+            const int n = n0 + lane;
             const float b = (p.bias && n < p.n) ? __bfloat162float(p.bias[n]) : 0.0f;
-            bool ok = mbar_wait(acc_full, tile_iter & 1, p.wait_ns);
+            bool ok = mbar_wait(&acc_full[q], tile_iter & 1, p.wait_ns);
             ok = __all_sync(0xFFFFFFFFu, ok ? 1 : 0) != 0;
             if (!ok) { if (lane == 0) record_timeout(abort_flag); break; }
             tc_fence_after();
             const uint32_t taddr = tmem_base + q * TT + (static_cast<uint32_t>(quad * 32) << 16);
-            __nv_bfloat16* yp = p.y + static_cast<size_t>(ti.tok0) * p.n + n;
 #pragma unroll 1
             for (int c0 = 0; c0 < TT; c0 += 32) {
                 uint32_t r[32];
                 tmem_load_32(taddr + c0, r);
                 tmem_load_wait();
-                if (n < p.n) {
-                    const int jmax = min(32, ti.count - c0);
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        if (j < jmax)
-                            yp[static_cast<size_t>(c0 + j) * p.n] = __float2bfloat16_rn(__uint_as_float(r[j]) + b);
+                if (c0 + 32 >= TT) {  // accumulator fully read: the issuer may go on
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&acc_empty[q]);
                 }
+                if (n0 >= p.n || c0 >= ti.count) continue;  // warp-uniform
+#pragma unroll
+                for (int j = 0; j < 32; ++j) blk[j * 32 + lane] = __float2bfloat16_rn(__uint_as_float(r[j]) + b);
+                __syncwarp();
+                const int jmax = min(32, ti.count - c0);
+                if (vec && n0 + 32 <= p.n) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int j = i * 8 + (lane >> 2);
+                        const int part = lane & 3;
+                        if (j < jmax)
+                            *reinterpret_cast<uint4*>(p.y + static_cast<size_t>(ti.tok0 + c0 + j) * p.n + n0 + part * 8) =
+                                *reinterpret_cast<const uint4*>(blk + j * 32 + part * 8);
+                    }
+                } else if (n < p.n) {
+                    for (int j = 0; j < jmax; ++j)
+                        p.y[static_cast<size_t>(ti.tok0 + c0 + j) * p.n + n] = blk[j * 32 + lane];
+                }
+                __syncwarp();
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(acc_empty);
         }
         __syncwarp();
     }
@@ -1161,7 +1187,7 @@ cudaError_t launch_dual(const GemmProblem& pr, int num_sms, cudaStream_t s, bool
     a.n_tiles = static_cast<int>(pr.n_pad / 128);
     a.splits = 1;
     a.persistent = 1;
-    const int ctrl = 1024;
+    const int ctrl = 1024 + 8 * 2048;  // barriers + epilogue staging
     int stages = (227 * 1024 - 1024 - ctrl) / G::kStageBytes;
     if (stages > 6) stages = 6;
     if (stages < 2) return cudaErrorInvalidConfiguration;

@@ -110,6 +110,30 @@ def test_dual_weight_tile_schedule(lib, m, n, k):
     _run_dense(lib, d, schedule=(192, -1, 0))
 
 
+def test_dual_schedule_unaligned_output(lib):
+    """y only 2-byte aligned (the ABI's minimum): the epilogue must fall back
+    from 16-byte stores."""
+    d = workloads.dense(m=200, n=256, k=256, seed=35, bias=True)
+    pw = lib.prepare_weight(to_dev_f32(d.w))
+    x = to_dev_bf16(d.x)
+    buf = torch.empty(d.m * d.n + 8, dtype=torch.bfloat16, device="cuda")
+    y = buf[1:1 + d.m * d.n].view(d.m, d.n)  # 2-byte offset from a 256-byte aligned base
+    import ctypes
+    lib.set_schedule(192, -1, 0)
+    try:
+        ws = torch.empty(lib.linear_workspace_bytes(d.m, d.k), dtype=torch.uint8, device="cuda")
+        st = lib.library().mxfp8_linear(ctypes.c_void_p(x.data_ptr()), d.m, ctypes.byref(pw.c),
+                                        ctypes.c_void_p(to_dev_bf16(d.bias).data_ptr()),
+                                        ctypes.c_void_p(y.data_ptr()), ctypes.c_void_p(ws.data_ptr()),
+                                        ws.numel(), None)
+        assert st == 0
+        torch.cuda.synchronize()
+    finally:
+        lib.set_schedule(0, 0, -1)
+    wq, wsf = oracle_weight(d.w)
+    assert_close_to_oracle(y, oracle.linear(d.x, wq, wsf, d.bias), "unaligned y")
+
+
 def test_multi_pipe_fewer_k_blocks_than_pipes(lib):
     """K = 256 is 2 K blocks: with 4 pipelines two of them idle."""
     d = workloads.dense(m=40, n=256, k=256, seed=34, bias=True)
