@@ -9,12 +9,12 @@
 //    process_weights_after_loading: quantize, pad N to a multiple of 128,
 //    lay data and scales out for the GEMM).
 //
-// Work unit: one warp quantizes one 256-element chunk of one row (eight
-// 32-blocks, four lanes per block, one 16-byte BF16 load per lane) -- fully
-// coalesced 512-byte reads and 256-byte E4M3 writes per warp.  The four scale
-// bytes of a 4-block group form one aligned 32-bit word in both scale layouts,
-// so each half-warp writes one word.  Both kernels are HBM-bound: grids are
-// sized to the SM count and each warp keeps UNROLL chunks in flight.
+// Work units: the activation kernel gives each lane a whole 32-block of an
+// 8-row x 128-column patch (one 8x4 scale tile per warp); the weight kernel
+// quantizes one 256-element chunk of a row per warp (four lanes per block,
+// one 16-byte load per lane), and each half-warp writes one aligned 32-bit
+// word of the prepared 128x4 scale layout.  Both kernels are HBM-bound: grids
+// are sized to the SM count and each warp keeps several units in flight.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -28,7 +28,7 @@ namespace mxk {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kUnroll = 4;
+constexpr int kUnroll = 2;
 
 __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
     uint4 r;
@@ -42,8 +42,12 @@ __device__ __forceinline__ void st_v2(void* p, uint2 v) {
     asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
 }
 
-// Activations: rows [0, m8) x chunks of 256.  Rows >= m only write their
-// (zero) scale words, which is what the 8x4 layout holds for padding rows.
+// Activations.  One warp quantizes an 8-row x 128-column patch: lane l owns
+// row l/4 of the patch and its 32-block l%4 (64 contiguous BF16 bytes), so
+// the block's amax needs no shuffle, the lane writes its 32 E4M3 bytes as two
+// 16-byte stores, and the patch's 32 scale bytes -- exactly one 8x4 tile, byte
+// (row%8)*4 + block%4 = lane -- go out as one coalesced 32-byte store.  Rows in
+// [m, m8) quantize zeros and write only their (zero) scales.
 __global__ void __launch_bounds__(kThreads) quant_act_kernel(const __nv_bfloat16* __restrict__ x,
                                                              int64_t m, int64_t m8, int64_t k,
                                                              uint8_t* __restrict__ q,
@@ -52,39 +56,41 @@ __global__ void __launch_bounds__(kThreads) quant_act_kernel(const __nv_bfloat16
     // for this grid's completion before reading what it writes.
     pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
-    const int64_t chunks = k >> 8;
-    const int64_t total = m8 * chunks;
-    const int64_t kq = k >> 7;  // 4-block groups per row
+    const int64_t quads = k >> 7;  // 128-column patches per row group
+    const int64_t total = (m8 >> 3) * quads;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
-    int64_t t0 = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
-    for (; t0 < total; t0 += nwarps * kUnroll) {
-        uint4 raw[kUnroll];
-        int64_t row[kUnroll], chunk[kUnroll];
+    const int r8 = lane >> 2;
+    const int b4 = lane & 3;
+    for (int64_t t0 = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5; t0 < total;
+         t0 += nwarps * kUnroll) {
+        uint4 raw[kUnroll][4];
+        int64_t row[kUnroll], col[kUnroll];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
             const int64_t t = t0 + u * nwarps;
-            row[u] = t / chunks;
-            chunk[u] = t - row[u] * chunks;
-            raw[u] = make_uint4(0, 0, 0, 0);
-            if (t < total && row[u] < m)
-                raw[u] = ld_nc_v4(x + row[u] * k + chunk[u] * 256 + lane * 8);
+            const int64_t g = t / quads;
+            row[u] = g * 8 + r8;
+            col[u] = (t - g * quads) * 128 + b4 * 32;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) raw[u][i] = make_uint4(0, 0, 0, 0);
+            if (t < total && row[u] < m) {
+                const __nv_bfloat16* src = x + row[u] * k + col[u];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) raw[u][i] = *reinterpret_cast<const uint4*>(src + i * 8);
+            }
         }
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
             const int64_t t = t0 + u * nwarps;
             if (t >= total) break;  // warp-uniform
-            float v[8];
-            bf16x8_to_float(raw[u], v);
-            uint2 qq;
-            uint32_t s;
-            quantize_lane8(v, qq, s);
-            const uint32_t word = gather_scale_word(s);
-            const int64_t r = row[u];
-            if (r < m) st_v2(q + r * k + chunk[u] * 256 + lane * 8, qq);
-            if ((lane & 15) == 0) {
-                const int64_t grp = chunk[u] * 2 + (lane >> 4);
-                *reinterpret_cast<uint32_t*>(sf + ((r >> 3) * kq + grp) * 32 + (r & 7) * 4) = word;
+            uint32_t qq[8];
+            const uint32_t s = quantize_block32(raw[u], qq);
+            if (row[u] < m) {
+                uint4* dst = reinterpret_cast<uint4*>(q + row[u] * k + col[u]);
+                dst[0] = make_uint4(qq[0], qq[1], qq[2], qq[3]);
+                dst[1] = make_uint4(qq[4], qq[5], qq[6], qq[7]);
             }
+            sf[t * 32 + lane] = static_cast<uint8_t>(s);  // tile (g, quad) = t
         }
     }
 }
@@ -154,7 +160,7 @@ int grid_for(int64_t warps_of_work, int num_sms, int per_warp) {
 cudaError_t launch_quant_act(const void* x, int64_t m, int64_t k, uint8_t* q, uint8_t* sf,
                              int num_sms, cudaStream_t s) {
     const int64_t m8 = (m + 7) / 8 * 8;
-    const int64_t work = m8 * (k / 256);
+    const int64_t work = (m8 / 8) * (k / 128);
     quant_act_kernel<<<grid_for(work, num_sms, kUnroll), kThreads, 0, s>>>(
         static_cast<const __nv_bfloat16*>(x), m, m8, k, q, sf);
     return cudaGetLastError();

@@ -58,6 +58,40 @@ __device__ __forceinline__ uint32_t gather_scale_word(uint32_t scale) {
     return scale | (s1 << 8) | (s2 << 16) | (s3 << 24);
 }
 
+// One lane quantizes a whole 32-block held in 16 registers of packed BF16
+// (same arithmetic as quantize_lane8, without shuffles).  Writes the 32 E4M3
+// bytes into q[0..7] (little-endian words) and returns the scale byte.
+__device__ __forceinline__ uint32_t quantize_block32(const uint4 (&raw)[4], uint32_t (&q)[8]) {
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        w[4 * i] = raw[i].x; w[4 * i + 1] = raw[i].y; w[4 * i + 2] = raw[i].z; w[4 * i + 3] = raw[i].w;
+    }
+    uint32_t a = 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        a = max(a, (w[i] << 16) & 0x7FFFFFFFu);
+        a = max(a, w[i] & 0x7FFF0000u);
+    }
+    if (a >= 0x7F800000u) {  // Inf or NaN somewhere in the block
+#pragma unroll
+        for (int i = 0; i < 8; ++i) q[i] = 0x7F7F7F7Fu;
+        return 0xFFu;
+    }
+    int sb = static_cast<int>(a >> 23) - 8;
+    sb = sb < 0 ? 0 : sb;
+    const float mul = __uint_as_float(static_cast<uint32_t>(254 - sb) << 23);  // 2^(127-sb)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t lo = cvt_e4m3x2(__uint_as_float(w[2 * i] << 16) * mul,
+                                       __uint_as_float(w[2 * i] & 0xFFFF0000u) * mul);
+        const uint32_t hi = cvt_e4m3x2(__uint_as_float(w[2 * i + 1] << 16) * mul,
+                                       __uint_as_float(w[2 * i + 1] & 0xFFFF0000u) * mul);
+        q[i] = lo | (hi << 16);
+    }
+    return static_cast<uint32_t>(sb);
+}
+
 __device__ __forceinline__ void bf16x8_to_float(const uint4& raw, float (&v)[8]) {
     const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
