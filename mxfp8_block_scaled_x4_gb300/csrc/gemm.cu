@@ -37,10 +37,12 @@
 //   persistent   grid <= #SMs x occupancy, tiles strided over CTAs (large M,
 //                grouped).
 //   one tile     one output tile per cluster of `splits` CTAs, each a K range
-//                (small M).  With splits > 1 every rank pushes its FP32
-//                partials into the owning rank's shared memory (DSMEM stores),
-//                one cluster barrier, and each owner sums its token slice in
-//                rank order (deterministic).
+//                (small M).  With splits > 1 each rank owns a slice of the
+//                token columns; every rank pushes the FP32 partials of the
+//                other ranks' slices into their shared memory with st.async,
+//                which counts the bytes on the owner's mbarrier, and each owner
+//                sums its slice in rank order (deterministic) as soon as its
+//                bytes have landed -- no cluster-wide barrier on that path.
 // Programmatic dependent launch: the kernel lets the next grid start at once;
 // it reads nothing a previous grid may write before griddepcontrol.wait,
 // except the weights, their scales, the bias and the grouped offsets, which
@@ -108,6 +110,14 @@ __host__ __device__ constexpr int tokens_per_owner(int tt, int splits) {
     return ((tt + splits - 1) / splits + 3) & ~3;
 }
 
+// Bytes of split-K partials rank `rank` receives from its peers: one whole
+// slot [128][per] FP32 from each of the other splits - 1 ranks if it owns any
+// token column (columns past TT in a slot are never read), else none.
+__host__ __device__ constexpr uint32_t red_bytes(int tt, int splits, int rank) {
+    return rank * tokens_per_owner(tt, splits) < tt
+               ? static_cast<uint32_t>((splits - 1) * 128 * 4 * tokens_per_owner(tt, splits)) : 0u;
+}
+
 struct TileInfo {
     int e, n_tile, tok0, count;
 };
@@ -151,10 +161,6 @@ __device__ __forceinline__ TileInfo decode_tile(int t, const GemmArgs& p, const 
 __device__ __forceinline__ void record_timeout(volatile uint32_t* abort_flag) {
     atomicOr(&g_gemm_error, 1u);
     *abort_flag = 1u;
-}
-
-__device__ __forceinline__ void st_shared_v2(void* p, uint2 v) {
-    asm volatile("st.shared.v2.u32 [%0], {%1,%2};" ::"r"(smem_addr(p)), "r"(v.x), "r"(v.y) : "memory");
 }
 
 // ----------------------------------------------------------------- kernel
@@ -358,10 +364,14 @@ __device__ __forceinline__ void run_reorder(const GemmArgs& p, const Ctx& c, int
     }
 }
 
-// Fused activation quantizer (one tile per CTA): each pass of a warp
-// quantizes 8 (row, block) pairs; lanes 4g..4g+3 hold the 32 values of one
-// block.  Passes of all K blocks are flattened and their loads issued in
-// batches of 8 before any is quantized.
+// Fused activation quantizer (one tile per CTA).  The tile's BF16 rows are
+// cut into patches of 8 token rows x one 128-wide K block; lane l of a warp
+// quantizes 32-block l%4 of patch row l/4 on its own (same arithmetic as
+// quant.cu), writes its 32 E4M3 bytes into the swizzled B tile and its scale
+// byte into the TMEM-copy order.  Patches go round-robin over the epilogue
+// warps with kBatch patches of loads in flight; after each patch the warp
+// fences and arrives on the K block's full barrier, which expects one
+// arrival per patch besides the producer's.
 template <int TT, int PIPES>
 __device__ __forceinline__ void run_fused_quant(const GemmArgs& p, const Ctx& c, int ew, int lane) {
     using G = Geometry<TT>;
@@ -370,31 +380,37 @@ __device__ __forceinline__ void run_fused_quant(const GemmArgs& p, const Ctx& c,
     const int nk = c.kb_end - c.kb_begin;
     const int S = c.stages;
     constexpr int kEpi = epi_warps(TT);
-    constexpr int kPasses = TT * 4 / (kEpi * 8);  // passes per K block per warp
-    const int total = nk * kPasses;
-    for (int p0 = 0; p0 < total; p0 += 8) {
-        uint4 raw[8];
+    constexpr int kPatches = TT / 8;  // per K block
+    constexpr int kBatch = (TT == 16 || PIPES == 1) ? 2 : 4;  // within the register budget
+    const int total = nk * kPatches;
+    const int r8 = lane >> 2;
+    const int b4 = lane & 3;
+    for (int p0 = ew; p0 < total; p0 += kEpi * kBatch) {
+        uint4 raw[kBatch][4];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int ps = p0 + u;
-            const int i = ps / kPasses;
-            const int pr = ((ps - i * kPasses) * kEpi + ew) * 8 + (lane >> 2);
-            const int row = pr >> 2;
-            const int col = (c.kb_begin + i) * 128 + (pr & 3) * 32 + (lane & 3) * 8;
-            raw[u] = make_uint4(0, 0, 0, 0);
-            if (ps < total && row < ti.count)
-                raw[u] = *reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(ti.tok0 + row) * p.k + col);
+        for (int u = 0; u < kBatch; ++u) {
+            const int ps = p0 + u * kEpi;
+            const int i = ps / kPatches;
+            const int row = (ps - i * kPatches) * 8 + r8;
+#pragma unroll
+            for (int v = 0; v < 4; ++v) raw[u][v] = make_uint4(0, 0, 0, 0);
+            if (ps < total && row < ti.count) {
+                const uint4* src = reinterpret_cast<const uint4*>(
+                    p.x + static_cast<size_t>(ti.tok0 + row) * p.k + (c.kb_begin + i) * 128 + b4 * 32);
+#pragma unroll
+                for (int v = 0; v < 4; ++v) raw[u][v] = src[v];
+            }
         }
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int ps = p0 + u;
+        for (int u = 0; u < kBatch; ++u) {
+            const int ps = p0 + u * kEpi;
             if (ps >= total) break;  // warp-uniform
-            const int i = ps / kPasses;
-            const int pass = ps - i * kPasses;
+            const int i = ps / kPatches;
+            const int row = (ps - i * kPatches) * 8 + r8;
             const int q = i % PIPES;
             const int jq = i / PIPES;
             const int s = q * S + jq % S;
-            if (pass == 0 && jq >= S) {
+            if (jq >= S) {
                 bool ok = mbar_wait(&c.empty[s], ((jq / S) & 1) ^ 1, p.wait_ns);
                 ok = __all_sync(0xFFFFFFFFu, ok ? 1 : 0) != 0;
                 if (!ok) {
@@ -402,28 +418,19 @@ __device__ __forceinline__ void run_fused_quant(const GemmArgs& p, const Ctx& c,
                     return;
                 }
             }
+            uint32_t qq[8];
+            const uint32_t sc = quantize_block32(raw[u], qq);
             uint8_t* st = c.smem + s * G::kStageBytes;
-            const int pr = (pass * kEpi + ew) * 8 + (lane >> 2);
-            const int row = pr >> 2;
-            const int byte = (pr & 3) * 32 + (lane & 3) * 8;  // within the 128-byte K block
-            float v[8];
-            bf16x8_to_float(raw[u], v);
-            uint2 q8;
-            uint32_t sc;
-            quantize_lane8(v, q8, sc);
-            const int chunk = byte >> 4;  // 128-byte swizzle: chunk ^= row % 8
-            st_shared_v2(st + G::kOffA + row * 128 + ((chunk ^ (row & 7)) << 4) + (byte & 15), q8);
-            const uint32_t word = gather_scale_word(sc);
-            if ((lane & 15) == 0) {
-                const int rr = row & 127;
-                *reinterpret_cast<uint32_t*>(st + G::kOffAsfT + (row >> 7) * 512 + (rr & 31) * 16 +
-                                             (rr >> 5) * 4) = word;
-            }
-            if (pass == kPasses - 1) {
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&c.full[s]);
-            }
+            // Bytes [32*b4, 32*b4 + 32) of the row's 128-byte K block are
+            // 16-byte chunks 2*b4 and 2*b4 + 1, swizzled with row % 8.
+            uint8_t* brow = st + G::kOffA + row * 128;
+            *reinterpret_cast<uint4*>(brow + (((2 * b4) ^ (row & 7)) << 4)) = make_uint4(qq[0], qq[1], qq[2], qq[3]);
+            *reinterpret_cast<uint4*>(brow + (((2 * b4 + 1) ^ (row & 7)) << 4)) = make_uint4(qq[4], qq[5], qq[6], qq[7]);
+            const int rr = row & 127;
+            st[G::kOffAsfT + (row >> 7) * 512 + (rr & 31) * 16 + (rr >> 5) * 4 + b4] = static_cast<uint8_t>(sc);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&c.full[s]);
         }
     }
 }
@@ -464,7 +471,8 @@ __global__ void __launch_bounds__(32 * num_warps(TT, PIPES),
     c.acc_full = c.sfraw + ST;
     c.acc_empty = c.acc_full + 1;
     c.drain = c.acc_empty + 1;  // [PIPES]
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(c.drain + PIPES);
+    uint64_t* red = c.drain + PIPES;  // split-K: the peers' partials have landed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red + 1);
     c.abort_flag = tmem_slot + 1;
     int* prefix = reinterpret_cast<int*>(tmem_slot + 2);   // [experts + 1]
     int* offs = prefix + (kMaxExperts + 1);                 // [experts + 1]
@@ -481,15 +489,20 @@ __global__ void __launch_bounds__(32 * num_warps(TT, PIPES),
             tma_prefetch_desc(&p.map_asf);
         }
         for (int s = 0; s < ST; ++s) {
-            // full: the producer's arrival (+ TMA bytes) and either the eight
-            // fused-quantizer warps or the scale re-order warp.
-            mbar_init(&c.full[s], fused ? 1 + kEpi : 2);
+            // full: the producer's arrival (+ TMA bytes) and either one
+            // arrival per fused-quantizer patch or the scale re-order warp's.
+            mbar_init(&c.full[s], fused ? 1 + TT / 8 : 2);
             mbar_init(&c.empty[s], 1);
             mbar_init(&c.sfraw[s], 1);
         }
         mbar_init(c.acc_full, PIPES);
         mbar_init(c.acc_empty, kEpi);
         for (int q = 0; q < PIPES; ++q) mbar_init(&c.drain[q], 1);
+        if (reduce) {
+            // Bytes the other ranks push into this rank's slice of the tile.
+            mbar_init(red, 1);
+            mbar_arrive_expect_tx(red, red_bytes(TT, splits, static_cast<int>(cluster_rank())));
+        }
         *c.abort_flag = 0u;
         fence_barrier_init();
     }
@@ -525,11 +538,12 @@ __global__ void __launch_bounds__(32 * num_warps(TT, PIPES),
     __syncthreads();
     tc_fence_after();
     c.tmem_base = *tmem_slot;
-    // Peers must have started before any DSMEM store: arrive now, wait just
-    // before the first remote access.
+    // Split-K lifetime protocol (cluster barrier, two phases, every thread):
+    // phase 1 (arrive here, wait before the first remote store) guarantees
+    // that every peer has initialised its barriers; phase 2 (arrive once this
+    // thread's pushes are issued, wait before exit) keeps every CTA alive
+    // until no peer can push into its shared memory any more.
     if (reduce) cluster_arrive_relaxed();
-    bool cluster_waited = false;
-    float b_red = 0.0f;  // split-K owners: bias of their output feature
 
     // Work assignment: a list of (tile, K range).
     int rank = 0;
@@ -560,32 +574,29 @@ __global__ void __launch_bounds__(32 * num_warps(TT, PIPES),
         __syncwarp();
     } else {
         const int ew = warp - 2;  // warps 2 .. 1+kEpi
-        // Bias of the output feature this thread finishes in the split-K
-        // reduction, fetched before anything else so its latency hides.
-        if (reduce && p.bias) {
-            const TileInfo t0 = decode_tile<TT>(c.tile_first, p, prefix, offs);
-            const int n_red = t0.n_tile * 128 + ((threadIdx.x - 64) & 127);
-            if (n_red < p.n) b_red = __bfloat162float(p.bias[static_cast<size_t>(t0.e) * p.n + n_red]);
-        }
         if (fused) run_fused_quant<TT, PIPES>(p, c, ew, lane);
+        if (reduce) {
+            __syncwarp();
+            cluster_wait();  // phase 1: peers are running (latency hidden behind the MMAs)
+        }
         // ------------------------------------------------------- epilogue
         const int quad = warp & 3;             // TMEM lanes [32*quad, 32*quad + 32)
         const int half = ew >> 2;              // token columns [half*kCols, (half+1)*kCols)
         constexpr int kCols = TT * 4 / kEpi;
         const int col0 = half * kCols;
         const int n_active = nk < PIPES ? nk : PIPES;
+        const int nl = quad * 32 + lane;       // weight row within the tile
+        float acc[kCols];
+        float b = 0.0f;
         int tile_iter = 0;
         for (int t = c.tile_first; t < c.num_tiles; t += c.tile_stride, ++tile_iter) {
             const TileInfo ti = decode_tile<TT>(t, p, prefix, offs);
-            const int nl = quad * 32 + lane;  // weight row within the tile
             const int n = ti.n_tile * 128 + nl;
-            const float b = (!reduce && p.bias && n < p.n)
-                                ? __bfloat162float(p.bias[static_cast<size_t>(ti.e) * p.n + n]) : 0.0f;
+            b = (p.bias && n < p.n) ? __bfloat162float(p.bias[static_cast<size_t>(ti.e) * p.n + n]) : 0.0f;
             bool ok = mbar_wait(c.acc_full, tile_iter & 1, p.wait_ns);
             ok = __all_sync(0xFFFFFFFFu, ok ? 1 : 0) != 0;
             if (!ok) { if (lane == 0) record_timeout(c.abort_flag); break; }
             tc_fence_after();
-            float acc[kCols];
 #pragma unroll
             for (int i = 0; i < kCols; ++i) acc[i] = 0.0f;
             for (int q = 0; q < n_active; ++q) {  // pipe order: deterministic sums
@@ -613,21 +624,15 @@ __global__ void __launch_bounds__(32 * num_warps(TT, PIPES),
             if (lane == 0) mbar_arrive(c.acc_empty);
 
             if (reduce) {
-                // Push: token columns j..j+3 go to rank j / per as one 16-byte
-                // store into its slot [rank][nl][j % per].
-                __syncwarp();
-                cluster_wait();
-                cluster_waited = true;
-                const uint32_t pbase = smem_addr(partial);
+                // Stage the partial tile in the idle pipeline stages (every MMA
+                // has completed) as 4-column chunks: staging[col/4][row][col%4].
+                // Rank o's slice, columns [o*per, o*per + per), is then one
+                // contiguous run of per * 512 bytes.
+                float4* stg = reinterpret_cast<float4*>(smem);
 #pragma unroll
-                for (int j = 0; j < kCols; j += 4) {
-                    const int col = col0 + j;
-                    const int owner = col / per;
-                    const uint32_t a = pbase + static_cast<uint32_t>(((rank * 128 + nl) * per + (col - owner * per)) * 4);
-                    st_cluster_v4(map_to_rank(a, static_cast<uint32_t>(owner)), __float_as_uint(acc[j]),
-                                  __float_as_uint(acc[j + 1]), __float_as_uint(acc[j + 2]),
-                                  __float_as_uint(acc[j + 3]));
-                }
+                for (int j = 0; j < kCols; j += 4)
+                    stg[((col0 + j) >> 2) * 128 + nl] = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+                fence_proxy_async_smem();
             } else if (n < p.n) {
                 const int jmax = min(kCols, ti.count - col0);
                 __nv_bfloat16* yp = p.y + static_cast<size_t>(ti.tok0 + col0) * p.n + n;
@@ -636,41 +641,75 @@ __global__ void __launch_bounds__(32 * num_warps(TT, PIPES),
                     if (j < jmax) yp[static_cast<size_t>(j) * p.n] = __float2bfloat16_rn(acc[j] + b);
             }
         }
-        __syncwarp();
-    }
-
-    // ------------------------------------------------- split-K reduction
-    if (reduce) {
-        __syncwarp();
-        if (!__all_sync(0xFFFFFFFFu, cluster_waited ? 1 : 0)) cluster_wait();
-        cluster_sync();  // every rank's pushes have landed
-        const bool epi = warp >= 2 && warp < 2 + kEpi;
-        if (epi && !*c.abort_flag) {
-            // Owner: tokens [rank*per, rank*per + per), four per thread and step,
-            // summed over source ranks in rank order.
+        if (reduce) {
+            // Push: once every epilogue warp has staged its partials, one
+            // thread hands each peer its slice (one bulk copy per peer into
+            // the peer's slot [rank], counted on the peer's `red` barrier).
+            // Nothing is pushed if any role of this CTA gave up.
+            named_barrier_sync(1, kEpi * 32);
+            const bool push = *c.abort_flag == 0u;
+            const uint32_t slot_bytes = static_cast<uint32_t>(per * 512);
+            if (push && ew == 0 && lane < splits && lane != rank && red_bytes(TT, splits, lane) > 0) {
+                // Lane o of the first epilogue warp issues the copy to peer o.
+                bulk_copy_to_peer(map_to_rank(smem_addr(partial) + rank * slot_bytes, static_cast<uint32_t>(lane)),
+                                  smem + lane * slot_bytes, slot_bytes,
+                                  map_to_rank(smem_addr(red), static_cast<uint32_t>(lane)));
+            }
+            // Owner: columns [rank*per, rank*per + per) of the tile, spread
+            // over all epilogue threads (row et % 128, every (kEpi/4)-th
+            // 4-column chunk), summed over the ranks in rank order.
+            const bool owns = red_bytes(TT, splits, rank) > 0;
+            const int et = ew * 32 + lane;
+            const int rn = et & 127;
             const TileInfo ti = decode_tile<TT>(c.tile_first, p, prefix, offs);
-            const int et = threadIdx.x - 64;
-            const int nl = et & 127;
-            const int n = ti.n_tile * 128 + nl;
-            const float* part = reinterpret_cast<const float*>(partial);
-            const int j0 = rank * per;
-            for (int qq = et >> 7; qq < per / 4; qq += (kEpi * 32) / 128) {
-                float4 sum = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                for (int r = 0; r < splits; ++r) {
-                    const float4 v = *reinterpret_cast<const float4*>(part + (r * 128 + nl) * per + qq * 4);
-                    sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
+            const int n = ti.n_tile * 128 + rn;
+            const float bn = (owns && p.bias && n < p.n)
+                                 ? __bfloat162float(p.bias[static_cast<size_t>(ti.e) * p.n + n]) : 0.0f;
+            bool landed = !owns;
+            if (owns) {
+                landed = push && mbar_wait(red, 0, p.wait_ns);
+                landed = __all_sync(0xFFFFFFFFu, landed ? 1 : 0) != 0;
+                if (!landed) {
+                    if (push && lane == 0) record_timeout(c.abort_flag);
+                    // Error path: let copies already in flight land (their
+                    // sources stay alive until phase 2 completes).
+                    (void)mbar_wait(red, 0, kDrainNs);
                 }
-                const float sv[4] = {sum.x, sum.y, sum.z, sum.w};
-                if (n < p.n) {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int j = j0 + qq * 4 + i;
-                        if (j < ti.count && j < TT)
-                            p.y[static_cast<size_t>(ti.tok0 + j) * p.n + n] = __float2bfloat16_rn(sv[i] + b_red);
+            }
+            // Phase 2: every copy into this CTA has landed (or the drain ran
+            // out), so the copies that read the peers' staging areas are done.
+            __syncwarp();
+            cluster_arrive_relaxed();
+            if (owns && landed && push && n < p.n) {
+                const float4* own = reinterpret_cast<const float4*>(smem) + rank * (per / 4) * 128;
+                const float4* part = reinterpret_cast<const float4*>(partial);
+                const int o0 = rank * per;
+                const int cmax = min(per, ti.count - o0);
+                for (int q = et >> 7; q * 4 < cmax; q += kEpi / 4) {
+                    float4 sum = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                    for (int r = 0; r < splits; ++r) {
+                        const float4 v = (r == rank ? own : part + r * (per / 4) * 128)[q * 128 + rn];
+                        sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
                     }
+                    const float sv[4] = {sum.x, sum.y, sum.z, sum.w};
+                    __nv_bfloat16* yq = p.y + static_cast<size_t>(ti.tok0 + o0 + q * 4) * p.n + n;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        if (q * 4 + i < cmax) yq[static_cast<size_t>(i) * p.n] = __float2bfloat16_rn(sv[i] + bn);
                 }
             }
         }
+        __syncwarp();
+    }
+
+    if (reduce) {
+        __syncwarp();
+        const bool epi = warp >= 2 && warp < 2 + kEpi;
+        if (!epi) {
+            cluster_wait();            // phase 1
+            cluster_arrive_relaxed();  // phase 2: this warp receives nothing
+        }
+        cluster_wait();  // phase 2: every owner has received all of its slice
     }
 
     // -------------------------------------------------------------- teardown
@@ -1054,6 +1093,13 @@ LaunchPlan plan_for(int splits, bool persistent, int kq) {
         const int nq = (nk + PIPES - 1) / PIPES;
         if (stages > nq) stages = nq;
     }
+    if (splits > 1) {
+        // The split-K partials are staged in the pipeline stages: keep room
+        // for one [128][per] FP32 slot per rank.
+        const int staging = splits * 128 * tokens_per_owner(TT, splits) * 4;
+        const int need = (staging + PIPES * G::kStageBytes - 1) / (PIPES * G::kStageBytes);
+        if (stages < need) stages = need;
+    }
     lp.stages = stages;
     lp.tmem_cols = pow2_cols(PIPES * TT + PIPES * stages * G::kSfSlotCols);
     lp.smem = 1024 + static_cast<size_t>(PIPES * stages) * G::kStageBytes + lp.partial + ctrl;
@@ -1088,6 +1134,11 @@ cudaError_t launch_tt(const GemmProblem& pr, const GemmSchedule& sch, int num_sm
     const int splits = sch.persistent ? 1 : sch.split_k;
     const LaunchPlan lp = plan_for<TT, PIPES>(splits, sch.persistent, kq);
     if (lp.stages < 1) return cudaErrorInvalidConfiguration;
+    // Split-K partials are staged in the pipeline stages, one slot per rank.
+    if (splits > 1 &&
+        static_cast<size_t>(splits) * 128 * tokens_per_owner(TT, splits) * 4 >
+            static_cast<size_t>(PIPES * lp.stages) * G::kStageBytes)
+        return cudaErrorInvalidConfiguration;
 
     a.wsf = pr.wsf;
     a.bias = static_cast<const __nv_bfloat16*>(pr.bias);

@@ -264,10 +264,6 @@ __device__ __forceinline__ uint32_t cluster_id_x() {
     asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
     return r;
 }
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
-                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
 // Split cluster barrier: every thread arrives once (relaxed: no ordering
 // implied) and later waits once.
 __device__ __forceinline__ void cluster_arrive_relaxed() {
@@ -282,15 +278,20 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
     return r;
 }
-__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
-    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+// Bulk copy of `bytes` from this CTA's shared memory to a cluster peer's
+// (`dst` and `bar` are peer addresses from mapa; 16-byte aligned addresses,
+// size % 16 == 0).  The copy engine counts the bytes on the peer's mbarrier.
+// The source must stay untouched until the peer has seen them land.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "r"(smem_addr(src)), "r"(bytes), "r"(bar)
+        : "memory");
 }
-// 16-byte store to (possibly remote) shared memory; addr 16-byte aligned.
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                              uint32_t d) {
-    asm volatile("st.shared::cluster.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-                 "r"(d)
-                 : "memory");
+
+// Barrier among the `threads` threads (whole warps) that use named barrier `id`.
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 // ----------------------------------------------- programmatic dependent launch

@@ -18,6 +18,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <string.h>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -53,8 +54,11 @@ __global__ void __launch_bounds__(kThreads) quant_act_kernel(const __nv_bfloat16
                                                              uint8_t* __restrict__ q,
                                                              uint8_t* __restrict__ sf) {
     // Dependent kernels (the GEMM) may start their prologue now; they wait
-    // for this grid's completion before reading what it writes.
+    // for this grid's completion before reading what it writes.  This grid
+    // itself may start before the kernel that produced x has finished: every
+    // CTA waits for it before touching x, q or sf.
     pdl_launch_dependents();
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int64_t quads = k >> 7;  // 128-column patches per row group
     const int64_t total = (m8 >> 3) * quads;
@@ -161,9 +165,17 @@ cudaError_t launch_quant_act(const void* x, int64_t m, int64_t k, uint8_t* q, ui
                              int num_sms, cudaStream_t s) {
     const int64_t m8 = (m + 7) / 8 * 8;
     const int64_t work = (m8 / 8) * (k / 128);
-    quant_act_kernel<<<grid_for(work, num_sms, kUnroll), kThreads, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(x), m, m8, k, q, sf);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(grid_for(work, num_sms, kUnroll), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.stream = s;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, quant_act_kernel, static_cast<const __nv_bfloat16*>(x), m, m8, k, q, sf);
 }
 
 cudaError_t launch_prepare_weight(const void* src, bool src_is_bf16, int64_t experts, int64_t n,
