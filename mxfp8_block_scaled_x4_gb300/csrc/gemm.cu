@@ -277,6 +277,7 @@ __device__ __forceinline__ void run_mma(const GemmArgs& p, const Ctx& c, int q) 
     const uint64_t asf_desc0 = desc_sf_32x16(smem_addr(c.smem + G::kOffAsfT));
     constexpr uint64_t kStageStep = static_cast<uint64_t>(G::kStageBytes >> 4);
     const int nk = c.kb_end - c.kb_begin;
+    const int nq = pipe_jobs<PIPES>(q, nk);  // jobs of this pipe in one tile
     const int S = c.stages;
     const uint32_t acc = c.tmem_base + q * TT;
     int jq = 0;
@@ -312,7 +313,9 @@ __device__ __forceinline__ void run_mma(const GemmArgs& p, const Ctx& c, int q) 
             for (int kk = 0; kk < 4; ++kk)
                 mma_mxf8(acc, a_desc0 + sd + 2 * kk, b_desc0 + sd + 2 * kk, idesc[kk], sfa, sfb,
                          (i > q || kk > 0) ? 1u : 0u);
-            mma_commit(&c.empty[s]);
+            // Release the stage to its producer -- unless no later job of this
+            // pipe uses it (one-tile schedules): a commit costs issue time.
+            if (p.persistent || jq + S < nq) mma_commit(&c.empty[s]);
         }
         if (stop) break;
         mma_commit(c.acc_full);  // also for a pipe with no K block in this tile
@@ -401,36 +404,68 @@ __device__ __forceinline__ void run_fused_quant(const GemmArgs& p, const Ctx& c,
                 for (int v = 0; v < 4; ++v) raw[u][v] = src[v];
             }
         }
+        // Quantize the whole batch first (independent register math that
+        // interleaves), then publish it.
+        uint32_t qq[kBatch][8];
+        uint32_t sc[kBatch];
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-            const int ps = p0 + u * kEpi;
-            if (ps >= total) break;  // warp-uniform
+        for (int u = 0; u < kBatch; ++u) sc[u] = quantize_block32(raw[u], qq[u]);
+        auto store_patch = [&](int u, int ps) {
             const int i = ps / kPatches;
             const int row = (ps - i * kPatches) * 8 + r8;
-            const int q = i % PIPES;
             const int jq = i / PIPES;
-            const int s = q * S + jq % S;
-            if (jq >= S) {
-                bool ok = mbar_wait(&c.empty[s], ((jq / S) & 1) ^ 1, p.wait_ns);
-                ok = __all_sync(0xFFFFFFFFu, ok ? 1 : 0) != 0;
-                if (!ok) {
-                    if (lane == 0) record_timeout(c.abort_flag);
-                    return;
-                }
-            }
-            uint32_t qq[8];
-            const uint32_t sc = quantize_block32(raw[u], qq);
-            uint8_t* st = c.smem + s * G::kStageBytes;
+            uint8_t* st = c.smem + ((i % PIPES) * S + jq % S) * G::kStageBytes;
             // Bytes [32*b4, 32*b4 + 32) of the row's 128-byte K block are
             // 16-byte chunks 2*b4 and 2*b4 + 1, swizzled with row % 8.
             uint8_t* brow = st + G::kOffA + row * 128;
-            *reinterpret_cast<uint4*>(brow + (((2 * b4) ^ (row & 7)) << 4)) = make_uint4(qq[0], qq[1], qq[2], qq[3]);
-            *reinterpret_cast<uint4*>(brow + (((2 * b4 + 1) ^ (row & 7)) << 4)) = make_uint4(qq[4], qq[5], qq[6], qq[7]);
+            *reinterpret_cast<uint4*>(brow + (((2 * b4) ^ (row & 7)) << 4)) =
+                make_uint4(qq[u][0], qq[u][1], qq[u][2], qq[u][3]);
+            *reinterpret_cast<uint4*>(brow + (((2 * b4 + 1) ^ (row & 7)) << 4)) =
+                make_uint4(qq[u][4], qq[u][5], qq[u][6], qq[u][7]);
             const int rr = row & 127;
-            st[G::kOffAsfT + (row >> 7) * 512 + (rr & 31) * 16 + (rr >> 5) * 4 + b4] = static_cast<uint8_t>(sc);
+            st[G::kOffAsfT + (row >> 7) * 512 + (rr & 31) * 16 + (rr >> 5) * 4 + b4] = static_cast<uint8_t>(sc[u]);
+        };
+        auto full_of = [&](int ps) {
+            const int i = ps / kPatches;
+            return &c.full[(i % PIPES) * S + (i / PIPES) % S];
+        };
+        // A patch whose stage is in use again must wait for the MMA to free
+        // it, and that MMA may need an earlier patch of this very batch: such
+        // batches publish patch by patch.  Otherwise one proxy fence covers
+        // the batch.
+        const bool reuse = (p0 + (kBatch - 1) * kEpi) / kPatches / PIPES >= S;
+        if (!reuse) {
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u)
+                if (p0 + u * kEpi < total) store_patch(u, p0 + u * kEpi);
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&c.full[s]);
+            if (lane == 0) {
+#pragma unroll
+                for (int u = 0; u < kBatch; ++u)
+                    if (p0 + u * kEpi < total) mbar_arrive(full_of(p0 + u * kEpi));
+            }
+        } else {
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+                const int ps = p0 + u * kEpi;
+                if (ps >= total) break;  // warp-uniform
+                const int i = ps / kPatches;
+                const int jq = i / PIPES;
+                if (jq >= S) {
+                    const int s = (i % PIPES) * S + jq % S;
+                    bool ok = mbar_wait(&c.empty[s], ((jq / S) & 1) ^ 1, p.wait_ns);
+                    ok = __all_sync(0xFFFFFFFFu, ok ? 1 : 0) != 0;
+                    if (!ok) {
+                        if (lane == 0) record_timeout(c.abort_flag);
+                        return;
+                    }
+                }
+                store_patch(u, ps);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(full_of(ps));
+            }
         }
     }
 }

@@ -67,12 +67,16 @@ __device__ __forceinline__ uint32_t quantize_block32(const uint4 (&raw)[4], uint
     for (int i = 0; i < 4; ++i) {
         w[4 * i] = raw[i].x; w[4 * i + 1] = raw[i].y; w[4 * i + 2] = raw[i].z; w[4 * i + 3] = raw[i].w;
     }
-    uint32_t a = 0;
+    // amax magnitude as a BF16 bit pattern: per-halfword unsigned max of the
+    // sign-cleared pairs, as a balanced tree.
+    uint32_t m[8];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        a = max(a, (w[i] << 16) & 0x7FFFFFFFu);
-        a = max(a, w[i] & 0x7FFF0000u);
-    }
+    for (int i = 0; i < 8; ++i) m[i] = __vmaxu2(w[2 * i] & 0x7FFF7FFFu, w[2 * i + 1] & 0x7FFF7FFFu);
+#pragma unroll
+    for (int d = 1; d < 8; d <<= 1)
+#pragma unroll
+        for (int i = 0; i < 8; i += 2 * d) m[i] = __vmaxu2(m[i], m[i + d]);
+    const uint32_t a = max(m[0] & 0xFFFFu, m[0] >> 16) << 16;  // FP32 bits of |amax|
     if (a >= 0x7F800000u) {  // Inf or NaN somewhere in the block
 #pragma unroll
         for (int i = 0; i < 8; ++i) q[i] = 0x7F7F7F7Fu;
