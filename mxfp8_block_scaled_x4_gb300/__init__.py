@@ -95,6 +95,14 @@ def library():
         "mxfp8_set_wait_limit_ns": (None, [ctypes.c_uint64]),
         "mxfp8_set_pipes": (None, [ctypes.c_int]),
         "mxfp8_static_scratch_last_cuda_error": (ctypes.c_int, []),
+        "mxfp8_moe_route_workspace_bytes": (sz, [i64, i64, i64]),
+        "mxfp8_moe_route": (ctypes.c_int, [vp, i64, i64, i64, ctypes.c_int, vp, vp, vp, vp, vp, vp, sz, vp]),
+        "mxfp8_prepare_gate_up_weight": (ctypes.c_int, [vp, ctypes.c_int, W, vp]),
+        "mxfp8_moe_gate_up_workspace_bytes": (sz, [i64, i64]),
+        "mxfp8_moe_gate_up_swiglu": (ctypes.c_int, [vp, vp, i64, vp, W, vp, vp, sz, vp]),
+        "mxfp8_moe_finalize": (ctypes.c_int, [vp, vp, vp, i64, i64, i64, vp, vp]),
+        "mxfp8_moe_workspace_bytes": (sz, [i64, i64, i64, i64, i64]),
+        "mxfp8_moe_expert_mlp": (ctypes.c_int, [vp, vp, i64, i64, ctypes.c_int, W, W, vp, vp, sz, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -253,6 +261,112 @@ def grouped_linear(x_sorted: torch.Tensor, offsets: torch.Tensor, pw: PreparedWe
                                           _ptr(workspace), workspace.numel(), _stream(x_sorted)),
            "mxfp8_grouped_linear")
     return y
+
+
+# -------------------------------------------------------------------- MoE
+ROUTE_RENORMALIZE = 0
+ROUTE_RENORMALIZE_NAIVE = 1
+
+
+class Routing:
+    """Device outputs of moe_route: topk ids/weights [t, k], expert offsets
+    [e+1], sorted_token [t*k] (token of each expert-sorted row) and row_of
+    [t*k] (sorted row of pair (t, s) at t*k + s)."""
+
+    def __init__(self, ids, weights, offsets, sorted_token, row_of):
+        self.ids, self.weights, self.offsets = ids, weights, offsets
+        self.sorted_token, self.row_of = sorted_token, row_of
+
+
+def moe_route(logits: torch.Tensor, topk: int, method: int = ROUTE_RENORMALIZE) -> Routing:
+    """Top-k routing of float32 logits [tokens, experts] and the stable
+    expert-sorted order of the (token, slot) pairs."""
+    _need(logits.is_cuda and logits.dtype == torch.float32 and logits.dim() == 2,
+          "logits must be a float32 CUDA tensor [tokens, experts]")
+    lg = logits.contiguous()
+    t, e = lg.shape
+    dev = logits.device
+    ids = torch.empty((t, topk), dtype=torch.int32, device=dev)
+    w = torch.empty((t, topk), dtype=torch.float32, device=dev)
+    off = torch.empty((e + 1,), dtype=torch.int32, device=dev)
+    stok = torch.empty((max(t * topk, 1),), dtype=torch.int32, device=dev)
+    row_of = torch.empty((max(t * topk, 1),), dtype=torch.int32, device=dev)
+    nws = library().mxfp8_moe_route_workspace_bytes(t, e, topk)
+    ws = torch.empty((max(nws, 16),), dtype=torch.uint8, device=dev)
+    _check(library().mxfp8_moe_route(_ptr(lg), t, e, topk, method, _ptr(ids), _ptr(w), _ptr(off),
+                                     _ptr(stok), _ptr(row_of), _ptr(ws), ws.numel(), _stream(logits)),
+           "mxfp8_moe_route")
+    return Routing(ids, w, off, stok[:t * topk], row_of[:t * topk])
+
+
+def prepare_gate_up_weight(w13: torch.Tensor, out: PreparedWeight = None) -> PreparedWeight:
+    """GEMM1 weights [experts, 2*I, k] (rows [gate; up]) -> prepared with the
+    gated-row reorder (tile j = gate rows 64j.. then up rows I+64j..)."""
+    _need(w13.is_cuda and w13.dtype in (torch.float32, torch.bfloat16) and w13.dim() == 3,
+          "w13 must be a float32/bfloat16 CUDA tensor [experts, 2I, k]")
+    w3 = w13.contiguous()
+    e, n, k = w3.shape
+    if out is not None:
+        _need((out.num_experts, out.n, out.k) == (e, n, k), "refit needs a weight of the same shape")
+        pw = out
+    else:
+        q = torch.empty((e, n, k), dtype=torch.uint8, device=w13.device)
+        sf = torch.empty((e, n * (k // 32)), dtype=torch.uint8, device=w13.device)
+        pw = PreparedWeight(q, sf, n)
+    dt = IN_BF16 if w3.dtype == torch.bfloat16 else IN_F32
+    _check(library().mxfp8_prepare_gate_up_weight(_ptr(w3), dt, ctypes.byref(pw.c), _stream(w13)),
+           "mxfp8_prepare_gate_up_weight")
+    return pw
+
+
+def moe_gate_up_swiglu(x: torch.Tensor, routing: Routing, w13: PreparedWeight) -> torch.Tensor:
+    """h [t*k, I] bf16 = silu(gate) * up of GEMM1 on the expert-sorted,
+    MXFP8-quantized token rows."""
+    _need(x.is_cuda and x.dtype == torch.bfloat16, "x must be bf16 CUDA")
+    x2 = x.contiguous()
+    rows = routing.sorted_token.numel()
+    h = torch.empty((rows, w13.n // 2), dtype=torch.bfloat16, device=x.device)
+    nws = library().mxfp8_moe_gate_up_workspace_bytes(rows, w13.k)
+    ws = torch.empty((max(nws, 16),), dtype=torch.uint8, device=x.device)
+    _check(library().mxfp8_moe_gate_up_swiglu(_ptr(x2), _ptr(routing.sorted_token), rows,
+                                              _ptr(routing.offsets), ctypes.byref(w13.c), _ptr(h),
+                                              _ptr(ws), ws.numel(), _stream(x)),
+           "mxfp8_moe_gate_up_swiglu")
+    return h
+
+
+def moe_finalize(y2: torch.Tensor, routing: Routing) -> torch.Tensor:
+    """out [t, hidden] bf16 = per token, the routing-weighted sum of its k
+    expert outputs y2 [t*k, hidden] (expert-sorted rows)."""
+    t, k = routing.ids.shape
+    hidden = y2.shape[1]
+    out = torch.empty((t, hidden), dtype=torch.bfloat16, device=y2.device)
+    _check(library().mxfp8_moe_finalize(_ptr(y2.contiguous()), _ptr(routing.row_of), _ptr(routing.weights),
+                                        t, k, hidden, _ptr(out), _stream(y2)),
+           "mxfp8_moe_finalize")
+    return out
+
+
+def moe_expert_mlp(x: torch.Tensor, logits: torch.Tensor, topk: int, w13: PreparedWeight,
+                   w2: PreparedWeight, method: int = ROUTE_RENORMALIZE, workspace=None) -> torch.Tensor:
+    """The whole expert MLP: route -> gate_up + SwiGLU -> down -> finalize."""
+    _need(x.is_cuda and x.dtype == torch.bfloat16, "x must be bf16 CUDA")
+    _need(logits.is_cuda and logits.dtype == torch.float32, "logits must be float32 CUDA")
+    t, hdim = x.shape
+    e = w13.num_experts
+    nws = library().mxfp8_moe_workspace_bytes(t, e, topk, hdim, w13.n // 2)
+    if workspace is None:
+        workspace = torch.empty((max(nws, 16),), dtype=torch.uint8, device=x.device)
+    out = torch.empty((t, hdim), dtype=torch.bfloat16, device=x.device)
+    _check(library().mxfp8_moe_expert_mlp(_ptr(x.contiguous()), _ptr(logits.contiguous()), t, topk, method,
+                                          ctypes.byref(w13.c), ctypes.byref(w2.c), _ptr(out),
+                                          _ptr(workspace), workspace.numel(), _stream(x)),
+           "mxfp8_moe_expert_mlp")
+    return out
+
+
+def moe_workspace_bytes(tokens, experts, topk, hidden, inter) -> int:
+    return library().mxfp8_moe_workspace_bytes(tokens, experts, topk, hidden, inter)
 
 
 # ------------------------------------------------------------------ hooks

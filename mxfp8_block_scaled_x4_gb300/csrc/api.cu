@@ -11,6 +11,7 @@
 #include <stdlib.h>
 
 #include "../../include/mxfp8.h"
+#include "../../include/mxfp8_moe.h"
 #include "internal.h"
 
 namespace {
@@ -153,6 +154,7 @@ static mxk::GemmProblem make_problem(const void* qa, const void* sfa, int64_t m,
     p.y = y;
     p.offsets = offsets;
     p.x = x;
+    p.gated = false;
     return p;
 }
 
@@ -222,6 +224,174 @@ mxfp8_status mxfp8_grouped_linear(const void* x_sorted, int64_t rows, const int3
     if (!expert_offsets) return MXFP8_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(expert_offsets) & 3u)) return MXFP8_ERR_MISALIGNED;
     return linear_common(x_sorted, rows, expert_offsets, w, bias, y, workspace, workspace_bytes, stream);
+}
+
+// ------------------------------------------------------------------- MoE
+size_t mxfp8_moe_route_workspace_bytes(int64_t tokens, int64_t experts, int64_t topk) {
+    if (tokens < 0 || experts < 1 || topk < 1) return 0;
+    return static_cast<size_t>(((tokens + 31) / 32 * experts + tokens * topk) * 4);
+}
+
+static mxfp8_status check_route_shape(int64_t tokens, int64_t experts, int64_t topk) {
+    if (tokens < 0 || topk < 1 || topk > 16 || experts < topk || experts > 1024) return MXFP8_ERR_INVALID_ARG;
+    if (tokens * topk >= (int64_t(1) << 31)) return MXFP8_ERR_INVALID_ARG;
+    return MXFP8_OK;
+}
+
+mxfp8_status mxfp8_moe_route(const float* logits, int64_t tokens, int64_t experts, int64_t topk,
+                             mxfp8_route_method method, int32_t* topk_ids, float* topk_weights,
+                             int32_t* expert_offsets, int32_t* sorted_token, int32_t* row_of, void* ws,
+                             size_t ws_bytes, void* stream) {
+    mxfp8_status st = check_route_shape(tokens, experts, topk);
+    if (st != MXFP8_OK) return st;
+    if (method != MXFP8_ROUTE_RENORMALIZE && method != MXFP8_ROUTE_RENORMALIZE_NAIVE) return MXFP8_ERR_INVALID_ARG;
+    if (tokens == 0) return MXFP8_OK;
+    if (!logits || !topk_ids || !topk_weights || !expert_offsets || !sorted_token || !row_of || !ws)
+        return MXFP8_ERR_INVALID_ARG;
+    const void* ptrs[] = {logits, topk_ids, topk_weights, expert_offsets, sorted_token, row_of, ws};
+    for (const void* q : ptrs)
+        if (reinterpret_cast<uintptr_t>(q) & 3u) return MXFP8_ERR_MISALIGNED;
+    if (ws_bytes < mxfp8_moe_route_workspace_bytes(tokens, experts, topk)) return MXFP8_ERR_WORKSPACE_TOO_SMALL;
+    int sms = 0;
+    if ((st = device_sms(&sms)) != MXFP8_OK) return st;
+    cudaError_t e = mxk::launch_moe_route(logits, tokens, experts, topk, static_cast<int>(method), topk_ids,
+                                          topk_weights, expert_offsets, sorted_token, row_of,
+                                          static_cast<int32_t*>(ws), static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MXFP8_OK : cuda_fail(e);
+}
+
+static mxfp8_status check_gated(const mxfp8_weight* w) {
+    mxfp8_status st = check_weight(w);
+    if (st != MXFP8_OK) return st;
+    if (w->n % 128 != 0) return MXFP8_ERR_INVALID_ARG;  // n = 2 I with I % 64 == 0
+    return MXFP8_OK;
+}
+
+mxfp8_status mxfp8_prepare_gate_up_weight(const void* src, mxfp8_in_dtype dtype, const mxfp8_weight* w,
+                                          void* stream) {
+    mxfp8_status st = check_gated(w);
+    if (st != MXFP8_OK) return st;
+    if (!src || (dtype != MXFP8_IN_F32 && dtype != MXFP8_IN_BF16)) return MXFP8_ERR_INVALID_ARG;
+    if (!aligned16(src)) return MXFP8_ERR_MISALIGNED;
+    int sms = 0;
+    if ((st = device_sms(&sms)) != MXFP8_OK) return st;
+    cudaError_t e = mxk::launch_prepare_weight(src, dtype == MXFP8_IN_BF16, w->num_experts, w->n, w->n_pad, w->k,
+                                               static_cast<uint8_t*>(w->q), static_cast<uint8_t*>(w->sf), sms,
+                                               static_cast<cudaStream_t>(stream), w->n / 2);
+    return e == cudaSuccess ? MXFP8_OK : cuda_fail(e);
+}
+
+size_t mxfp8_moe_gate_up_workspace_bytes(int64_t rows, int64_t k) { return mxfp8_linear_workspace_bytes(rows, k); }
+
+mxfp8_status mxfp8_moe_gate_up_swiglu(const void* x, const int32_t* sorted_token, int64_t rows,
+                                      const int32_t* expert_offsets, const mxfp8_weight* w13, void* h, void* ws,
+                                      size_t ws_bytes, void* stream) {
+    mxfp8_status st = check_gated(w13);
+    if (st != MXFP8_OK) return st;
+    if (rows < 0 || rows > kMaxRows) return MXFP8_ERR_INVALID_ARG;
+    if (rows == 0) return MXFP8_OK;
+    if (!x || !sorted_token || !expert_offsets || !h || !ws) return MXFP8_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(ws) || (reinterpret_cast<uintptr_t>(h) & 1u) ||
+        (reinterpret_cast<uintptr_t>(sorted_token) & 3u) || (reinterpret_cast<uintptr_t>(expert_offsets) & 3u))
+        return MXFP8_ERR_MISALIGNED;
+    if (ws_bytes < mxfp8_moe_gate_up_workspace_bytes(rows, w13->k)) return MXFP8_ERR_WORKSPACE_TOO_SMALL;
+    int sms = 0;
+    if ((st = device_sms(&sms)) != MXFP8_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* qa = static_cast<uint8_t*>(ws);
+    uint8_t* sfa = qa + ceil_to(rows * w13->k, 256);
+    cudaError_t e = mxk::launch_quant_act(x, rows, w13->k, qa, sfa, sms, s, sorted_token);
+    if (e != cudaSuccess) return cuda_fail(e);
+    mxk::GemmProblem p = make_problem(qa, sfa, rows, w13, nullptr, h, expert_offsets, nullptr);
+    p.gated = true;
+    const mxk::GemmSchedule sch = mxk::choose_schedule(p, sms, g_force_tt, 0, -1);
+    bool enc_fail = false;
+    e = mxk::launch_gemm(p, sch, sms, s, &enc_fail);
+    return launch_status(e, enc_fail);
+}
+
+mxfp8_status mxfp8_moe_finalize(const void* y2, const int32_t* row_of, const float* topk_weights,
+                                int64_t tokens, int64_t topk, int64_t hidden, void* out, void* stream) {
+    if (tokens < 0 || topk < 1 || topk > 16 || hidden < 8 || hidden % 8 != 0 || hidden > kMaxK)
+        return MXFP8_ERR_INVALID_ARG;
+    if (tokens * topk >= (int64_t(1) << 31)) return MXFP8_ERR_INVALID_ARG;
+    if (tokens == 0) return MXFP8_OK;
+    if (!y2 || !row_of || !topk_weights || !out) return MXFP8_ERR_INVALID_ARG;
+    if (!aligned16(y2) || !aligned16(out) || (reinterpret_cast<uintptr_t>(row_of) & 3u) ||
+        (reinterpret_cast<uintptr_t>(topk_weights) & 3u))
+        return MXFP8_ERR_MISALIGNED;
+    int sms = 0;
+    mxfp8_status st = device_sms(&sms);
+    if (st != MXFP8_OK) return st;
+    cudaError_t e = mxk::launch_moe_finalize(y2, row_of, topk_weights, tokens, topk, hidden, out, sms,
+                                             static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MXFP8_OK : cuda_fail(e);
+}
+
+namespace {
+// Sub-buffers of the expert-MLP workspace, each 256-byte aligned.
+struct MoeWs {
+    size_t ids, weights, offsets, sorted_token, row_of, route, g1, h, g2, y2, total;
+};
+MoeWs moe_layout(int64_t tokens, int64_t experts, int64_t topk, int64_t hidden, int64_t inter) {
+    const int64_t r = tokens * topk;
+    MoeWs l;
+    size_t at = 0;
+    auto take = [&](size_t bytes) { const size_t p = at; at += static_cast<size_t>(ceil_to(bytes, 256)); return p; };
+    l.ids = take(r * 4);
+    l.weights = take(r * 4);
+    l.offsets = take((experts + 1) * 4);
+    l.sorted_token = take(r * 4);
+    l.row_of = take(r * 4);
+    l.route = take(mxfp8_moe_route_workspace_bytes(tokens, experts, topk));
+    l.g1 = take(mxfp8_linear_workspace_bytes(r, hidden));
+    l.h = take(r * inter * 2);
+    l.g2 = take(mxfp8_linear_workspace_bytes(r, inter));
+    l.y2 = take(r * hidden * 2);
+    l.total = at;
+    return l;
+}
+}  // namespace
+
+size_t mxfp8_moe_workspace_bytes(int64_t tokens, int64_t experts, int64_t topk, int64_t hidden, int64_t inter) {
+    if (check_route_shape(tokens, experts, topk) != MXFP8_OK || hidden <= 0 || inter <= 0 || hidden % 32 ||
+        inter % 32)
+        return 0;
+    return moe_layout(tokens, experts, topk, hidden, inter).total;
+}
+
+mxfp8_status mxfp8_moe_expert_mlp(const void* x, const float* logits, int64_t tokens, int64_t topk,
+                                  mxfp8_route_method method, const mxfp8_weight* w13, const mxfp8_weight* w2,
+                                  void* out, void* ws, size_t ws_bytes, void* stream) {
+    mxfp8_status st = check_gated(w13);
+    if (st != MXFP8_OK) return st;
+    if ((st = check_weight(w2)) != MXFP8_OK) return st;
+    const int64_t experts = w13->num_experts, hidden = w13->k, inter = w13->n / 2;
+    if (w2->num_experts != experts || w2->n != hidden || w2->k != inter) return MXFP8_ERR_INVALID_ARG;
+    if ((st = check_route_shape(tokens, experts, topk)) != MXFP8_OK) return st;
+    if (tokens == 0) return MXFP8_OK;
+    if (!x || !logits || !out || !ws) return MXFP8_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(out) || !aligned16(ws) || (reinterpret_cast<uintptr_t>(logits) & 3u))
+        return MXFP8_ERR_MISALIGNED;
+    const MoeWs l = moe_layout(tokens, experts, topk, hidden, inter);
+    if (ws_bytes < l.total) return MXFP8_ERR_WORKSPACE_TOO_SMALL;
+    uint8_t* b = static_cast<uint8_t*>(ws);
+    int32_t* ids = reinterpret_cast<int32_t*>(b + l.ids);
+    float* wts = reinterpret_cast<float*>(b + l.weights);
+    int32_t* off = reinterpret_cast<int32_t*>(b + l.offsets);
+    int32_t* stok = reinterpret_cast<int32_t*>(b + l.sorted_token);
+    int32_t* row_of = reinterpret_cast<int32_t*>(b + l.row_of);
+    const int64_t r = tokens * topk;
+    st = mxfp8_moe_route(logits, tokens, experts, topk, method, ids, wts, off, stok, row_of, b + l.route,
+                         mxfp8_moe_route_workspace_bytes(tokens, experts, topk), stream);
+    if (st != MXFP8_OK) return st;
+    st = mxfp8_moe_gate_up_swiglu(x, stok, r, off, w13, b + l.h, b + l.g1, mxfp8_linear_workspace_bytes(r, hidden),
+                                  stream);
+    if (st != MXFP8_OK) return st;
+    st = mxfp8_grouped_linear(b + l.h, r, off, w2, nullptr, b + l.y2, b + l.g2, mxfp8_linear_workspace_bytes(r, inter),
+                              stream);
+    if (st != MXFP8_OK) return st;
+    return mxfp8_moe_finalize(b + l.y2, row_of, wts, tokens, topk, hidden, out, stream);
 }
 
 const char* mxfp8_status_string(mxfp8_status s) {

@@ -87,6 +87,7 @@ struct GemmArgs {
     int experts, n_tiles;
     int box_rows, sf_groups;
     int stages, splits, persistent;
+    int gated;               // grouped SwiGLU epilogue: y = silu(gate) * up, [m][n/2]
     int num_tiles;           // dense (grouped counts tiles on the device)
     uint32_t tmem_cols;
     uint64_t wait_ns;        // limit of every pipeline wait
@@ -497,7 +498,10 @@ __global__ void __launch_bounds__(32 * num_warps(TT, PIPES),
     const int per = tokens_per_owner(TT, splits);
 
     uint8_t* partial = smem + ST * G::kStageBytes;  // split-K partials [splits][128][per] f32
-    uint8_t* ctrl = partial + (reduce ? splits * per * 512 : 0);
+    // Gated epilogue: the up half of each tile's accumulator passes through
+    // xbuf [TT columns][64 rows] FP32 to the gate half.
+    float* xbuf = reinterpret_cast<float*>(partial + (reduce ? splits * per * 512 : 0));
+    uint8_t* ctrl = reinterpret_cast<uint8_t*>(xbuf) + (p.gated ? 64 * TT * 4 : 0);
     Ctx c;
     c.smem = smem;
     c.full = reinterpret_cast<uint64_t*>(ctrl);
@@ -507,7 +511,9 @@ __global__ void __launch_bounds__(32 * num_warps(TT, PIPES),
     c.acc_empty = c.acc_full + 1;
     c.drain = c.acc_empty + 1;  // [PIPES]
     uint64_t* red = c.drain + PIPES;  // split-K: the peers' partials have landed
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red + 1);
+    uint64_t* xfull = red + 1;        // gated: the up half of a tile is in xbuf
+    uint64_t* xempty = red + 2;       // gated: the gate half has read it
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red + 3);
     c.abort_flag = tmem_slot + 1;
     int* prefix = reinterpret_cast<int*>(tmem_slot + 2);   // [experts + 1]
     int* offs = prefix + (kMaxExperts + 1);                 // [experts + 1]
@@ -533,6 +539,10 @@ __global__ void __launch_bounds__(32 * num_warps(TT, PIPES),
         mbar_init(c.acc_full, PIPES);
         mbar_init(c.acc_empty, kEpi);
         for (int q = 0; q < PIPES; ++q) mbar_init(&c.drain[q], 1);
+        if (p.gated) {
+            mbar_init(xfull, kEpi / 2);   // one arrival per up-half warp
+            mbar_init(xempty, kEpi / 2);  // one arrival per gate-half warp
+        }
         if (reduce) {
             // Bytes the other ranks push into this rank's slice of the tile.
             mbar_init(red, 1);
@@ -668,6 +678,36 @@ __global__ void __launch_bounds__(32 * num_warps(TT, PIPES),
                 for (int j = 0; j < kCols; j += 4)
                     stg[((col0 + j) >> 2) * 128 + nl] = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
                 fence_proxy_async_smem();
+            } else if (p.gated) {
+                // SwiGLU: rows [0, 64) of the tile are gate rows, [64, 128) the
+                // matching up rows (gated-row order of the prepared weights);
+                // output feature ti.n_tile * 64 + nl of h = silu(gate) * up.
+                const bool up_half = nl >= 64;  // warp-uniform
+                const int inter = p.n >> 1;
+                if (up_half) {
+                    bool okx = tile_iter == 0 || mbar_wait(xempty, (tile_iter - 1) & 1, p.wait_ns);
+                    okx = __all_sync(0xFFFFFFFFu, okx ? 1 : 0) != 0;
+                    if (!okx) { if (lane == 0) record_timeout(c.abort_flag); break; }
+#pragma unroll
+                    for (int j = 0; j < kCols; ++j) xbuf[(col0 + j) * 64 + (nl - 64)] = acc[j];
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(xfull);
+                } else {
+                    bool okx = mbar_wait(xfull, tile_iter & 1, p.wait_ns);
+                    okx = __all_sync(0xFFFFFFFFu, okx ? 1 : 0) != 0;
+                    if (!okx) { if (lane == 0) record_timeout(c.abort_flag); break; }
+                    const int f = ti.n_tile * 64 + nl;
+                    const int jmax = min(kCols, ti.count - col0);
+                    __nv_bfloat16* hp = p.y + static_cast<size_t>(ti.tok0 + col0) * inter + f;
+#pragma unroll
+                    for (int j = 0; j < kCols; ++j) {
+                        const float g = acc[j];
+                        const float hv = g / (1.0f + expf(-g)) * xbuf[(col0 + j) * 64 + nl];
+                        if (j < jmax) hp[static_cast<size_t>(j) * inter] = __float2bfloat16_rn(hv);
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(xempty);
+                }
             } else if (n < p.n) {
                 const int jmax = min(kCols, ti.count - col0);
                 __nv_bfloat16* yp = p.y + static_cast<size_t>(ti.tok0 + col0) * p.n + n;
@@ -1112,7 +1152,7 @@ struct LaunchPlan {
 };
 
 template <int TT, int PIPES>
-LaunchPlan plan_for(int splits, bool persistent, int kq) {
+LaunchPlan plan_for(int splits, bool persistent, int kq, bool gated) {
     using G = Geometry<TT>;
     LaunchPlan lp;
     // Pipeline depth: as many stages as fit next to the partial buffer and
@@ -1120,7 +1160,8 @@ LaunchPlan plan_for(int splits, bool persistent, int kq) {
     // one-tile CTA never needs more than its K blocks).
     const int ctrl = 8 * 64 + 8 + 4 * 2 * (kMaxExperts + 1) + 64;  // barriers, slots, prefix/offsets
     lp.partial = splits > 1 ? splits * tokens_per_owner(TT, splits) * 512 : 0;
-    const int budget = 227 * 1024 - 1024 - ctrl - lp.partial;
+    const int xbuf = gated ? 64 * TT * 4 : 0;
+    const int budget = 227 * 1024 - 1024 - ctrl - lp.partial - xbuf;
     int stages = budget / (PIPES * G::kStageBytes);
     if (stages * PIPES > 8) stages = 8 / PIPES;
     if (!persistent) {
@@ -1137,7 +1178,7 @@ LaunchPlan plan_for(int splits, bool persistent, int kq) {
     }
     lp.stages = stages;
     lp.tmem_cols = pow2_cols(PIPES * TT + PIPES * stages * G::kSfSlotCols);
-    lp.smem = 1024 + static_cast<size_t>(PIPES * stages) * G::kStageBytes + lp.partial + ctrl;
+    lp.smem = 1024 + static_cast<size_t>(PIPES * stages) * G::kStageBytes + lp.partial + xbuf + ctrl;
     return lp;
 }
 
@@ -1167,7 +1208,7 @@ cudaError_t launch_tt(const GemmProblem& pr, const GemmSchedule& sch, int num_sm
     const int tok_tiles = static_cast<int>((pr.m + TT - 1) / TT);
     const int n_tiles = static_cast<int>(pr.n_pad / 128);
     const int splits = sch.persistent ? 1 : sch.split_k;
-    const LaunchPlan lp = plan_for<TT, PIPES>(splits, sch.persistent, kq);
+    const LaunchPlan lp = plan_for<TT, PIPES>(splits, sch.persistent, kq, pr.gated);
     if (lp.stages < 1) return cudaErrorInvalidConfiguration;
     // Split-K partials are staged in the pipeline stages, one slot per rank.
     if (splits > 1 &&
@@ -1189,6 +1230,7 @@ cudaError_t launch_tt(const GemmProblem& pr, const GemmSchedule& sch, int num_sm
     a.n_tiles = n_tiles;
     a.splits = splits;
     a.persistent = sch.persistent ? 1 : 0;
+    a.gated = pr.gated ? 1 : 0;
     a.stages = lp.stages;
     a.tmem_cols = lp.tmem_cols;
     a.wait_ns = g_wait_limit_ns ? g_wait_limit_ns : kWaitNs;
@@ -1334,6 +1376,7 @@ GemmSchedule choose_schedule(const GemmProblem& p, int num_sms, int force_tt, in
         tt = p.m <= 16 ? 16 : p.m <= 32 ? 32 : p.m <= 128 ? 64 : 256;
     }
     if (force_tt) tt = force_tt;
+    if (p.gated && tt > 128) tt = 128;  // the gated exchange buffer holds 64 x TT FP32
     // Dense large M: two weight tiles x 192 tokens per CTA tile whenever
     // that still gives every SM a tile (measured on 8192^3).
     bool dual = false;

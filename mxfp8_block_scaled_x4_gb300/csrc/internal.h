@@ -8,15 +8,27 @@
 namespace mxk {
 
 // Activation quantizer, 8x4 scale layout.  It lets a dependent grid launched
-// with programmatic stream serialization start its prologue early.
+// with programmatic stream serialization start its prologue early.  With
+// src_rows, output row r quantizes input row src_rows[r].
 cudaError_t launch_quant_act(const void* x, int64_t m, int64_t k, uint8_t* q, uint8_t* sf,
-                             int num_sms, cudaStream_t s);
+                             int num_sms, cudaStream_t s, const int32_t* src_rows = nullptr);
 
 // Weight preparation: quantize + pad N + prepared layout.  src_is_bf16
-// selects the element type of src ([experts][n][k]).
+// selects the element type of src ([experts][n][k]); inter > 0 applies the
+// gated-row reorder of GEMM1 weights [gate; up] with n = 2 * inter.
 cudaError_t launch_prepare_weight(const void* src, bool src_is_bf16, int64_t experts, int64_t n,
                                   int64_t n_pad, int64_t k, uint8_t* q, uint8_t* sf, int num_sms,
-                                  cudaStream_t s);
+                                  cudaStream_t s, int64_t inter = 0);
+
+// Mixture-of-experts helpers (moe.cu).  Routing: top-k per token, weights,
+// and the stable expert-sorted order; ws holds ceil(tokens/32) * experts
+// group counts plus tokens * topk ranks (int32).
+cudaError_t launch_moe_route(const float* logits, int64_t tokens, int64_t experts, int64_t topk, int method,
+                             int32_t* ids, float* weights, int32_t* offsets, int32_t* sorted_token,
+                             int32_t* row_of, int32_t* ws, cudaStream_t s);
+// out[t] = bf16(sum_s weights[t, s] * y2[row_of[t * topk + s]]), FP32 sum in slot order.
+cudaError_t launch_moe_finalize(const void* y2, const int32_t* row_of, const float* weights, int64_t tokens,
+                                int64_t topk, int64_t hidden, void* out, int num_sms, cudaStream_t s);
 
 struct GemmProblem {
     const uint8_t* qa;         // [m][k] E4M3 activations
@@ -30,6 +42,7 @@ struct GemmProblem {
     void* y;                   // bf16 [m][n]
     const int32_t* offsets;    // grouped: device [experts + 1]; dense: null
     const void* x;             // bf16 [m][k] activations when the GEMM may quantize them itself
+    bool gated;                // grouped only: SwiGLU epilogue, y = silu(gate) * up, bf16 [m][n/2]
 };
 
 struct GemmSchedule {

@@ -49,8 +49,11 @@ __device__ __forceinline__ void st_v2(void* p, uint2 v) {
 // 16-byte stores, and the patch's 32 scale bytes -- exactly one 8x4 tile, byte
 // (row%8)*4 + block%4 = lane -- go out as one coalesced 32-byte store.  Rows in
 // [m, m8) quantize zeros and write only their (zero) scales.
+// With `src_rows`, output row r reads input row src_rows[r] (a gather, e.g.
+// tokens into expert-sorted order).
 __global__ void __launch_bounds__(kThreads) quant_act_kernel(const __nv_bfloat16* __restrict__ x,
                                                              int64_t m, int64_t m8, int64_t k,
+                                                             const int32_t* __restrict__ src_rows,
                                                              uint8_t* __restrict__ q,
                                                              uint8_t* __restrict__ sf) {
     // Dependent kernels (the GEMM) may start their prologue now; they wait
@@ -78,7 +81,8 @@ __global__ void __launch_bounds__(kThreads) quant_act_kernel(const __nv_bfloat16
 #pragma unroll
             for (int i = 0; i < 4; ++i) raw[u][i] = make_uint4(0, 0, 0, 0);
             if (t < total && row[u] < m) {
-                const __nv_bfloat16* src = x + row[u] * k + col[u];
+                const int64_t sr = src_rows ? static_cast<int64_t>(src_rows[row[u]]) : row[u];
+                const __nv_bfloat16* src = x + sr * k + col[u];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) raw[u][i] = *reinterpret_cast<const uint4*>(src + i * 8);
             }
@@ -100,12 +104,15 @@ __global__ void __launch_bounds__(kThreads) quant_act_kernel(const __nv_bfloat16
 }
 
 // Weights: experts x rows [0, n_pad) x chunks.  Rows >= n write zero data and
-// zero scales.  Scale word of (row r, 4-block group g) in the prepared layout:
+// zero scales.  With `inter` > 0 (gated GEMM1 weights [gate; up], n = 2 inter)
+// prepared row r of 128-row tile j = r / 128 reads gate row 64 j + r % 128
+// for r % 128 < 64, else up row inter + 64 j + r % 128 - 64 (gated-row
+// reorder: one tile yields 64 features of silu(gate) * up).  Scale word of (row r, 4-block group g) in the prepared layout:
 // tile (r/128, g) of 512 bytes, inner offset (r%32)*16 + ((r%128)/32)*4.
 template <bool kBf16>
 __global__ void __launch_bounds__(kThreads)
     prepare_weight_kernel(const void* __restrict__ src, int64_t experts, int64_t n, int64_t n_pad,
-                          int64_t k, uint8_t* __restrict__ q, uint8_t* __restrict__ sf) {
+                          int64_t k, int64_t inter, uint8_t* __restrict__ q, uint8_t* __restrict__ sf) {
     const int lane = threadIdx.x & 31;
     const int64_t chunks = k >> 8;
     const int64_t kq = k >> 7;
@@ -119,7 +126,9 @@ __global__ void __launch_bounds__(kThreads)
         const int64_t r = rowp - e * n_pad;
         float v[8];
         if (r < n) {
-            const int64_t off = (e * n + r) * k + chunk * 256 + lane * 8;
+            const int64_t o = r & 127;
+            const int64_t sr = inter <= 0 ? r : (o < 64 ? (r >> 7) * 64 + o : inter + (r >> 7) * 64 + o - 64);
+            const int64_t off = (e * n + sr) * k + chunk * 256 + lane * 8;
             if (kBf16) {
                 bf16x8_to_float(ld_nc_v4(static_cast<const __nv_bfloat16*>(src) + off), v);
             } else {
@@ -162,7 +171,7 @@ int grid_for(int64_t warps_of_work, int num_sms, int per_warp) {
 }  // namespace
 
 cudaError_t launch_quant_act(const void* x, int64_t m, int64_t k, uint8_t* q, uint8_t* sf,
-                             int num_sms, cudaStream_t s) {
+                             int num_sms, cudaStream_t s, const int32_t* src_rows) {
     const int64_t m8 = (m + 7) / 8 * 8;
     const int64_t work = (m8 / 8) * (k / 128);
     cudaLaunchConfig_t cfg;
@@ -175,18 +184,19 @@ cudaError_t launch_quant_act(const void* x, int64_t m, int64_t k, uint8_t* q, ui
     attr.val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, quant_act_kernel, static_cast<const __nv_bfloat16*>(x), m, m8, k, q, sf);
+    return cudaLaunchKernelEx(&cfg, quant_act_kernel, static_cast<const __nv_bfloat16*>(x), m, m8, k, src_rows, q,
+                              sf);
 }
 
 cudaError_t launch_prepare_weight(const void* src, bool src_is_bf16, int64_t experts, int64_t n,
                                   int64_t n_pad, int64_t k, uint8_t* q, uint8_t* sf, int num_sms,
-                                  cudaStream_t s) {
+                                  cudaStream_t s, int64_t inter) {
     const int64_t work = experts * n_pad * (k / 256);
     const int grid = grid_for(work, num_sms, 2);
     if (src_is_bf16)
-        prepare_weight_kernel<true><<<grid, kThreads, 0, s>>>(src, experts, n, n_pad, k, q, sf);
+        prepare_weight_kernel<true><<<grid, kThreads, 0, s>>>(src, experts, n, n_pad, k, inter, q, sf);
     else
-        prepare_weight_kernel<false><<<grid, kThreads, 0, s>>>(src, experts, n, n_pad, k, q, sf);
+        prepare_weight_kernel<false><<<grid, kThreads, 0, s>>>(src, experts, n, n_pad, k, inter, q, sf);
     return cudaGetLastError();
 }
 

@@ -24,8 +24,10 @@ Readings where the pages are silent (each listed in the design notes):
   * The per-expert rows are the (token, slot) pairs sorted by expert, then
     token (stable); offsets are the exclusive prefix of per-expert counts.
   * The intermediate activation h is a BF16 tensor (round to nearest even),
-    quantized to MXFP8 like any layer input before GEMM2.
-  * The output of token t is sum_s w[t,s] * GEMM2(h)[row(t,s)], no bias.
+    quantized to MXFP8 like any layer input before GEMM2; GEMM2's output is
+    BF16 too (every GEMM of the layer emits BF16, as the linear layer does).
+  * The output of token t is sum_s w[t,s] * y2[row(t,s)] over its k slots
+    (y2 the BF16 GEMM2 rows), no bias; returned unrounded (float64).
 """
 import numpy as np
 
@@ -130,6 +132,21 @@ def prepare_experts(w):
     return q, sf
 
 
+def down_finalize(h_sorted, off, row_of, weights, w2q, w2sf, rows):
+    """GEMM2 of given expert-sorted h rows (BF16 values) and the weighted sum
+    per token: out[a] = sum_s weights[t,s] * bf16(GEMM2(h)[row(t,s)]) for the
+    tokens t = rows[a]."""
+    k = weights.shape[1]
+    need = np.array(sorted(int(row_of[i * k + s]) for i in rows for s in range(k)), dtype=np.int64)
+    y2 = bf16_rne(grouped_linear(np.asarray(h_sorted, dtype=np.float32), off, w2q, w2sf, rows=need))
+    pos = {int(r): j for j, r in enumerate(need)}
+    out = np.zeros((len(rows), w2q.shape[1]), dtype=np.float64)
+    for a, i in enumerate(rows):
+        for s in range(k):
+            out[a] += weights[i, s] * y2[pos[int(row_of[i * k + s])]]
+    return out
+
+
 def expert_mlp(x, ids, weights, w13q, w13sf, w2q, w2sf, rows=None):
     """The expert MLP of one MoE layer for given routing.
 
@@ -152,7 +169,7 @@ def expert_mlp(x, ids, weights, w13q, w13sf, w2q, w2sf, rows=None):
     h = bf16_rne(silu(gu[:, :inter]) * gu[:, inter:])
     h_full = np.zeros((t * k, inter), dtype=np.float32)
     h_full[need] = h.astype(np.float32)                                # exact (BF16 values)
-    y2 = grouped_linear(h_full, off, w2q, w2sf, rows=need)              # [len(need), H]
+    y2 = bf16_rne(grouped_linear(h_full, off, w2q, w2sf, rows=need))    # [len(need), H], BF16 values
     pos = {int(r): j for j, r in enumerate(need)}
     out = np.zeros((len(toks), hdim), dtype=np.float64)
     for a, i in enumerate(toks):

@@ -14,7 +14,8 @@ import re
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "mxfp8.h")
+HEADERS = [os.path.join(ROOT, "include", h) for h in sorted(os.listdir(os.path.join(ROOT, "include")))
+           if h.endswith(".h")]
 
 
 @pytest.fixture(scope="module")
@@ -26,16 +27,20 @@ def mx():
 
 
 def declared_functions():
-    src = open(HEADER).read()
-    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    names = re.findall(r"^\s*[\w\s\*]+?\b(mxfp8_\w+)\s*\(", src, flags=re.M)
+    names = []
+    for h in HEADERS:
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        names += re.findall(r"^\s*[\w\s\*]+?\b(mxfp8_\w+)\s*\(", src, flags=re.M)
     return sorted(set(names))
 
 
 def test_header_declares_the_boundary():
     names = declared_functions()
     for required in ("mxfp8_prepare_weight", "mxfp8_quantize_act", "mxfp8_linear",
-                     "mxfp8_gemm", "mxfp8_grouped_linear", "mxfp8_act_scale_bytes"):
+                     "mxfp8_gemm", "mxfp8_grouped_linear", "mxfp8_act_scale_bytes",
+                     "mxfp8_moe_route", "mxfp8_prepare_gate_up_weight", "mxfp8_moe_gate_up_swiglu",
+                     "mxfp8_moe_finalize", "mxfp8_moe_expert_mlp"):
         assert required in names
 
 
@@ -114,3 +119,19 @@ def test_argument_errors_before_launch(mx):
     # prepare: bad dtype, misaligned source
     assert lib.mxfp8_prepare_weight(A, 7, wp, None) == 1
     assert lib.mxfp8_prepare_weight(A + 4, 0, wp, None) == 3
+
+
+def test_moe_size_helpers_and_argument_checks(mx):
+    lib = mx.library()
+    assert lib.mxfp8_moe_route_workspace_bytes(256, 128, 8) == ((256 + 31) // 32 * 128 + 256 * 8) * 4
+    assert lib.mxfp8_moe_route_workspace_bytes(-1, 128, 8) == 0
+    assert lib.mxfp8_moe_workspace_bytes(256, 128, 17, 2048, 768) == 0   # topk > 16
+    assert lib.mxfp8_moe_workspace_bytes(256, 4, 8, 2048, 768) == 0      # topk > experts
+    assert lib.mxfp8_moe_workspace_bytes(256, 128, 8, 2048, 768) > 0
+    assert lib.mxfp8_moe_gate_up_workspace_bytes(2048, 2048) == mx.linear_workspace_bytes(2048, 2048)
+    # checked before the device is touched (1 = MXFP8_ERR_INVALID_ARG)
+    assert lib.mxfp8_moe_route(None, 4, 8, 0, 0, None, None, None, None, None, None, 0, None) == 1
+    assert lib.mxfp8_moe_route(None, 4, 8, 2, 5, None, None, None, None, None, None, 0, None) == 1
+    assert lib.mxfp8_moe_route(None, 0, 8, 2, 0, None, None, None, None, None, None, 0, None) == mx.OK
+    assert lib.mxfp8_moe_finalize(None, None, None, 4, 2, 12, None, None) == 1  # hidden % 8: invalid argument
+    assert lib.mxfp8_moe_finalize(None, None, None, 0, 2, 16, None, None) == mx.OK

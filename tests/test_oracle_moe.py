@@ -130,7 +130,7 @@ def _dense_reference(x, ids, w, w13q, w13sf, w2q, w2sf):
             hh = M.bf16_rne(M.silu(gu[:inter]) * gu[inter:])
             hq, hsf = oracle.quantize_rows(hh.astype(np.float32)[None, :])
             hd = oracle.dequant_rows(hq, hsf)[0]
-            out[i] += w[i, s] * (oracle.dequant_rows(w2q[ex], w2sf[ex]) @ hd)
+            out[i] += w[i, s] * M.bf16_rne(oracle.dequant_rows(w2q[ex], w2sf[ex]) @ hd)
     return out
 
 
@@ -166,3 +166,19 @@ def test_expert_mlp_gate_and_up_are_not_interchangeable():
     sw = np.concatenate([w13[:, inter:], w13[:, :inter]], axis=1)
     b, _, _ = M.expert_mlp(x, ids, w, *M.prepare_experts(sw), *M.prepare_experts(w2))
     assert not np.allclose(a, b)
+
+
+def test_down_finalize_agrees_with_expert_mlp():
+    rng = np.random.default_rng(12)
+    t, h, inter, e, k = 5, 64, 64, 3, 2
+    x = rng.standard_normal((t, h)).astype(np.float32)
+    logits = rng.standard_normal((t, e))
+    w13 = rng.standard_normal((e, 2 * inter, h)) * 0.1
+    w2 = rng.standard_normal((e, h, inter)) * 0.1
+    w13q, w13sf = M.prepare_experts(w13)
+    w2q, w2sf = M.prepare_experts(w2)
+    ids, w = M.route(logits, k)
+    out, hv, off = M.expert_mlp(x, ids, w, w13q, w13sf, w2q, w2sf)
+    _, _, row_of = M.sort_by_expert(ids, e)
+    out2 = M.down_finalize(hv, off, row_of, w, w2q, w2sf, list(range(t)))
+    assert np.array_equal(out, out2)

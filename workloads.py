@@ -22,6 +22,12 @@ Workload-specific structure:
     2048 (token, expert) pairs stable-sorted by (expert, token); expert e owns
     rows [off[e], off[e+1]) of x_sorted, x_sorted[r] = x[token(r)]; K=2048,
     per-expert N=1536, no bias.
+  * MoE expert MLP (the whole layer around the grouped gate_up): tokens x
+    ~ N(0, 1) rounded to BF16, router logits ~ N(0, 1) float32, GEMM1 weights
+    [E, 2I, H] and GEMM2 weights [E, H, I] ~ N(0, 0.02) float32; 256 tokens,
+    128 experts, top-8, H=2048, I=768 (the shapes of the gate_up workload
+    plus its down projection).  The routing itself is part of the method and
+    is not done here.
 These stand in for the layers of the 30B-A3B MoE model the pages benchmark
 end to end; no dataset or checkpoint is involved.
 """
@@ -167,3 +173,33 @@ def grouped_from_counts(counts, n, k, seed, bias=False) -> Grouped:
     b = bf16_round(normal(rng, (e, n), 0.1)) if bias else None
     return Grouped("grouped_counts_e%d_n%d_k%d" % (e, n, k), rows, e, 1, n, k, x,
                    off, np.arange(rows, dtype=np.int64), w, b, seed)
+
+
+@dataclass
+class Moe:
+    name: str
+    tokens: int
+    experts: int
+    topk: int
+    hidden: int
+    inter: int
+    x: np.ndarray                 # float32 [tokens, hidden], exact BF16 values
+    logits: np.ndarray            # float32 [tokens, experts]
+    w13: np.ndarray               # float32 [experts, 2*inter, hidden], rows [gate; up]
+    w2: np.ndarray                # float32 [experts, hidden, inter]
+    seed: int = 0
+
+
+def moe(seed=6, tokens=256, experts=128, topk=8, hidden=2048, inter=768, logit_ties=False) -> Moe:
+    """Inputs of one MoE expert-MLP layer.  logit_ties: integer-valued logits
+    in [-3, 3] (many equal logits, to exercise the tie rule)."""
+    rng = np.random.default_rng(seed)
+    x = bf16_round(normal(rng, (tokens, hidden)))
+    if logit_ties:
+        logits = rng.integers(-3, 4, size=(tokens, experts)).astype(np.float32)
+    else:
+        logits = normal(rng, (tokens, experts))
+    w13 = normal(rng, (experts, 2 * inter, hidden), 0.02)
+    w2 = normal(rng, (experts, hidden, inter), 0.02)
+    return Moe("moe_t%d_e%d_top%d_h%d_i%d" % (tokens, experts, topk, hidden, inter),
+               tokens, experts, topk, hidden, inter, x, logits, w13, w2, seed)
