@@ -54,7 +54,7 @@ def parse_args():
     ap.add_argument("--no-configs", action="store_true", help="skip the per-workload table")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle CPU-baseline budget")
     ap.add_argument("--workload", default="decode16",
-                    choices=["decode16", "decode1", "tiny", "mid", "mid130", "prefill", "grouped"],
+                    choices=["decode16", "decode1", "tiny", "mid", "mid130", "prefill", "grouped", "moe"],
                     help="decode16 = the contract line; any other runs only that workload "
                          "for --steps calls (profiling aid) and prints its table entry")
     return ap.parse_args()
@@ -324,6 +324,47 @@ def measure_grouped(mx, peaks, calls=200):
     return out
 
 
+def measure_moe(mx, peaks, calls=200):
+    """The whole MoE expert MLP (routing, gather + quantize, gated GEMM1 with
+    SwiGLU, quantize h, GEMM2, top-k finalize) of the 256-token, 128-expert,
+    top-8 layer with H=2048, I=768.  HBM-bound: both weight sets stream once
+    per call (604 MB > L2)."""
+    import torch
+    import workloads
+    g = workloads.moe()
+    w13 = mx.prepare_gate_up_weight(torch.from_numpy(g.w13).cuda())
+    w2 = mx.prepare_weight(torch.from_numpy(g.w2).cuda())
+    x = torch.from_numpy(g.x).cuda().to(torch.bfloat16)
+    lg = torch.from_numpy(g.logits).cuda()
+    ws = torch.empty(mx.moe_workspace_bytes(g.tokens, g.experts, g.topk, g.hidden, g.inter),
+                     dtype=torch.uint8, device="cuda")
+    out = torch.empty((g.tokens, g.hidden), dtype=torch.bfloat16, device="cuda")
+    lib = mx.library()
+    import ctypes
+
+    def call(i):
+        st = lib.mxfp8_moe_expert_mlp(ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(lg.data_ptr()), g.tokens,
+                                      g.topk, 0, ctypes.byref(w13.c), ctypes.byref(w2.c),
+                                      ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(ws.data_ptr()),
+                                      ws.numel(), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+        assert st == 0, st
+
+    ms = time_steps(call, calls, warmup=10) / calls
+    rows = g.tokens * g.topk
+    flops = 2.0 * rows * (2 * g.inter) * g.hidden + 2.0 * rows * g.hidden * g.inter
+    wb = weight_bytes(2 * g.inter, g.hidden, g.experts) + weight_bytes(g.hidden, g.inter, g.experts)
+    # algorithmic bytes: weights + x + logits + out (the intermediates stay in L2)
+    nbytes = wb + 2 * g.tokens * g.hidden + 4 * g.tokens * g.experts + 2 * g.tokens * g.hidden
+    res = {"tokens": g.tokens, "experts": g.experts, "topk": g.topk, "hidden": g.hidden, "inter": g.inter,
+           "us_per_call": ms * 1e3, "tflops": flops / (ms * 1e-3) / 1e12, "weight_gbs": wb / (ms * 1e-3) / 1e9,
+           "alg_gbs": nbytes / (ms * 1e-3) / 1e9, "flops": flops, "alg_bytes": nbytes,
+           "note": "route + gate_up/SwiGLU + down + finalize; weights (604 MB) exceed L2; single copy"}
+    res.update(roofline_entry(flops, nbytes, ms, peaks))
+    del w13, w2, x, lg, ws, out
+    torch.cuda.empty_cache()
+    return res
+
+
 # ------------------------------------------------------------ CPU baseline
 def oracle_sample(d, budget_s, max_calls=None):
     """Time the CPU oracle (one core) on whole output column blocks of the
@@ -425,6 +466,8 @@ def main():
                     "prefill": workloads.prefill}
         if args.workload == "grouped":
             res = measure_grouped(mx, peaks, args.steps)
+        elif args.workload == "moe":
+            res = measure_moe(mx, peaks, args.steps)
         else:
             res = measure_config(mx, args.workload, builders[args.workload](), peaks, args.steps)
         res["workload"] = args.workload
@@ -493,6 +536,7 @@ def main():
         cfgs["mid_m128_n130_k4096_bias"] = measure_config(mx, "mid130", workloads.mid(n=130, bias=True), peaks, 2000)
         cfgs["prefill_m8192_n8192_k8192"] = measure_config(mx, "prefill", workloads.prefill(), peaks, 40)
         cfgs["grouped_t256_e128_top8_n1536_k2048"] = measure_grouped(mx, peaks, 200)
+        cfgs["moe_mlp_t256_e128_top8_h2048_i768"] = measure_moe(mx, peaks, 200)
         for v in cfgs.values():
             v["peaks"] = peak_src
         out["configs"] = cfgs

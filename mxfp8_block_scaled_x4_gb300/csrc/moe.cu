@@ -8,10 +8,10 @@
 // exact arithmetic), in descending order, ties to the lower expert id.  The
 // (token, slot) pairs are then sorted by expert, then token -- stable and
 // deterministic, no atomics:
-//   route_topk_kernel   one lane per token: top-k by insertion over the
-//                       logits, the weights, and per 32-token group a ballot
-//                       per expert -> group counts and each pair's rank
-//                       inside its group;
+//   route_topk_kernel   one CTA per 32-token group, one warp per token: k
+//                       rounds of warp arg-max over the logits, the weights,
+//                       then per-expert token masks -> group counts and each
+//                       pair's rank inside its group;
 //   route_scan_kernel   one CTA: per-expert totals -> offsets, and per
 //                       (group, expert) the first sorted row of that group;
 //   route_assign_kernel row_of[t*k + s] and sorted_token[row].
@@ -28,80 +28,101 @@ namespace mxk {
 namespace {
 
 constexpr int kMaxTopK = 16;
-constexpr int kRouteThreads = 128;
+constexpr int kMaxExpertsRoute = 1024;
 
-__global__ void __launch_bounds__(kRouteThreads)
+// (v, e) ranks above (bv, be): larger logit, or equal logit and lower id.
+__device__ __forceinline__ bool better(float v, int e, float bv, int be) {
+    return v > bv || (v == bv && e < be);
+}
+
+// One CTA per group of 32 tokens, one warp per token.  Round r of a warp
+// picks the best (logit, id) among the candidates ranked below round r-1's
+// pick (so earlier picks are excluded without storing them) with a strided
+// scan per lane and a butterfly arg-max.  Then the group's picks go into
+// per-expert 32-bit token masks in shared memory (atomicOr: the result does
+// not depend on the order), which give the group count of every expert and
+// each pair's rank among the group's tokens.
+__global__ void __launch_bounds__(1024)
     route_topk_kernel(const float* __restrict__ logits, int tokens, int experts, int topk, int method,
                       int32_t* __restrict__ ids, float* __restrict__ weights,
                       int32_t* __restrict__ grp_count, int32_t* __restrict__ rank) {
+    __shared__ int sel[32][kMaxTopK];
+    __shared__ unsigned bits[kMaxExpertsRoute];
     const int lane = threadIdx.x & 31;
-    const int group = (blockIdx.x * kRouteThreads + threadIdx.x) >> 5;
-    const int t = group * 32 + lane;
-    const bool live = t < tokens;
-    if (group * 32 >= tokens) return;  // warp-uniform
-    float v[kMaxTopK];
-    int id[kMaxTopK];
+    const int w = threadIdx.x >> 5;
+    const int group = blockIdx.x;
+    const int t = group * 32 + w;
+    for (int e = threadIdx.x; e < experts; e += blockDim.x) bits[e] = 0u;
+    if (t < tokens) {
+        const float* lg = logits + static_cast<size_t>(t) * experts;
+        float pv = INFINITY;
+        int pe = -1;  // previous pick; round 0 admits everything
+        float top[kMaxTopK];
 #pragma unroll
-    for (int i = 0; i < kMaxTopK; ++i) { v[i] = -INFINITY; id[i] = 0x7FFFFFFF; }
-    const float* lg = logits + static_cast<size_t>(live ? t : 0) * experts;
-    if (live) {
-        // Insertion over ascending expert ids: a new logit goes after every
-        // kept entry >= it, so equal logits keep the lower id first.
-        for (int e = 0; e < experts; ++e) {
-            const float x = lg[e];
-            if (!(x > v[topk - 1]) && id[topk - 1] != 0x7FFFFFFF) continue;
-#pragma unroll
-            for (int i = kMaxTopK - 1; i >= 0; --i) {
-                if (i >= topk) continue;
-                // Slots x beats move down by one; x lands below the last
-                // entry it does not beat.
-                const bool beats_here = x > v[i] || id[i] == 0x7FFFFFFF;
-                if (!beats_here) continue;
-                const bool goes_higher = i > 0 && (x > v[i > 0 ? i - 1 : 0] || id[i > 0 ? i - 1 : 0] == 0x7FFFFFFF);
-                if (goes_higher) { v[i] = v[i - 1]; id[i] = id[i - 1]; }
-                else { v[i] = x; id[i] = e; }
+        for (int r = 0; r < kMaxTopK; ++r) {
+            if (r >= topk) break;
+            float bv = -INFINITY;
+            int be = 0x7FFFFFFF;
+            for (int e = lane; e < experts; e += 32) {
+                const float v = lg[e];
+                if (better(pv, pe, v, e) && better(v, e, bv, be)) { bv = v; be = e; }
             }
+#pragma unroll
+            for (int d = 16; d > 0; d >>= 1) {
+                const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, d);
+                const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, d);
+                if (better(ov, oe, bv, be)) { bv = ov; be = oe; }
+            }
+            top[r] = bv;
+            if (lane == 0) {
+                ids[static_cast<size_t>(t) * topk + r] = be;
+                sel[w][r] = be;
+            }
+            pv = bv;
+            pe = be;
         }
-        // Weights.  m = v[0] is the largest logit of the token.
+        // Weights (m = top[0] is the token's largest logit).
         float z[kMaxTopK];
         float zs = 0.0f;
 #pragma unroll
-        for (int i = 0; i < kMaxTopK; ++i) {
-            z[i] = i < topk ? expf(v[i] - v[0]) : 0.0f;
-            zs += z[i];
+        for (int r = 0; r < kMaxTopK; ++r) {
+            z[r] = r < topk ? expf(top[r] - top[0]) : 0.0f;
+            zs += z[r];
         }
         if (method == 1) {
-            // Softmax over all logits, then renormalize the selected ones.
+            // Softmax over all logits (lane-strided partial sums, then a
+            // fixed butterfly: deterministic), then renormalize the k picks.
             float all = 0.0f;
-            for (int e = 0; e < experts; ++e) all += expf(lg[e] - v[0]);
+            for (int e = lane; e < experts; e += 32) all += expf(lg[e] - top[0]);
+#pragma unroll
+            for (int d = 16; d > 0; d >>= 1) all += __shfl_xor_sync(0xFFFFFFFFu, all, d);
             float ps = 0.0f;
 #pragma unroll
-            for (int i = 0; i < kMaxTopK; ++i) {
-                z[i] = z[i] / all;
-                ps += i < topk ? z[i] : 0.0f;
+            for (int r = 0; r < kMaxTopK; ++r) {
+                z[r] = z[r] / all;
+                ps += r < topk ? z[r] : 0.0f;
             }
             zs = ps;
         }
+        if (lane < topk) {
+            float mine = 0.0f;
 #pragma unroll
-        for (int i = 0; i < kMaxTopK; ++i) {
-            if (i < topk) {
-                ids[static_cast<size_t>(t) * topk + i] = id[i];
-                weights[static_cast<size_t>(t) * topk + i] = z[i] / zs;
-            }
+            for (int r = 0; r < kMaxTopK; ++r)
+                if (r == lane) mine = z[r];
+            weights[static_cast<size_t>(t) * topk + lane] = mine / zs;
         }
     }
-    // Group counts and ranks: one ballot per expert over the group's tokens
-    // (a token picks an expert at most once).
-    const unsigned lt = (1u << lane) - 1u;
-    for (int e = 0; e < experts; ++e) {
-        int slot = -1;
-#pragma unroll
-        for (int i = 0; i < kMaxTopK; ++i)
-            if (live && i < topk && id[i] == e) slot = i;
-        const unsigned mask = __ballot_sync(0xFFFFFFFFu, slot >= 0);
-        if (lane == 0) grp_count[static_cast<size_t>(group) * experts + e] = __popc(mask);
-        if (slot >= 0) rank[static_cast<size_t>(t) * topk + slot] = __popc(mask & lt);
+    __syncthreads();
+    const int live = min(32, tokens - group * 32);
+    for (int i = threadIdx.x; i < live * topk; i += blockDim.x) atomicOr(&bits[sel[i / topk][i % topk]], 1u << (i / topk));
+    __syncthreads();
+    for (int i = threadIdx.x; i < live * topk; i += blockDim.x) {
+        const int tw = i / topk;
+        rank[static_cast<size_t>(group * 32 + tw) * topk + (i % topk)] =
+            __popc(bits[sel[tw][i % topk]] & ((1u << tw) - 1u));
     }
+    for (int e = threadIdx.x; e < experts; e += blockDim.x)
+        grp_count[static_cast<size_t>(group) * experts + e] = __popc(bits[e]);
 }
 
 // One CTA, thread e per expert (loops if experts > blockDim).  Replaces the
@@ -206,9 +227,8 @@ cudaError_t launch_moe_route(const float* logits, int64_t tokens, int64_t expert
     const int groups = static_cast<int>((tokens + 31) / 32);
     int32_t* grp = ws;
     int32_t* rank = ws + static_cast<size_t>(groups) * experts;
-    const int blocks = (groups * 32 + kRouteThreads - 1) / kRouteThreads;
-    route_topk_kernel<<<blocks, kRouteThreads, 0, s>>>(logits, static_cast<int>(tokens), static_cast<int>(experts),
-                                                       static_cast<int>(topk), method, ids, weights, grp, rank);
+    route_topk_kernel<<<groups, 1024, 0, s>>>(logits, static_cast<int>(tokens), static_cast<int>(experts),
+                                              static_cast<int>(topk), method, ids, weights, grp, rank);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     route_scan_kernel<<<1, 1024, 0, s>>>(groups, static_cast<int>(experts), grp, offsets);
