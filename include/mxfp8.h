@@ -186,6 +186,54 @@ mxfp8_status mxfp8_linear_static_scratch(const void* x, int64_t m, const mxfp8_w
                                          const void* bias, void* y, void* stream);
 int mxfp8_static_scratch_last_cuda_error(void);
 
+/* ------------------------------------------------------------------ tactics
+ * A tactic is a GEMM schedule, four int32:
+ *   [0] tokens per tile: 16, 32, 64, 128, 256, or 192 = two 128-row weight
+ *       tiles x 192 tokens per CTA tile (dense only);
+ *   [1] split_k: -1 = persistent tiles, 1..8 = one output tile per cluster
+ *       of that many CTAs with K split among them (tiles of <= 128 tokens,
+ *       dense only);
+ *   [2] fuse_quant: 1 = the GEMM quantizes x itself (one-tile mxfp8_linear);
+ *   [3] pipes: MMA pipelines per CTA, 1, 2 (tiles <= 64) or 4 (16 only).
+ * The tactic table maps (current device, call kind, power-of-two bucket of M,
+ * N, K, experts) to a tactic; every call consults it before the built-in
+ * heuristic.  The pages leave tactics to later work (vLLM PR #52204 "does
+ * not add tactic hints"; FlashInfer PR #1214 review: an autotuner with
+ * benching/perf tuning).  Tactics change the FP32 summation order, not the
+ * arithmetic: results stay within the layer tolerance and are deterministic
+ * for a given table. */
+typedef enum mxfp8_call_kind {
+    MXFP8_KIND_LINEAR = 0,  /* mxfp8_linear */
+    MXFP8_KIND_GEMM = 1,    /* mxfp8_gemm (pre-quantized activations) */
+    MXFP8_KIND_GROUPED = 2, /* mxfp8_grouped_linear */
+    MXFP8_KIND_GATED = 3    /* MoE GEMM1 with the SwiGLU epilogue (mxfp8_moe.h) */
+} mxfp8_call_kind;
+
+/* Times every valid tactic for this call (arguments as mxfp8_linear, `iters`
+ * timed calls each, <= 0 means 20) on the caller's buffers, stores the
+ * fastest in the table for the call's class and writes it to chosen[4] (may
+ * be NULL).  SYNCHRONOUS: it waits for the stream; not allowed while the
+ * stream is being captured (MXFP8_ERR_INVALID_ARG).  y is overwritten. */
+mxfp8_status mxfp8_autotune_linear(const void* x, int64_t m, const mxfp8_weight* w,
+                                   const void* bias, void* y, void* workspace,
+                                   size_t workspace_bytes, int iters, void* stream,
+                                   int32_t* chosen);
+/* The same for mxfp8_grouped_linear. */
+mxfp8_status mxfp8_autotune_grouped_linear(const void* x_sorted, int64_t rows,
+                                           const int32_t* expert_offsets,
+                                           const mxfp8_weight* w, const void* bias, void* y,
+                                           void* workspace, size_t workspace_bytes, int iters,
+                                           void* stream, int32_t* chosen);
+/* Table access (host only, no device work): get returns
+ * MXFP8_ERR_INVALID_ARG when the class has no entry; set validates the
+ * tactic for the kind and K. */
+mxfp8_status mxfp8_tactic_get(int kind, int64_t m, int64_t n, int64_t k, int64_t experts,
+                              int32_t* tactic);
+mxfp8_status mxfp8_tactic_set(int kind, int64_t m, int64_t n, int64_t k, int64_t experts,
+                              const int32_t* tactic);
+void mxfp8_tactic_clear(void);
+int64_t mxfp8_tactic_count(void);
+
 /* --------------------------------------------------------- status helpers */
 
 const char* mxfp8_status_string(mxfp8_status status);

@@ -95,6 +95,12 @@ def library():
         "mxfp8_set_wait_limit_ns": (None, [ctypes.c_uint64]),
         "mxfp8_set_pipes": (None, [ctypes.c_int]),
         "mxfp8_static_scratch_last_cuda_error": (ctypes.c_int, []),
+        "mxfp8_autotune_linear": (ctypes.c_int, [vp, i64, W, vp, vp, vp, sz, ctypes.c_int, vp, vp]),
+        "mxfp8_autotune_grouped_linear": (ctypes.c_int, [vp, i64, vp, W, vp, vp, vp, sz, ctypes.c_int, vp, vp]),
+        "mxfp8_tactic_get": (ctypes.c_int, [ctypes.c_int, i64, i64, i64, i64, vp]),
+        "mxfp8_tactic_set": (ctypes.c_int, [ctypes.c_int, i64, i64, i64, i64, vp]),
+        "mxfp8_tactic_clear": (None, []),
+        "mxfp8_tactic_count": (i64, []),
         "mxfp8_moe_route_workspace_bytes": (sz, [i64, i64, i64]),
         "mxfp8_moe_route": (ctypes.c_int, [vp, i64, i64, i64, ctypes.c_int, vp, vp, vp, vp, vp, vp, sz, vp]),
         "mxfp8_prepare_gate_up_weight": (ctypes.c_int, [vp, ctypes.c_int, W, vp]),
@@ -261,6 +267,70 @@ def grouped_linear(x_sorted: torch.Tensor, offsets: torch.Tensor, pw: PreparedWe
                                           _ptr(workspace), workspace.numel(), _stream(x_sorted)),
            "mxfp8_grouped_linear")
     return y
+
+
+# ----------------------------------------------------------------- tactics
+KIND_LINEAR, KIND_GEMM, KIND_GROUPED, KIND_GATED = 0, 1, 2, 3
+
+
+def _tactic_array(t=None):
+    a = (ctypes.c_int32 * 4)()
+    if t is not None:
+        for i, v in enumerate(t):
+            a[i] = int(v)
+    return a
+
+
+def autotune_linear(x: torch.Tensor, pw: PreparedWeight, bias=None, iters: int = 20, workspace=None):
+    """Time every valid tactic for this linear call on these buffers, store
+    the fastest in the tactic table and return it (tokens per tile, split_k,
+    fuse_quant, pipes).  Synchronous."""
+    _need(x.is_cuda and x.dtype == torch.bfloat16, "x must be bf16 CUDA")
+    x2 = x.reshape(-1, x.shape[-1]).contiguous()
+    m = x2.shape[0]
+    if workspace is None:
+        workspace = torch.empty((max(linear_workspace_bytes(m, pw.k), 16),), dtype=torch.uint8, device=x.device)
+    y = torch.empty((m, pw.n), dtype=torch.bfloat16, device=x.device)
+    out = _tactic_array()
+    _check(library().mxfp8_autotune_linear(_ptr(x2), m, ctypes.byref(pw.c), _ptr(bias), _ptr(y), _ptr(workspace),
+                                           workspace.numel(), iters, _stream(x), out), "mxfp8_autotune_linear")
+    return tuple(out)
+
+
+def autotune_grouped_linear(x_sorted: torch.Tensor, offsets: torch.Tensor, pw: PreparedWeight, bias=None,
+                            iters: int = 20, workspace=None):
+    """autotune_linear for the grouped (MoE expert) layer."""
+    _need(x_sorted.is_cuda and x_sorted.dtype == torch.bfloat16, "x_sorted must be bf16 CUDA")
+    x2 = x_sorted.contiguous()
+    rows = x2.shape[0]
+    if workspace is None:
+        workspace = torch.empty((max(linear_workspace_bytes(rows, pw.k), 16),), dtype=torch.uint8,
+                                device=x_sorted.device)
+    y = torch.empty((rows, pw.n), dtype=torch.bfloat16, device=x_sorted.device)
+    out = _tactic_array()
+    _check(library().mxfp8_autotune_grouped_linear(_ptr(x2), rows, _ptr(offsets.contiguous()), ctypes.byref(pw.c),
+                                                   _ptr(bias), _ptr(y), _ptr(workspace), workspace.numel(), iters,
+                                                   _stream(x_sorted), out), "mxfp8_autotune_grouped_linear")
+    return tuple(out)
+
+
+def tactic_get(kind: int, m: int, n: int, k: int, experts: int = 1):
+    """The stored tactic for a call class, or None."""
+    out = _tactic_array()
+    st = library().mxfp8_tactic_get(kind, m, n, k, experts, out)
+    return tuple(out) if st == OK else None
+
+
+def tactic_set(kind: int, m: int, n: int, k: int, experts: int, tactic) -> None:
+    _check(library().mxfp8_tactic_set(kind, m, n, k, experts, _tactic_array(tactic)), "mxfp8_tactic_set")
+
+
+def tactic_clear() -> None:
+    library().mxfp8_tactic_clear()
+
+
+def tactic_count() -> int:
+    return int(library().mxfp8_tactic_count())
 
 
 # -------------------------------------------------------------------- MoE

@@ -14,7 +14,7 @@ CSRC = os.path.join(PKG, "csrc")
 OBJ = os.path.join(ROOT, "_build", "mxfp8")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libmxfp8_gb300.so")
-SOURCES = ["api.cu", "quant.cu", "gemm.cu", "noalloc.cu", "moe.cu"]
+SOURCES = ["api.cu", "quant.cu", "gemm.cu", "noalloc.cu", "moe.cu", "tactics.cu"]
 HEADERS = ["ptx.cuh", "quant_block.cuh", "internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr"]

@@ -158,6 +158,24 @@ static mxk::GemmProblem make_problem(const void* qa, const void* sfa, int64_t m,
     return p;
 }
 
+// Set by the autotuner while it times one candidate on this thread.
+thread_local const mxk::GemmSchedule* t_override = nullptr;
+
+// Schedule of a call: the autotuner's candidate, else the testing hooks if
+// set, else the tactic table, else the built-in heuristic.
+static mxk::GemmSchedule select_schedule(const mxk::GemmProblem& p, int sms, int kind) {
+    if (t_override) return *t_override;
+    if (g_force_tt != 0 || g_force_split != 0 || g_force_fuse != -1)
+        return mxk::choose_schedule(p, sms, g_force_tt, g_force_split, g_force_fuse);
+    int dev = 0;
+    mxk::GemmSchedule s;
+    if (cudaGetDevice(&dev) == cudaSuccess && mxk::tactic_lookup(dev, kind, p.m, p.n, p.k, p.experts, &s)) {
+        if (s.fuse_quant && p.x == nullptr) s.fuse_quant = false;
+        return s;
+    }
+    return mxk::choose_schedule(p, sms, 0, 0, -1);
+}
+
 static mxfp8_status launch_status(cudaError_t e, bool enc_fail) {
     if (enc_fail) return MXFP8_ERR_INVALID_ARG;
     return e == cudaSuccess ? MXFP8_OK : cuda_fail(e);
@@ -176,7 +194,7 @@ mxfp8_status mxfp8_gemm(const void* qa, const void* sfa, int64_t m, const mxfp8_
     int sms = 0;
     if ((st = device_sms(&sms)) != MXFP8_OK) return st;
     const mxk::GemmProblem p = make_problem(qa, sfa, m, w, bias, y, nullptr, nullptr);
-    const mxk::GemmSchedule sch = mxk::choose_schedule(p, sms, g_force_tt, g_force_split, g_force_fuse);
+    const mxk::GemmSchedule sch = select_schedule(p, sms, mxk::kTacticGemm);
     bool enc_fail = false;
     cudaError_t e = mxk::launch_gemm(p, sch, sms, static_cast<cudaStream_t>(stream), &enc_fail);
     return launch_status(e, enc_fail);
@@ -202,7 +220,7 @@ static mxfp8_status linear_common(const void* x, int64_t m, const int32_t* offse
     // Small M: the GEMM quantizes its own K slices of x (no separate launch,
     // the workspace stays unused).  Otherwise quantize into the workspace.
     const mxk::GemmProblem p = make_problem(qa, sfa, m, w, bias, y, offsets, offsets ? nullptr : x);
-    const mxk::GemmSchedule sch = mxk::choose_schedule(p, sms, g_force_tt, g_force_split, g_force_fuse);
+    const mxk::GemmSchedule sch = select_schedule(p, sms, offsets ? mxk::kTacticGrouped : mxk::kTacticLinear);
     if (!sch.fuse_quant) {
         cudaError_t e = mxk::launch_quant_act(x, m, w->k, qa, sfa, sms, s);
         if (e != cudaSuccess) return cuda_fail(e);
@@ -225,6 +243,123 @@ mxfp8_status mxfp8_grouped_linear(const void* x_sorted, int64_t rows, const int3
     if ((reinterpret_cast<uintptr_t>(expert_offsets) & 3u)) return MXFP8_ERR_MISALIGNED;
     return linear_common(x_sorted, rows, expert_offsets, w, bias, y, workspace, workspace_bytes, stream);
 }
+
+// --------------------------------------------------------------- tactics
+namespace {
+// {tokens_per_tile (192 = two weight tiles), split_k (-1 = persistent),
+//  fuse_quant, pipes}
+void encode_tactic(const mxk::GemmSchedule& s, int32_t* t4) {
+    t4[0] = s.dual ? 192 : s.tokens_per_tile;
+    t4[1] = s.persistent ? -1 : s.split_k;
+    t4[2] = s.fuse_quant ? 1 : 0;
+    t4[3] = s.pipes;
+}
+bool decode_tactic(const int32_t* t4, int kind, int64_t k, mxk::GemmSchedule* s) {
+    s->dual = t4[0] == 192;
+    s->tokens_per_tile = s->dual ? 192 : t4[0];
+    s->persistent = t4[1] == -1;
+    s->split_k = s->persistent ? 1 : t4[1];
+    s->fuse_quant = t4[2] != 0;
+    s->pipes = t4[3];
+    if (s->dual) return t4[1] == -1 && !s->fuse_quant && mxk::schedule_valid(*s, kind, k);
+    return mxk::schedule_valid(*s, kind, k);
+}
+bool kind_ok(int kind) { return kind >= mxk::kTacticLinear && kind <= mxk::kTacticGated; }
+}  // namespace
+
+static mxfp8_status autotune_common(const void* x, int64_t m, const int32_t* offsets, const mxfp8_weight* w,
+                                    const void* bias, void* y, void* workspace, size_t workspace_bytes, int iters,
+                                    void* stream, int32_t* chosen) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(s, &cap);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (cap != cudaStreamCaptureStatusNone) return MXFP8_ERR_INVALID_ARG;  // tuning synchronizes
+    // One ordinary call validates every argument (and warms the caches).
+    mxfp8_status st = linear_common(x, m, offsets, w, bias, y, workspace, workspace_bytes, stream);
+    if (st != MXFP8_OK || m == 0) return st;
+    if (iters <= 0) iters = 20;
+    const int kind = offsets ? mxk::kTacticGrouped : mxk::kTacticLinear;
+    const std::vector<mxk::GemmSchedule> cands = mxk::candidate_schedules(kind, m, w->k);
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    if ((e = cudaEventCreate(&e0)) != cudaSuccess || (e = cudaEventCreate(&e1)) != cudaSuccess) {
+        if (e0) cudaEventDestroy(e0);
+        return cuda_fail(e);
+    }
+    int best = -1;
+    float best_ms = 0.0f;
+    for (size_t i = 0; i < cands.size() && e == cudaSuccess; ++i) {
+        t_override = &cands[i];
+        bool ok = true;
+        for (int r = 0; r < 2 && ok; ++r)
+            ok = linear_common(x, m, offsets, w, bias, y, workspace, workspace_bytes, stream) == MXFP8_OK;
+        if (!ok) {  // this shape rejects the candidate at launch (resources): skip it
+            (void)cudaGetLastError();
+            continue;
+        }
+        e = cudaEventRecord(e0, s);
+        for (int r = 0; r < iters && ok && e == cudaSuccess; ++r)
+            ok = linear_common(x, m, offsets, w, bias, y, workspace, workspace_bytes, stream) == MXFP8_OK;
+        if (e == cudaSuccess) e = cudaEventRecord(e1, s);
+        if (e == cudaSuccess) e = cudaEventSynchronize(e1);
+        float ms = 0.0f;
+        if (e == cudaSuccess && ok && cudaEventElapsedTime(&ms, e0, e1) == cudaSuccess && (best < 0 || ms < best_ms)) {
+            best = static_cast<int>(i);
+            best_ms = ms;
+        }
+    }
+    t_override = nullptr;
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (best < 0) return MXFP8_ERR_INVALID_ARG;
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_fail(e);
+    mxk::tactic_store(dev, kind, m, w->n, w->k, w->num_experts, cands[best]);
+    if (chosen) encode_tactic(cands[best], chosen);
+    return MXFP8_OK;
+}
+
+mxfp8_status mxfp8_autotune_linear(const void* x, int64_t m, const mxfp8_weight* w, const void* bias, void* y,
+                                   void* workspace, size_t workspace_bytes, int iters, void* stream,
+                                   int32_t* chosen) {
+    if (w && w->num_experts != 1) return MXFP8_ERR_INVALID_ARG;
+    return autotune_common(x, m, nullptr, w, bias, y, workspace, workspace_bytes, iters, stream, chosen);
+}
+
+mxfp8_status mxfp8_autotune_grouped_linear(const void* x_sorted, int64_t rows, const int32_t* expert_offsets,
+                                           const mxfp8_weight* w, const void* bias, void* y, void* workspace,
+                                           size_t workspace_bytes, int iters, void* stream, int32_t* chosen) {
+    if (!expert_offsets) return MXFP8_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(expert_offsets) & 3u)) return MXFP8_ERR_MISALIGNED;
+    return autotune_common(x_sorted, rows, expert_offsets, w, bias, y, workspace, workspace_bytes, iters, stream,
+                           chosen);
+}
+
+mxfp8_status mxfp8_tactic_get(int kind, int64_t m, int64_t n, int64_t k, int64_t experts, int32_t* tactic) {
+    if (!kind_ok(kind) || m < 1 || n < 1 || k < 1 || experts < 1 || !tactic) return MXFP8_ERR_INVALID_ARG;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;  // table operations need no device
+    mxk::GemmSchedule s;
+    if (!mxk::tactic_lookup(dev, kind, m, n, k, experts, &s)) return MXFP8_ERR_INVALID_ARG;
+    encode_tactic(s, tactic);
+    return MXFP8_OK;
+}
+
+mxfp8_status mxfp8_tactic_set(int kind, int64_t m, int64_t n, int64_t k, int64_t experts, const int32_t* tactic) {
+    if (!kind_ok(kind) || m < 1 || n < 1 || k < 1 || k % 256 != 0 || experts < 1 || !tactic)
+        return MXFP8_ERR_INVALID_ARG;
+    mxk::GemmSchedule s;
+    if (!decode_tactic(tactic, kind, k, &s)) return MXFP8_ERR_INVALID_ARG;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;  // table operations need no device
+    mxk::tactic_store(dev, kind, m, n, k, experts, s);
+    return MXFP8_OK;
+}
+
+void mxfp8_tactic_clear(void) { mxk::tactic_clear(); }
+
+int64_t mxfp8_tactic_count(void) { return mxk::tactic_count(); }
 
 // ------------------------------------------------------------------- MoE
 size_t mxfp8_moe_route_workspace_bytes(int64_t tokens, int64_t experts, int64_t topk) {
@@ -304,7 +439,7 @@ mxfp8_status mxfp8_moe_gate_up_swiglu(const void* x, const int32_t* sorted_token
     if (e != cudaSuccess) return cuda_fail(e);
     mxk::GemmProblem p = make_problem(qa, sfa, rows, w13, nullptr, h, expert_offsets, nullptr);
     p.gated = true;
-    const mxk::GemmSchedule sch = mxk::choose_schedule(p, sms, g_force_tt, 0, -1);
+    const mxk::GemmSchedule sch = select_schedule(p, sms, mxk::kTacticGated);
     bool enc_fail = false;
     e = mxk::launch_gemm(p, sch, sms, s, &enc_fail);
     return launch_status(e, enc_fail);

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <vector>
+
 namespace mxk {
 
 // Activation quantizer, 8x4 scale layout.  It lets a dependent grid launched
@@ -53,6 +55,19 @@ struct GemmSchedule {
     int pipes;                 // MMA pipelines per CTA (1, 2 or 4; >1 only for <= 64 tokens)
     bool dual;                 // dense, persistent, two weight tiles x 192 tokens per CTA tile
 };
+
+// Tactic table (tactics.cu).  Kinds of calls with separate entries.
+constexpr int kTacticLinear = 0;   // mxfp8_linear: x available, quantization may be fused
+constexpr int kTacticGemm = 1;     // mxfp8_gemm: pre-quantized activations
+constexpr int kTacticGrouped = 2;  // mxfp8_grouped_linear
+constexpr int kTacticGated = 3;    // MoE GEMM1 with the SwiGLU epilogue
+int64_t m_bucket(int64_t m);       // smallest power of two >= m
+bool schedule_valid(const GemmSchedule& s, int kind, int64_t k);
+bool tactic_lookup(int dev, int kind, int64_t m, int64_t n, int64_t k, int64_t experts, GemmSchedule* out);
+void tactic_store(int dev, int kind, int64_t m, int64_t n, int64_t k, int64_t experts, const GemmSchedule& s);
+void tactic_clear();
+int64_t tactic_count();
+std::vector<GemmSchedule> candidate_schedules(int kind, int64_t m, int64_t k);
 
 // Testing hook: pipelines per CTA for later launches (0 = automatic).
 void set_pipes(int pipes);

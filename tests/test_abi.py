@@ -40,7 +40,8 @@ def test_header_declares_the_boundary():
     for required in ("mxfp8_prepare_weight", "mxfp8_quantize_act", "mxfp8_linear",
                      "mxfp8_gemm", "mxfp8_grouped_linear", "mxfp8_act_scale_bytes",
                      "mxfp8_moe_route", "mxfp8_prepare_gate_up_weight", "mxfp8_moe_gate_up_swiglu",
-                     "mxfp8_moe_finalize", "mxfp8_moe_expert_mlp"):
+                     "mxfp8_moe_finalize", "mxfp8_moe_expert_mlp", "mxfp8_autotune_linear",
+                     "mxfp8_tactic_set", "mxfp8_tactic_get"):
         assert required in names
 
 
@@ -135,3 +136,38 @@ def test_moe_size_helpers_and_argument_checks(mx):
     assert lib.mxfp8_moe_route(None, 0, 8, 2, 0, None, None, None, None, None, None, 0, None) == mx.OK
     assert lib.mxfp8_moe_finalize(None, None, None, 4, 2, 12, None, None) == 1  # hidden % 8: invalid argument
     assert lib.mxfp8_moe_finalize(None, None, None, 0, 2, 16, None, None) == mx.OK
+
+
+def test_tactic_table_host_operations(mx):
+    mx.tactic_clear()
+    assert mx.tactic_count() == 0
+    assert mx.tactic_get(mx.KIND_LINEAR, 16, 5120, 2048) is None
+    mx.tactic_set(mx.KIND_LINEAR, 16, 5120, 2048, 1, (16, 4, 1, 2))
+    assert mx.tactic_get(mx.KIND_LINEAR, 16, 5120, 2048) == (16, 4, 1, 2)
+    # M buckets are powers of two: 9..16 share one entry, 17 does not
+    assert mx.tactic_get(mx.KIND_LINEAR, 9, 5120, 2048) == (16, 4, 1, 2)
+    assert mx.tactic_get(mx.KIND_LINEAR, 17, 5120, 2048) is None
+    # kinds are separate
+    assert mx.tactic_get(mx.KIND_GEMM, 16, 5120, 2048) is None
+    mx.tactic_set(mx.KIND_GEMM, 8192, 8192, 8192, 1, (192, -1, 0, 2))
+    mx.tactic_set(mx.KIND_GROUPED, 2048, 1536, 2048, 128, (32, -1, 0, 2))
+    assert mx.tactic_count() == 3
+    bad = [
+        (mx.KIND_LINEAR, (48, -1, 0, 1)),    # no such tile
+        (mx.KIND_LINEAR, (16, 9, 0, 1)),     # cluster of 9
+        (mx.KIND_LINEAR, (128, -1, 0, 2)),   # two pipes need tiles <= 64
+        (mx.KIND_LINEAR, (32, 1, 0, 4)),     # four pipes only with 16-token tiles
+        (mx.KIND_GEMM, (16, 4, 1, 2)),       # fused quantization needs x
+        (mx.KIND_GROUPED, (32, 2, 0, 2)),    # grouped tiles are persistent
+        (mx.KIND_GROUPED, (192, -1, 0, 2)),  # two weight tiles: dense only
+        (mx.KIND_GATED, (256, -1, 0, 1)),    # the gated exchange holds <= 128 tokens
+        (mx.KIND_LINEAR, (256, 2, 0, 1)),    # one-tile schedules take <= 128 tokens
+    ]
+    for kind, t in bad:
+        with pytest.raises(mx.Mxfp8Error):
+            mx.tactic_set(kind, 16, 512, 2048, 1, t)
+    with pytest.raises(mx.Mxfp8Error):
+        mx.tactic_set(mx.KIND_LINEAR, 16, 512, 2048, 1, (16, 16, 0, 1))  # split beyond K/128 = 16? (cluster <= 8)
+    assert mx.tactic_count() == 3
+    mx.tactic_clear()
+    assert mx.tactic_count() == 0
