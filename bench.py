@@ -54,7 +54,8 @@ def parse_args():
     ap.add_argument("--no-configs", action="store_true", help="skip the per-workload table")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle CPU-baseline budget")
     ap.add_argument("--workload", default="decode16",
-                    choices=["decode16", "decode1", "tiny", "mid", "mid130", "prefill", "grouped", "moe"],
+                    choices=["decode16", "decode1", "tiny", "mid", "mid130", "prefill", "grouped", "moe",
+                             "prefill128x4"],
                     help="decode16 = the contract line; any other runs only that workload "
                          "for --steps calls (profiling aid) and prints its table entry")
     return ap.parse_args()
@@ -265,13 +266,20 @@ class DenseSetup:
         return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
 
 
-def measure_config(mx, name, d, peaks, calls=2000):
+def measure_config(mx, name, d, peaks, calls=2000, tune=False):
+    """Time one dense workload.  tune: run the autotuner on the first copy
+    first (the stored tactic then serves every call of this class), report
+    the chosen tactic, and clear the table afterwards."""
     import torch
     wb = weight_bytes(d.n, d.k)
     nbytes = dense_bytes(d.m, d.n, d.k, d.bias is not None)
     gemm_bytes = (d.m * d.k + mx.act_scale_bytes(d.m, d.k) + wb + (2 * d.n if d.bias is not None else 0)
                   + 2 * d.m * d.n)
     setup = DenseSetup(mx, d, copies_for(nbytes))
+    tactic = None
+    if tune:
+        mx.tactic_clear()
+        tactic = mx.autotune_linear(setup.xs[0], setup.pws[0], setup.bias, iters=50)
     warm = max(3, calls // 10)
     ms = time_steps(setup.linear, calls, warmup=warm) / calls
     ms_g = time_steps(setup.gemm, calls, warmup=warm) / calls
@@ -282,9 +290,53 @@ def measure_config(mx, name, d, peaks, calls=2000):
            "tflops": flops / (ms * 1e-3) / 1e12, "gemm_tflops": flops / (ms_g * 1e-3) / 1e12,
            "weight_gbs": wb / (ms * 1e-3) / 1e9, "alg_gbs": nbytes / (ms * 1e-3) / 1e9,
            "flops": flops, "alg_bytes": nbytes, "gemm_alg_bytes": gemm_bytes}
+    if tune:
+        out["tactic"] = {"tokens_per_tile": tactic[0], "split_k": tactic[1], "fuse_quant": tactic[2],
+                         "pipes": tactic[3], "note": "autotuned linear; the gemm_us column keeps the heuristic"}
+        mx.tactic_clear()
     out.update(roofline_entry(flops, nbytes, ms, peaks))
     out["gemm_only"] = roofline_entry(flops, gemm_bytes, ms_g, peaks)
     del setup
+    torch.cuda.empty_cache()
+    return out
+
+
+def measure_128x4(mx, d, peaks, calls=40):
+    """The high-M variant with 128x4 activation scales (persistent 256-token
+    tiles), timed like measure_config: the whole layer and the GEMM alone."""
+    import ctypes
+    import torch
+    nbytes = dense_bytes(d.m, d.n, d.k, d.bias is not None)
+    setup = DenseSetup(mx, d, copies_for(nbytes))
+    lib = mx.library()
+    ws = torch.empty(lib.mxfp8_linear_128x4_workspace_bytes(d.m, d.k), dtype=torch.uint8, device="cuda")
+    q128 = [mx.quantize_act_128x4(x) for x in setup.xs]
+    bias = None if setup.bias is None else ctypes.c_void_p(setup.bias.data_ptr())
+
+    def lin(i):
+        r = i % setup.R
+        st = lib.mxfp8_linear_128x4(ctypes.c_void_p(setup.xs[r].data_ptr()), d.m, ctypes.byref(setup.pws[r].c), bias,
+                                    ctypes.c_void_p(setup.y.data_ptr()), ctypes.c_void_p(ws.data_ptr()), ws.numel(),
+                                    setup._stream())
+        assert st == 0, st
+
+    def gem(i):
+        r = i % setup.R
+        q, sf = q128[r]
+        st = lib.mxfp8_gemm_128x4(ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(sf.data_ptr()), d.m,
+                                  ctypes.byref(setup.pws[r].c), bias, ctypes.c_void_p(setup.y.data_ptr()),
+                                  setup._stream())
+        assert st == 0, st
+
+    warm = max(3, calls // 10)
+    ms = time_steps(lin, calls, warmup=warm) / calls
+    ms_g = time_steps(gem, calls, warmup=warm) / calls
+    flops = 2.0 * d.m * d.n * d.k
+    out = {"m": d.m, "n": d.n, "k": d.k, "us_per_call": ms * 1e3, "gemm_us": ms_g * 1e3,
+           "tflops": flops / (ms * 1e-3) / 1e12, "gemm_tflops": flops / (ms_g * 1e-3) / 1e12,
+           "note": "128x4 activation scales, persistent 256-token tiles (vs the 8x4 path's 192-token dual tiles)"}
+    out.update(roofline_entry(flops, nbytes, ms, peaks))
+    del setup, q128, ws
     torch.cuda.empty_cache()
     return out
 
@@ -468,6 +520,8 @@ def main():
             res = measure_grouped(mx, peaks, args.steps)
         elif args.workload == "moe":
             res = measure_moe(mx, peaks, args.steps)
+        elif args.workload == "prefill128x4":
+            res = measure_128x4(mx, workloads.prefill(), peaks, args.steps)
         else:
             res = measure_config(mx, args.workload, builders[args.workload](), peaks, args.steps)
         res["workload"] = args.workload
@@ -535,8 +589,12 @@ def main():
         cfgs["mid_m128_n2048_k4096"] = measure_config(mx, "mid", workloads.mid(), peaks, 2000)
         cfgs["mid_m128_n130_k4096_bias"] = measure_config(mx, "mid130", workloads.mid(n=130, bias=True), peaks, 2000)
         cfgs["prefill_m8192_n8192_k8192"] = measure_config(mx, "prefill", workloads.prefill(), peaks, 40)
+        cfgs["prefill_m8192_n8192_k8192_128x4"] = measure_128x4(mx, workloads.prefill(), peaks, 40)
         cfgs["grouped_t256_e128_top8_n1536_k2048"] = measure_grouped(mx, peaks, 200)
         cfgs["moe_mlp_t256_e128_top8_h2048_i768"] = measure_moe(mx, peaks, 200)
+        cfgs["decode_m16_n5120_k2048_autotuned"] = measure_config(mx, "d16", workloads.decode(m=16), peaks, 4000,
+                                                                  tune=True)
+        cfgs["mid_m128_n2048_k4096_autotuned"] = measure_config(mx, "mid", workloads.mid(), peaks, 2000, tune=True)
         for v in cfgs.values():
             v["peaks"] = peak_src
         out["configs"] = cfgs

@@ -95,6 +95,11 @@ def library():
         "mxfp8_set_wait_limit_ns": (None, [ctypes.c_uint64]),
         "mxfp8_set_pipes": (None, [ctypes.c_int]),
         "mxfp8_static_scratch_last_cuda_error": (ctypes.c_int, []),
+        "mxfp8_act_scale_bytes_128x4": (sz, [i64, i64]),
+        "mxfp8_linear_128x4_workspace_bytes": (sz, [i64, i64]),
+        "mxfp8_quantize_act_128x4": (ctypes.c_int, [vp, i64, i64, vp, vp, vp]),
+        "mxfp8_gemm_128x4": (ctypes.c_int, [vp, vp, i64, W, vp, vp, vp]),
+        "mxfp8_linear_128x4": (ctypes.c_int, [vp, i64, W, vp, vp, vp, sz, vp]),
         "mxfp8_autotune_linear": (ctypes.c_int, [vp, i64, W, vp, vp, vp, sz, ctypes.c_int, vp, vp]),
         "mxfp8_autotune_grouped_linear": (ctypes.c_int, [vp, i64, vp, W, vp, vp, vp, sz, ctypes.c_int, vp, vp]),
         "mxfp8_tactic_get": (ctypes.c_int, [ctypes.c_int, i64, i64, i64, i64, vp]),
@@ -267,6 +272,44 @@ def grouped_linear(x_sorted: torch.Tensor, offsets: torch.Tensor, pw: PreparedWe
                                           _ptr(workspace), workspace.numel(), _stream(x_sorted)),
            "mxfp8_grouped_linear")
     return y
+
+
+# -------------------------------------------------- 128x4 activation scales
+def quantize_act_128x4(x: torch.Tensor):
+    """BF16 [m, k] -> (E4M3 bytes [m, k], scales in the 128x4 layout
+    [ceil128(m) * k/32])."""
+    _need(x.is_cuda and x.dtype == torch.bfloat16, "x must be a bfloat16 CUDA tensor")
+    x2 = x.reshape(-1, x.shape[-1]).contiguous()
+    m, k = x2.shape
+    nsf = library().mxfp8_act_scale_bytes_128x4(m, k)
+    q = torch.empty((m, k), dtype=torch.uint8, device=x.device)
+    sf = torch.empty((max(nsf, 1),), dtype=torch.uint8, device=x.device)
+    _check(library().mxfp8_quantize_act_128x4(_ptr(x2), m, k, _ptr(q), _ptr(sf), _stream(x)),
+           "mxfp8_quantize_act_128x4")
+    return q, sf[:nsf]
+
+
+def gemm_128x4(qa: torch.Tensor, sfa: torch.Tensor, pw: PreparedWeight, bias=None) -> torch.Tensor:
+    m = qa.shape[0]
+    y = torch.empty((m, pw.n), dtype=torch.bfloat16, device=qa.device)
+    _check(library().mxfp8_gemm_128x4(_ptr(qa.contiguous()), _ptr(sfa.contiguous()), m, ctypes.byref(pw.c),
+                                      _ptr(bias), _ptr(y), _stream(qa)), "mxfp8_gemm_128x4")
+    return y
+
+
+def linear_128x4(x: torch.Tensor, pw: PreparedWeight, bias=None, workspace=None) -> torch.Tensor:
+    """The layer with 128x4 activation scales (the high-M variant)."""
+    _need(x.is_cuda and x.dtype == torch.bfloat16, "x must be bf16 CUDA")
+    lead = x.shape[:-1]
+    x2 = x.reshape(-1, x.shape[-1]).contiguous()
+    m = x2.shape[0]
+    need = library().mxfp8_linear_128x4_workspace_bytes(m, pw.k)
+    if workspace is None:
+        workspace = torch.empty((max(need, 16),), dtype=torch.uint8, device=x.device)
+    y = torch.empty((m, pw.n), dtype=torch.bfloat16, device=x.device)
+    _check(library().mxfp8_linear_128x4(_ptr(x2), m, ctypes.byref(pw.c), _ptr(bias), _ptr(y), _ptr(workspace),
+                                        workspace.numel(), _stream(x)), "mxfp8_linear_128x4")
+    return y.reshape(*lead, pw.n)
 
 
 # ----------------------------------------------------------------- tactics

@@ -155,6 +155,7 @@ static mxk::GemmProblem make_problem(const void* qa, const void* sfa, int64_t m,
     p.offsets = offsets;
     p.x = x;
     p.gated = false;
+    p.sf128 = false;
     return p;
 }
 
@@ -242,6 +243,74 @@ mxfp8_status mxfp8_grouped_linear(const void* x_sorted, int64_t rows, const int3
     if (!expert_offsets) return MXFP8_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(expert_offsets) & 3u)) return MXFP8_ERR_MISALIGNED;
     return linear_common(x_sorted, rows, expert_offsets, w, bias, y, workspace, workspace_bytes, stream);
+}
+
+// -------------------------------------------------- 128x4 activation scales
+size_t mxfp8_act_scale_bytes_128x4(int64_t m, int64_t k) {
+    if (m < 0 || k <= 0 || k % 128 != 0) return 0;
+    return static_cast<size_t>(ceil_to(m, 128) * (k / 32));
+}
+
+size_t mxfp8_linear_128x4_workspace_bytes(int64_t m, int64_t k) {
+    if (m < 0 || k <= 0 || k % 128 != 0) return 0;
+    return static_cast<size_t>(ceil_to(m * k, 256)) + mxfp8_act_scale_bytes_128x4(m, k);
+}
+
+mxfp8_status mxfp8_quantize_act_128x4(const void* x, int64_t m, int64_t k, void* q, void* sf, void* stream) {
+    if (m < 0 || k < 1) return MXFP8_ERR_INVALID_ARG;
+    if (k % 256 != 0) return MXFP8_ERR_K_NOT_MULTIPLE_OF_256;
+    if (m > kMaxRows || k > kMaxK) return MXFP8_ERR_INVALID_ARG;
+    if (m == 0) return MXFP8_OK;
+    if (!x || !q || !sf) return MXFP8_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(q) || !aligned16(sf)) return MXFP8_ERR_MISALIGNED;
+    int sms = 0;
+    mxfp8_status st = device_sms(&sms);
+    if (st != MXFP8_OK) return st;
+    cudaError_t e = mxk::launch_quant_act(x, m, k, static_cast<uint8_t*>(q), static_cast<uint8_t*>(sf), sms,
+                                          static_cast<cudaStream_t>(stream), nullptr, true);
+    return e == cudaSuccess ? MXFP8_OK : cuda_fail(e);
+}
+
+mxfp8_status mxfp8_gemm_128x4(const void* qa, const void* sfa, int64_t m, const mxfp8_weight* w, const void* bias,
+                              void* y, void* stream) {
+    mxfp8_status st = check_weight(w);
+    if (st != MXFP8_OK) return st;
+    if (w->num_experts != 1 || m < 0 || m > kMaxRows) return MXFP8_ERR_INVALID_ARG;
+    if (m == 0) return MXFP8_OK;
+    if (!qa || !sfa || !y) return MXFP8_ERR_INVALID_ARG;
+    if (!aligned16(qa) || !aligned16(sfa)) return MXFP8_ERR_MISALIGNED;
+    if ((reinterpret_cast<uintptr_t>(y) & 1u) || (reinterpret_cast<uintptr_t>(bias) & 1u))
+        return MXFP8_ERR_MISALIGNED;
+    int sms = 0;
+    if ((st = device_sms(&sms)) != MXFP8_OK) return st;
+    mxk::GemmProblem p = make_problem(qa, sfa, m, w, bias, y, nullptr, nullptr);
+    p.sf128 = true;
+    // Persistent tiles on 128-token boundaries: 256 tokens, or 128 for small M.
+    mxk::GemmSchedule sch;
+    sch.tokens_per_tile = m > 128 ? 256 : 128;
+    sch.split_k = 1;
+    sch.persistent = true;
+    sch.fuse_quant = false;
+    sch.pipes = 1;
+    sch.dual = false;
+    bool enc_fail = false;
+    cudaError_t e = mxk::launch_gemm(p, sch, sms, static_cast<cudaStream_t>(stream), &enc_fail);
+    return launch_status(e, enc_fail);
+}
+
+mxfp8_status mxfp8_linear_128x4(const void* x, int64_t m, const mxfp8_weight* w, const void* bias, void* y,
+                                void* workspace, size_t workspace_bytes, void* stream) {
+    mxfp8_status st = check_weight(w);
+    if (st != MXFP8_OK) return st;
+    if (w->num_experts != 1 || m < 0 || m > kMaxRows) return MXFP8_ERR_INVALID_ARG;
+    if (m == 0) return MXFP8_OK;
+    if (!x || !workspace) return MXFP8_ERR_INVALID_ARG;
+    if (!aligned16(workspace)) return MXFP8_ERR_MISALIGNED;
+    if (workspace_bytes < mxfp8_linear_128x4_workspace_bytes(m, w->k)) return MXFP8_ERR_WORKSPACE_TOO_SMALL;
+    uint8_t* qa = static_cast<uint8_t*>(workspace);
+    uint8_t* sfa = qa + ceil_to(m * w->k, 256);
+    if ((st = mxfp8_quantize_act_128x4(x, m, w->k, qa, sfa, stream)) != MXFP8_OK) return st;
+    return mxfp8_gemm_128x4(qa, sfa, m, w, bias, y, stream);
 }
 
 // --------------------------------------------------------------- tactics

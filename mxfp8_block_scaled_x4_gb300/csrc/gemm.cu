@@ -88,6 +88,7 @@ struct GemmArgs {
     int box_rows, sf_groups;
     int stages, splits, persistent;
     int gated;               // grouped SwiGLU epilogue: y = silu(gate) * up, [m][n/2]
+    const uint8_t* asf128;   // activation scales in the 128x4 layout (dense tiles of 128/256), or null
     int num_tiles;           // dense (grouped counts tiles on the device)
     uint32_t tmem_cols;
     uint64_t wait_ns;        // limit of every pipeline wait
@@ -214,9 +215,14 @@ __device__ __forceinline__ void run_producer(const GemmArgs& p, const Ctx& c, in
     const int S = c.stages;
     auto stage_of = [&](int jq) { return q * S + jq % S; };
     const uint32_t a_bytes = c.fused ? 0u : static_cast<uint32_t>(TT * 128);
+    // 128x4 activation scales: one 512-byte tile per 128 tokens of the tile
+    // that exist (the buffer holds ceil128(M) rows).
+    auto sf_chunks = [&](const TileInfo& ti) {
+        return p.asf128 ? min(G::kSfChunks, (ti.count + 127) / 128) : 0;
+    };
     auto issue_w = [&](const TileInfo& ti, int kb, int s) {
         uint8_t* st = c.smem + s * G::kStageBytes;
-        mbar_arrive_expect_tx(&c.full[s], 16384u + 512u + a_bytes);
+        mbar_arrive_expect_tx(&c.full[s], 16384u + 512u + a_bytes + 512u * static_cast<uint32_t>(sf_chunks(ti)));
         tma_load_2d(st + G::kOffW, &p.map_w, kb * 128, ti.e * p.n_pad + ti.n_tile * 128, &c.full[s], pol_w);
         bulk_load(st + G::kOffWsf,
                   p.wsf + ((static_cast<size_t>(ti.e) * p.n_tiles + ti.n_tile) * p.kq + kb) * 512, 512,
@@ -225,6 +231,15 @@ __device__ __forceinline__ void run_producer(const GemmArgs& p, const Ctx& c, in
     auto issue_a = [&](const TileInfo& ti, int kb, int s) {
         uint8_t* st = c.smem + s * G::kStageBytes;
         tma_load_2d(st + G::kOffA, &p.map_a, kb * 128, ti.tok0, &c.full[s], pol_a);
+        if (p.asf128) {
+            // Already in the TMEM-copy order: straight into the staging slot.
+            const int nch = sf_chunks(ti);
+            for (int ch = 0; ch < nch; ++ch)
+                bulk_load(st + G::kOffAsfT + ch * 512,
+                          p.asf128 + (static_cast<size_t>((ti.tok0 >> 7) + ch) * p.kq + kb) * 512, 512, &c.full[s],
+                          pol_a);
+            return;
+        }
         mbar_arrive_expect_tx(&c.sfraw[s], static_cast<uint32_t>(p.sf_groups * 32));
         tma_load_2d(st + G::kOffAsfRaw, &p.map_asf, kb * 32, ti.tok0 >> 3, &c.sfraw[s], pol_a);
     };
@@ -263,7 +278,7 @@ __device__ __forceinline__ void run_producer(const GemmArgs& p, const Ctx& c, in
     const int issued = jq > pre ? jq : pre;
     for (int j = issued - 1; j >= 0 && j >= issued - S; --j) {
         (void)mbar_wait(&c.full[stage_of(j)], (j / S) & 1, kDrainNs);
-        if (!c.fused) (void)mbar_wait(&c.sfraw[stage_of(j)], (j / S) & 1, kDrainNs);
+        if (!c.fused && !p.asf128) (void)mbar_wait(&c.sfraw[stage_of(j)], (j / S) & 1, kDrainNs);
     }
 }
 
@@ -527,12 +542,12 @@ __global__ void __launch_bounds__(32 * num_warps(TT, PIPES),
         tma_prefetch_desc(&p.map_w);
         if (!fused) {
             tma_prefetch_desc(&p.map_a);
-            tma_prefetch_desc(&p.map_asf);
+            if (!p.asf128) tma_prefetch_desc(&p.map_asf);
         }
         for (int s = 0; s < ST; ++s) {
             // full: the producer's arrival (+ TMA bytes) and either one
             // arrival per fused-quantizer patch or the scale re-order warp's.
-            mbar_init(&c.full[s], fused ? 1 + TT / 8 : 2);
+            mbar_init(&c.full[s], fused ? 1 + TT / 8 : (p.asf128 ? 1 : 2));
             mbar_init(&c.empty[s], 1);
             mbar_init(&c.sfraw[s], 1);
         }
@@ -615,7 +630,7 @@ __global__ void __launch_bounds__(32 * num_warps(TT, PIPES),
         if (lane == 0) run_mma<TT, PIPES>(p, c, warp == 1 ? 0 : warp - (kReorderWarp + PIPES) + 1);
         __syncwarp();
     } else if (warp == kReorderWarp) {
-        if (!fused) run_reorder<TT, PIPES>(p, c, lane);
+        if (!fused && !p.asf128) run_reorder<TT, PIPES>(p, c, lane);
         __syncwarp();
     } else {
         const int ew = warp - 2;  // warps 2 .. 1+kEpi
@@ -1199,7 +1214,9 @@ cudaError_t launch_tt(const GemmProblem& pr, const GemmSchedule& sch, int num_sm
     bool ok = encode_2d_u8(&a.map_w, pr.wq, pr.k, pr.experts * pr.n_pad, pr.k, 128, 128, true);
     if (ok && !fused)
         ok = encode_2d_u8(&a.map_a, pr.qa, pr.k, pr.m, pr.k, 128, a.box_rows, true) &&
-             encode_2d_u8(&a.map_asf, pr.sfa, pr.k / 4, m8 / 8, pr.k / 4, 32, a.sf_groups, false);
+             (pr.sf128 || encode_2d_u8(&a.map_asf, pr.sfa, pr.k / 4, m8 / 8, pr.k / 4, 32, a.sf_groups, false));
+    // 128x4 scales serve tiles that start on a 128-token boundary only.
+    if (pr.sf128 && (fused || !sch.persistent || TT < 128 || pr.offsets != nullptr)) return cudaErrorInvalidValue;
     if (!ok) {
         *encode_failed = true;
         return cudaErrorInvalidValue;
@@ -1231,6 +1248,7 @@ cudaError_t launch_tt(const GemmProblem& pr, const GemmSchedule& sch, int num_sm
     a.splits = splits;
     a.persistent = sch.persistent ? 1 : 0;
     a.gated = pr.gated ? 1 : 0;
+    a.asf128 = pr.sf128 ? pr.sfa : nullptr;
     a.stages = lp.stages;
     a.tmem_cols = lp.tmem_cols;
     a.wait_ns = g_wait_limit_ns ? g_wait_limit_ns : kWaitNs;
@@ -1291,6 +1309,7 @@ cudaError_t launch_tt(const GemmProblem& pr, const GemmSchedule& sch, int num_sm
 template <int TT>
 cudaError_t launch_dual(const GemmProblem& pr, int num_sms, cudaStream_t s, bool* encode_failed) {
     using G = DualGeometry<TT>;
+    if (pr.sf128) return cudaErrorInvalidValue;  // 192-token tiles straddle 128x4 scale tiles
     GemmArgs a;
     memset(&a, 0, sizeof(a));
     const int64_t m8 = (pr.m + 7) / 8 * 8;

@@ -13,7 +13,8 @@ namespace mxk {
 // with programmatic stream serialization start its prologue early.  With
 // src_rows, output row r quantizes input row src_rows[r].
 cudaError_t launch_quant_act(const void* x, int64_t m, int64_t k, uint8_t* q, uint8_t* sf,
-                             int num_sms, cudaStream_t s, const int32_t* src_rows = nullptr);
+                             int num_sms, cudaStream_t s, const int32_t* src_rows = nullptr,
+                             bool layout_128x4 = false);
 
 // Weight preparation: quantize + pad N + prepared layout.  src_is_bf16
 // selects the element type of src ([experts][n][k]); inter > 0 applies the
@@ -45,6 +46,7 @@ struct GemmProblem {
     const int32_t* offsets;    // grouped: device [experts + 1]; dense: null
     const void* x;             // bf16 [m][k] activations when the GEMM may quantize them itself
     bool gated;                // grouped only: SwiGLU epilogue, y = silu(gate) * up, bf16 [m][n/2]
+    bool sf128;                // sfa uses the 128x4 layout (dense, persistent tiles of 128/256 tokens)
 };
 
 struct GemmSchedule {

@@ -119,6 +119,7 @@ extern "C" mxfp8_status mxfp8_linear_static_scratch(const void* x, int64_t m, co
     p.offsets = nullptr;
     p.x = nullptr;  // the GEMM reads the quantized activations from the array
     p.gated = false;
+    p.sf128 = false;
     const mxk::GemmSchedule sch = mxk::choose_schedule(p, sms, 0, 0, 0);
     bool enc_fail = false;
     e = mxk::launch_gemm(p, sch, sms, s, &enc_fail);

@@ -50,12 +50,15 @@ __device__ __forceinline__ void st_v2(void* p, uint2 v) {
 // (row%8)*4 + block%4 = lane -- go out as one coalesced 32-byte store.  Rows in
 // [m, m8) quantize zeros and write only their (zero) scales.
 // With `src_rows`, output row r reads input row src_rows[r] (a gather, e.g.
-// tokens into expert-sorted order).
+// tokens into expert-sorted order).  With `layout128`, the scales go to the
+// 128x4 layout of the prepared weights instead (tile (row/128, K block) of
+// 512 bytes, byte (row%32)*16 + ((row%128)/32)*4 + block%4; rows up to
+// m_pad = ceil128(m)), one byte per lane.
 __global__ void __launch_bounds__(kThreads) quant_act_kernel(const __nv_bfloat16* __restrict__ x,
                                                              int64_t m, int64_t m8, int64_t k,
                                                              const int32_t* __restrict__ src_rows,
                                                              uint8_t* __restrict__ q,
-                                                             uint8_t* __restrict__ sf) {
+                                                             uint8_t* __restrict__ sf, int layout128) {
     // Dependent kernels (the GEMM) may start their prologue now; they wait
     // for this grid's completion before reading what it writes.  This grid
     // itself may start before the kernel that produced x has finished: every
@@ -98,7 +101,14 @@ __global__ void __launch_bounds__(kThreads) quant_act_kernel(const __nv_bfloat16
                 dst[0] = make_uint4(qq[0], qq[1], qq[2], qq[3]);
                 dst[1] = make_uint4(qq[4], qq[5], qq[6], qq[7]);
             }
-            sf[t * 32 + lane] = static_cast<uint8_t>(s);  // tile (g, quad) = t
+            if (!layout128) {
+                sf[t * 32 + lane] = static_cast<uint8_t>(s);  // 8x4 tile (g, quad) = t
+            } else {
+                const int64_t g = t / quads;
+                const int64_t r = row[u];
+                sf[((r >> 7) * quads + (t - g * quads)) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 + b4] =
+                    static_cast<uint8_t>(s);
+            }
         }
     }
 }
@@ -171,8 +181,10 @@ int grid_for(int64_t warps_of_work, int num_sms, int per_warp) {
 }  // namespace
 
 cudaError_t launch_quant_act(const void* x, int64_t m, int64_t k, uint8_t* q, uint8_t* sf,
-                             int num_sms, cudaStream_t s, const int32_t* src_rows) {
-    const int64_t m8 = (m + 7) / 8 * 8;
+                             int num_sms, cudaStream_t s, const int32_t* src_rows, bool layout_128x4) {
+    // Rows past m quantize zeros and write zero scales: up to ceil8(m) for
+    // the 8x4 layout, ceil128(m) for the 128x4 one.
+    const int64_t m8 = layout_128x4 ? (m + 127) / 128 * 128 : (m + 7) / 8 * 8;
     const int64_t work = (m8 / 8) * (k / 128);
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));
@@ -185,7 +197,7 @@ cudaError_t launch_quant_act(const void* x, int64_t m, int64_t k, uint8_t* q, ui
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, quant_act_kernel, static_cast<const __nv_bfloat16*>(x), m, m8, k, src_rows, q,
-                              sf);
+                              sf, layout_128x4 ? 1 : 0);
 }
 
 cudaError_t launch_prepare_weight(const void* src, bool src_is_bf16, int64_t experts, int64_t n,

@@ -146,6 +146,14 @@ def quantize_act(x):
     return q, act_scale_8x4(sf, x.shape[0], x.shape[1])
 
 
+def quantize_act_128x4(x):
+    """BF16 activations [m, k] -> (E4M3 bytes [m, k], scales in the 128x4
+    tiling of the prepared weights, rows padded with 0x00 to ceil128(m))."""
+    q, sf_lin = quantize_rows(x, RULE_OCP)
+    _, sf_t = weight_layout(q, sf_lin)
+    return q, sf_t
+
+
 def offset_w128x4(n: int, b: int, kb: int) -> int:
     return _load().oracle_offset_w128x4(n, b, kb)
 
