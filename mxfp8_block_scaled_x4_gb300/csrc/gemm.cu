@@ -87,7 +87,6 @@ struct GemmArgs {
     int experts, n_tiles;
     int box_rows, sf_groups;
     int stages, splits, persistent;
-    int gated;               // grouped SwiGLU epilogue: y = silu(gate) * up, [m][n/2]
     const uint8_t* asf128;   // activation scales in the 128x4 layout (dense tiles of 128/256), or null
     int num_tiles;           // dense (grouped counts tiles on the device)
     uint32_t tmem_cols;
@@ -105,6 +104,14 @@ struct Geometry {
     static constexpr int kStageBytes = ((kOffAsfT + 512 * kSfChunks) + 1023) / 1024 * 1024;
     static constexpr int kSfSlotCols = 4 + 4 * kSfChunks;         // TMEM columns per stage
 };
+
+// Kernel modes, compile-time so that each variant carries only its own code:
+//   kModePlain  the layer (8x4 activation scales)
+//   kModeGated  grouped GEMM1 with the SwiGLU epilogue (MoE)
+//   kModeSf128  dense tiles of 128/256 tokens with 128x4 activation scales
+constexpr int kModePlain = 0;
+constexpr int kModeGated = 1;
+constexpr int kModeSf128 = 2;
 
 // Tokens whose split-K sum one rank owns: a multiple of 4 so partials move as
 // 16-byte vectors (some ranks may own none).
@@ -204,7 +211,7 @@ __device__ __forceinline__ int pipe_jobs(int q, int nk) {
     return q < nk ? (nk - q + PIPES - 1) / PIPES : 0;
 }
 
-template <int TT, int PIPES>
+template <int TT, int PIPES, int MODE>
 __device__ __forceinline__ void run_producer(const GemmArgs& p, const Ctx& c, int q) {
     using G = Geometry<TT>;
     const uint64_t pol_w = policy_evict_normal();
@@ -218,7 +225,7 @@ __device__ __forceinline__ void run_producer(const GemmArgs& p, const Ctx& c, in
     // 128x4 activation scales: one 512-byte tile per 128 tokens of the tile
     // that exist (the buffer holds ceil128(M) rows).
     auto sf_chunks = [&](const TileInfo& ti) {
-        return p.asf128 ? min(G::kSfChunks, (ti.count + 127) / 128) : 0;
+        return MODE == kModeSf128 ? min(G::kSfChunks, (ti.count + 127) / 128) : 0;
     };
     auto issue_w = [&](const TileInfo& ti, int kb, int s) {
         uint8_t* st = c.smem + s * G::kStageBytes;
@@ -231,17 +238,17 @@ __device__ __forceinline__ void run_producer(const GemmArgs& p, const Ctx& c, in
     auto issue_a = [&](const TileInfo& ti, int kb, int s) {
         uint8_t* st = c.smem + s * G::kStageBytes;
         tma_load_2d(st + G::kOffA, &p.map_a, kb * 128, ti.tok0, &c.full[s], pol_a);
-        if (p.asf128) {
+        if constexpr (MODE == kModeSf128) {
             // Already in the TMEM-copy order: straight into the staging slot.
             const int nch = sf_chunks(ti);
             for (int ch = 0; ch < nch; ++ch)
                 bulk_load(st + G::kOffAsfT + ch * 512,
                           p.asf128 + (static_cast<size_t>((ti.tok0 >> 7) + ch) * p.kq + kb) * 512, 512, &c.full[s],
                           pol_a);
-            return;
+        } else {
+            mbar_arrive_expect_tx(&c.sfraw[s], static_cast<uint32_t>(p.sf_groups * 32));
+            tma_load_2d(st + G::kOffAsfRaw, &p.map_asf, kb * 32, ti.tok0 >> 3, &c.sfraw[s], pol_a);
         }
-        mbar_arrive_expect_tx(&c.sfraw[s], static_cast<uint32_t>(p.sf_groups * 32));
-        tma_load_2d(st + G::kOffAsfRaw, &p.map_asf, kb * 32, ti.tok0 >> 3, &c.sfraw[s], pol_a);
     };
     // Weight bytes of the first S jobs go out before waiting for the previous
     // grid: only the activations depend on it.
@@ -278,7 +285,7 @@ __device__ __forceinline__ void run_producer(const GemmArgs& p, const Ctx& c, in
     const int issued = jq > pre ? jq : pre;
     for (int j = issued - 1; j >= 0 && j >= issued - S; --j) {
         (void)mbar_wait(&c.full[stage_of(j)], (j / S) & 1, kDrainNs);
-        if (!c.fused && !p.asf128) (void)mbar_wait(&c.sfraw[stage_of(j)], (j / S) & 1, kDrainNs);
+        if (!c.fused && MODE != kModeSf128) (void)mbar_wait(&c.sfraw[stage_of(j)], (j / S) & 1, kDrainNs);
     }
 }
 
@@ -488,10 +495,12 @@ __device__ __forceinline__ void run_fused_quant(const GemmArgs& p, const Ctx& c,
 
 // Small token tiles with one pipe keep registers low enough for two CTAs
 // per SM.
-template <int TT, int PIPES>
+template <int TT, int PIPES, int MODE>
 __global__ void __launch_bounds__(32 * num_warps(TT, PIPES),
                                   ((TT <= 64 && PIPES == 1) || (TT <= 32 && PIPES == 2)) ? 2 : 1)
     mxfp8_gemm_kernel(const __grid_constant__ GemmArgs p) {
+    constexpr bool kGated = MODE == kModeGated;
+    constexpr bool kSf128 = MODE == kModeSf128;
     using G = Geometry<TT>;
     constexpr int kEpi = epi_warps(TT);
     constexpr int kReorderWarp = 2 + kEpi;
@@ -516,7 +525,7 @@ __global__ void __launch_bounds__(32 * num_warps(TT, PIPES),
     // Gated epilogue: the up half of each tile's accumulator passes through
     // xbuf [TT columns][64 rows] FP32 to the gate half.
     float* xbuf = reinterpret_cast<float*>(partial + (reduce ? splits * per * 512 : 0));
-    uint8_t* ctrl = reinterpret_cast<uint8_t*>(xbuf) + (p.gated ? 64 * TT * 4 : 0);
+    uint8_t* ctrl = reinterpret_cast<uint8_t*>(xbuf) + (kGated ? 64 * TT * 4 : 0);
     Ctx c;
     c.smem = smem;
     c.full = reinterpret_cast<uint64_t*>(ctrl);
@@ -542,19 +551,19 @@ __global__ void __launch_bounds__(32 * num_warps(TT, PIPES),
         tma_prefetch_desc(&p.map_w);
         if (!fused) {
             tma_prefetch_desc(&p.map_a);
-            if (!p.asf128) tma_prefetch_desc(&p.map_asf);
+            if (!kSf128) tma_prefetch_desc(&p.map_asf);
         }
         for (int s = 0; s < ST; ++s) {
             // full: the producer's arrival (+ TMA bytes) and either one
             // arrival per fused-quantizer patch or the scale re-order warp's.
-            mbar_init(&c.full[s], fused ? 1 + TT / 8 : (p.asf128 ? 1 : 2));
+            mbar_init(&c.full[s], fused ? 1 + TT / 8 : (kSf128 ? 1 : 2));
             mbar_init(&c.empty[s], 1);
             mbar_init(&c.sfraw[s], 1);
         }
         mbar_init(c.acc_full, PIPES);
         mbar_init(c.acc_empty, kEpi);
         for (int q = 0; q < PIPES; ++q) mbar_init(&c.drain[q], 1);
-        if (p.gated) {
+        if (kGated) {
             mbar_init(xfull, kEpi / 2);   // one arrival per up-half warp
             mbar_init(xempty, kEpi / 2);  // one arrival per gate-half warp
         }
@@ -624,13 +633,13 @@ __global__ void __launch_bounds__(32 * num_warps(TT, PIPES),
     const int nk = c.kb_end - c.kb_begin;
 
     if (warp == 0 || (warp > kReorderWarp && warp < kReorderWarp + PIPES)) {
-        if (lane == 0) run_producer<TT, PIPES>(p, c, warp == 0 ? 0 : warp - kReorderWarp);
+        if (lane == 0) run_producer<TT, PIPES, MODE>(p, c, warp == 0 ? 0 : warp - kReorderWarp);
         __syncwarp();
     } else if (warp == 1 || (warp >= kReorderWarp + PIPES && warp < num_warps(TT, PIPES))) {
         if (lane == 0) run_mma<TT, PIPES>(p, c, warp == 1 ? 0 : warp - (kReorderWarp + PIPES) + 1);
         __syncwarp();
     } else if (warp == kReorderWarp) {
-        if (!fused && !p.asf128) run_reorder<TT, PIPES>(p, c, lane);
+        if (!fused && !kSf128) run_reorder<TT, PIPES>(p, c, lane);
         __syncwarp();
     } else {
         const int ew = warp - 2;  // warps 2 .. 1+kEpi
@@ -693,7 +702,7 @@ __global__ void __launch_bounds__(32 * num_warps(TT, PIPES),
                 for (int j = 0; j < kCols; j += 4)
                     stg[((col0 + j) >> 2) * 128 + nl] = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
                 fence_proxy_async_smem();
-            } else if (p.gated) {
+            } else if constexpr (kGated) {
                 // SwiGLU: rows [0, 64) of the tile are gate rows, [64, 128) the
                 // matching up rows (gated-row order of the prepared weights);
                 // output feature ti.n_tile * 64 + nl of h = silu(gate) * up.
@@ -1197,7 +1206,7 @@ LaunchPlan plan_for(int splits, bool persistent, int kq, bool gated) {
     return lp;
 }
 
-template <int TT, int PIPES>
+template <int TT, int PIPES, int MODE>
 cudaError_t launch_tt(const GemmProblem& pr, const GemmSchedule& sch, int num_sms, cudaStream_t s,
                       bool* encode_failed) {
     constexpr int kThreads = 32 * num_warps(TT, PIPES);
@@ -1247,21 +1256,20 @@ cudaError_t launch_tt(const GemmProblem& pr, const GemmSchedule& sch, int num_sm
     a.n_tiles = n_tiles;
     a.splits = splits;
     a.persistent = sch.persistent ? 1 : 0;
-    a.gated = pr.gated ? 1 : 0;
     a.asf128 = pr.sf128 ? pr.sfa : nullptr;
     a.stages = lp.stages;
     a.tmem_cols = lp.tmem_cols;
     a.wait_ns = g_wait_limit_ns ? g_wait_limit_ns : kWaitNs;
     const size_t smem = lp.smem;
 
-    cudaError_t err = cudaFuncSetAttribute(mxfp8_gemm_kernel<TT, PIPES>,
+    cudaError_t err = cudaFuncSetAttribute(mxfp8_gemm_kernel<TT, PIPES, MODE>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;
 
     // TMEM is never oversubscribed: co-resident CTAs x columns <= 512.
     int per_sm = 1;
-    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mxfp8_gemm_kernel<TT, PIPES>, kThreads, smem);
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mxfp8_gemm_kernel<TT, PIPES, MODE>, kThreads, smem);
     if (err != cudaSuccess) return err;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     if (static_cast<uint32_t>(per_sm) * a.tmem_cols > 512u) return cudaErrorInvalidConfiguration;
@@ -1303,7 +1311,7 @@ cudaError_t launch_tt(const GemmProblem& pr, const GemmSchedule& sch, int num_sm
     t_last_schedule[2] = fused ? 1 : 0;
     t_last_schedule[3] = grid;
     t_last_schedule[4] = lp.stages;
-    return cudaLaunchKernelEx(&cfg, mxfp8_gemm_kernel<TT, PIPES>, a);
+    return cudaLaunchKernelEx(&cfg, mxfp8_gemm_kernel<TT, PIPES, MODE>, a);
 }
 
 template <int TT>
@@ -1455,24 +1463,51 @@ cudaError_t launch_gemm(const GemmProblem& p, const GemmSchedule& sch, int num_s
                         bool* encode_failed) {
     *encode_failed = false;
     if (sch.dual) return launch_dual<192>(p, num_sms, s, encode_failed);
+    if (p.gated && p.sf128) return cudaErrorInvalidValue;
+    if (p.gated) {  // grouped SwiGLU: tiles of <= 128 tokens
+        if (sch.pipes == 2) {
+            switch (sch.tokens_per_tile) {
+                case 16: return launch_tt<16, 2, kModeGated>(p, sch, num_sms, s, encode_failed);
+                case 32: return launch_tt<32, 2, kModeGated>(p, sch, num_sms, s, encode_failed);
+                case 64: return launch_tt<64, 2, kModeGated>(p, sch, num_sms, s, encode_failed);
+                default: return cudaErrorInvalidValue;
+            }
+        }
+        if (sch.pipes != 1) return cudaErrorInvalidValue;
+        switch (sch.tokens_per_tile) {
+            case 16: return launch_tt<16, 1, kModeGated>(p, sch, num_sms, s, encode_failed);
+            case 32: return launch_tt<32, 1, kModeGated>(p, sch, num_sms, s, encode_failed);
+            case 64: return launch_tt<64, 1, kModeGated>(p, sch, num_sms, s, encode_failed);
+            case 128: return launch_tt<128, 1, kModeGated>(p, sch, num_sms, s, encode_failed);
+            default: return cudaErrorInvalidValue;
+        }
+    }
+    if (p.sf128) {  // 128x4 activation scales: one pipe, tiles of 128/256 tokens
+        if (sch.pipes != 1) return cudaErrorInvalidValue;
+        switch (sch.tokens_per_tile) {
+            case 128: return launch_tt<128, 1, kModeSf128>(p, sch, num_sms, s, encode_failed);
+            case 256: return launch_tt<256, 1, kModeSf128>(p, sch, num_sms, s, encode_failed);
+            default: return cudaErrorInvalidValue;
+        }
+    }
     if (sch.pipes == 2) {
         switch (sch.tokens_per_tile) {
-            case 16: return launch_tt<16, 2>(p, sch, num_sms, s, encode_failed);
-            case 32: return launch_tt<32, 2>(p, sch, num_sms, s, encode_failed);
-            case 64: return launch_tt<64, 2>(p, sch, num_sms, s, encode_failed);
+            case 16: return launch_tt<16, 2, kModePlain>(p, sch, num_sms, s, encode_failed);
+            case 32: return launch_tt<32, 2, kModePlain>(p, sch, num_sms, s, encode_failed);
+            case 64: return launch_tt<64, 2, kModePlain>(p, sch, num_sms, s, encode_failed);
             default: return cudaErrorInvalidValue;
         }
     }
     if (sch.pipes == 4) {
-        if (sch.tokens_per_tile == 16) return launch_tt<16, 4>(p, sch, num_sms, s, encode_failed);
+        if (sch.tokens_per_tile == 16) return launch_tt<16, 4, kModePlain>(p, sch, num_sms, s, encode_failed);
         return cudaErrorInvalidValue;
     }
     switch (sch.tokens_per_tile) {
-        case 16: return launch_tt<16, 1>(p, sch, num_sms, s, encode_failed);
-        case 32: return launch_tt<32, 1>(p, sch, num_sms, s, encode_failed);
-        case 64: return launch_tt<64, 1>(p, sch, num_sms, s, encode_failed);
-        case 128: return launch_tt<128, 1>(p, sch, num_sms, s, encode_failed);
-        case 256: return launch_tt<256, 1>(p, sch, num_sms, s, encode_failed);
+        case 16: return launch_tt<16, 1, kModePlain>(p, sch, num_sms, s, encode_failed);
+        case 32: return launch_tt<32, 1, kModePlain>(p, sch, num_sms, s, encode_failed);
+        case 64: return launch_tt<64, 1, kModePlain>(p, sch, num_sms, s, encode_failed);
+        case 128: return launch_tt<128, 1, kModePlain>(p, sch, num_sms, s, encode_failed);
+        case 256: return launch_tt<256, 1, kModePlain>(p, sch, num_sms, s, encode_failed);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -54,11 +54,12 @@ __device__ __forceinline__ void st_v2(void* p, uint2 v) {
 // 128x4 layout of the prepared weights instead (tile (row/128, K block) of
 // 512 bytes, byte (row%32)*16 + ((row%128)/32)*4 + block%4; rows up to
 // m_pad = ceil128(m)), one byte per lane.
+template <bool kGather, bool kLayout128>
 __global__ void __launch_bounds__(kThreads) quant_act_kernel(const __nv_bfloat16* __restrict__ x,
                                                              int64_t m, int64_t m8, int64_t k,
                                                              const int32_t* __restrict__ src_rows,
                                                              uint8_t* __restrict__ q,
-                                                             uint8_t* __restrict__ sf, int layout128) {
+                                                             uint8_t* __restrict__ sf) {
     // Dependent kernels (the GEMM) may start their prologue now; they wait
     // for this grid's completion before reading what it writes.  This grid
     // itself may start before the kernel that produced x has finished: every
@@ -84,7 +85,7 @@ __global__ void __launch_bounds__(kThreads) quant_act_kernel(const __nv_bfloat16
 #pragma unroll
             for (int i = 0; i < 4; ++i) raw[u][i] = make_uint4(0, 0, 0, 0);
             if (t < total && row[u] < m) {
-                const int64_t sr = src_rows ? static_cast<int64_t>(src_rows[row[u]]) : row[u];
+                const int64_t sr = kGather ? static_cast<int64_t>(src_rows[row[u]]) : row[u];
                 const __nv_bfloat16* src = x + sr * k + col[u];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) raw[u][i] = *reinterpret_cast<const uint4*>(src + i * 8);
@@ -101,7 +102,7 @@ __global__ void __launch_bounds__(kThreads) quant_act_kernel(const __nv_bfloat16
                 dst[0] = make_uint4(qq[0], qq[1], qq[2], qq[3]);
                 dst[1] = make_uint4(qq[4], qq[5], qq[6], qq[7]);
             }
-            if (!layout128) {
+            if constexpr (!kLayout128) {
                 sf[t * 32 + lane] = static_cast<uint8_t>(s);  // 8x4 tile (g, quad) = t
             } else {
                 const int64_t g = t / quads;
@@ -196,8 +197,11 @@ cudaError_t launch_quant_act(const void* x, int64_t m, int64_t k, uint8_t* q, ui
     attr.val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, quant_act_kernel, static_cast<const __nv_bfloat16*>(x), m, m8, k, src_rows, q,
-                              sf, layout_128x4 ? 1 : 0);
+    const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+    if (src_rows && layout_128x4) return cudaErrorInvalidValue;
+    if (src_rows) return cudaLaunchKernelEx(&cfg, quant_act_kernel<true, false>, xb, m, m8, k, src_rows, q, sf);
+    if (layout_128x4) return cudaLaunchKernelEx(&cfg, quant_act_kernel<false, true>, xb, m, m8, k, src_rows, q, sf);
+    return cudaLaunchKernelEx(&cfg, quant_act_kernel<false, false>, xb, m, m8, k, src_rows, q, sf);
 }
 
 cudaError_t launch_prepare_weight(const void* src, bool src_is_bf16, int64_t experts, int64_t n,
