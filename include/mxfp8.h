@@ -148,7 +148,11 @@ mxfp8_status mxfp8_linear(const void* x, int64_t m, const mxfp8_weight* w,
 /* Grouped (MoE expert) layer over expert-sorted rows: rows
  * [off[e], off[e+1]) of x_sorted use expert e of w.  expert_offsets: device
  * int32 [num_experts + 1], non-decreasing, off[0] = 0, off[E] = rows (empty
- * experts allowed; the values are read on the device, not checked).
+ * experts allowed; the values are read on the device, not checked).  The
+ * GEMM reads the offsets (like the weights) in its prologue, before it waits
+ * for the previous kernel: they must be complete when the call is enqueued,
+ * or written by a kernel that does not release programmatic dependents
+ * early (ordinary kernels never do; mxfp8_moe_route does not).
  * bias: bfloat16 [num_experts][n] or NULL; y: bfloat16 [rows][n].
  * The activations are quantized as one [rows, k] matrix.  num_experts <= 1024. */
 mxfp8_status mxfp8_grouped_linear(const void* x_sorted, int64_t rows,

@@ -88,6 +88,7 @@ struct GemmArgs {
     int box_rows, sf_groups;
     int stages, splits, persistent;
     const uint8_t* asf128;   // activation scales in the 128x4 layout (dense tiles of 128/256), or null
+    int acc_bufs;            // TMEM accumulators per pipe: 2 lets tile t+1's MMAs overlap tile t's epilogue
     int num_tiles;           // dense (grouped counts tiles on the device)
     uint32_t tmem_cols;
     uint64_t wait_ns;        // limit of every pipeline wait
@@ -302,7 +303,7 @@ __device__ __forceinline__ void run_mma(const GemmArgs& p, const Ctx& c, int q) 
     const int nk = c.kb_end - c.kb_begin;
     const int nq = pipe_jobs<PIPES>(q, nk);  // jobs of this pipe in one tile
     const int S = c.stages;
-    const uint32_t acc = c.tmem_base + q * TT;
+    const int nb = p.acc_bufs;
     int jq = 0;
     int tile_iter = 0;
     for (int t = c.tile_first; t < c.num_tiles; t += c.tile_stride, ++tile_iter) {
@@ -311,9 +312,13 @@ __device__ __forceinline__ void run_mma(const GemmArgs& p, const Ctx& c, int q) 
         uint32_t idesc[4];
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) idesc[kk] = idesc_mxf8(128, n_mma, kk, kk);
-        // Every pipe waits for the epilogue to drain the previous tile, so the
-        // accumulator barrier can never run two phases ahead of any pipe.
-        if (tile_iter > 0 && !mbar_wait(c.acc_empty, (tile_iter - 1) & 1, p.wait_ns)) {
+        // Accumulator buffer a takes tiles a, a + nb, ...: every pipe waits for
+        // the epilogue to drain the buffer's previous tile, so a buffer's
+        // barriers never run two phases ahead of any pipe.
+        const int ab = tile_iter % nb;
+        const int use = tile_iter / nb;
+        const uint32_t acc = c.tmem_base + (ab * PIPES + q) * TT;
+        if (use > 0 && !mbar_wait(&c.acc_empty[ab], (use - 1) & 1, p.wait_ns)) {
             record_timeout(c.abort_flag);
             break;
         }
@@ -327,7 +332,7 @@ __device__ __forceinline__ void run_mma(const GemmArgs& p, const Ctx& c, int q) 
                 break;
             }
             const uint64_t sd = static_cast<uint64_t>(s) * kStageStep;
-            const uint32_t sfa = c.tmem_base + PIPES * TT + s * G::kSfSlotCols;
+            const uint32_t sfa = c.tmem_base + nb * PIPES * TT + s * G::kSfSlotCols;
             const uint32_t sfb = sfa + 4;
             tmem_copy_sf(sfa, wsf_desc0 + sd);
 #pragma unroll
@@ -341,7 +346,7 @@ __device__ __forceinline__ void run_mma(const GemmArgs& p, const Ctx& c, int q) 
             if (p.persistent || jq + S < nq) mma_commit(&c.empty[s]);
         }
         if (stop) break;
-        mma_commit(c.acc_full);  // also for a pipe with no K block in this tile
+        mma_commit(&c.acc_full[ab]);  // also for a pipe with no K block in this tile
     }
     // Drain every MMA this thread issued before TMEM is released.
     mma_commit(&c.drain[q]);
@@ -497,7 +502,7 @@ __device__ __forceinline__ void run_fused_quant(const GemmArgs& p, const Ctx& c,
 // per SM.
 template <int TT, int PIPES, int MODE>
 __global__ void __launch_bounds__(32 * num_warps(TT, PIPES),
-                                  ((TT <= 64 && PIPES == 1) || (TT <= 32 && PIPES == 2)) ? 2 : 1)
+                                  ((TT <= 64 && PIPES == 1) || (TT <= 32 && PIPES == 2) || (TT == 16 && PIPES == 4)) ? 2 : 1)
     mxfp8_gemm_kernel(const __grid_constant__ GemmArgs p) {
     constexpr bool kGated = MODE == kModeGated;
     constexpr bool kSf128 = MODE == kModeSf128;
@@ -532,8 +537,8 @@ __global__ void __launch_bounds__(32 * num_warps(TT, PIPES),
     c.empty = c.full + ST;
     c.sfraw = c.empty + ST;
     c.acc_full = c.sfraw + ST;
-    c.acc_empty = c.acc_full + 1;
-    c.drain = c.acc_empty + 1;  // [PIPES]
+    c.acc_empty = c.acc_full + 2;  // acc_full[2], acc_empty[2]: one pair per accumulator buffer
+    c.drain = c.acc_empty + 2;     // [PIPES]
     uint64_t* red = c.drain + PIPES;  // split-K: the peers' partials have landed
     uint64_t* xfull = red + 1;        // gated: the up half of a tile is in xbuf
     uint64_t* xempty = red + 2;       // gated: the gate half has read it
@@ -560,8 +565,10 @@ __global__ void __launch_bounds__(32 * num_warps(TT, PIPES),
             mbar_init(&c.empty[s], 1);
             mbar_init(&c.sfraw[s], 1);
         }
-        mbar_init(c.acc_full, PIPES);
-        mbar_init(c.acc_empty, kEpi);
+        for (int ab = 0; ab < 2; ++ab) {
+            mbar_init(&c.acc_full[ab], PIPES);
+            mbar_init(&c.acc_empty[ab], kEpi);
+        }
         for (int q = 0; q < PIPES; ++q) mbar_init(&c.drain[q], 1);
         if (kGated) {
             mbar_init(xfull, kEpi / 2);   // one arrival per up-half warp
@@ -662,14 +669,16 @@ __global__ void __launch_bounds__(32 * num_warps(TT, PIPES),
             const TileInfo ti = decode_tile<TT>(t, p, prefix, offs);
             const int n = ti.n_tile * 128 + nl;
             b = (p.bias && n < p.n) ? __bfloat162float(p.bias[static_cast<size_t>(ti.e) * p.n + n]) : 0.0f;
-            bool ok = mbar_wait(c.acc_full, tile_iter & 1, p.wait_ns);
+            const int ab = tile_iter % p.acc_bufs;
+            bool ok = mbar_wait(&c.acc_full[ab], (tile_iter / p.acc_bufs) & 1, p.wait_ns);
             ok = __all_sync(0xFFFFFFFFu, ok ? 1 : 0) != 0;
             if (!ok) { if (lane == 0) record_timeout(c.abort_flag); break; }
             tc_fence_after();
 #pragma unroll
             for (int i = 0; i < kCols; ++i) acc[i] = 0.0f;
             for (int q = 0; q < n_active; ++q) {  // pipe order: deterministic sums
-                const uint32_t taddr = c.tmem_base + q * TT + (static_cast<uint32_t>(quad * 32) << 16) + col0;
+                const uint32_t taddr =
+                    c.tmem_base + (ab * PIPES + q) * TT + (static_cast<uint32_t>(quad * 32) << 16) + col0;
                 uint32_t r[kCols];
                 if constexpr (kCols >= 32) {
 #pragma unroll
@@ -690,7 +699,7 @@ __global__ void __launch_bounds__(32 * num_warps(TT, PIPES),
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(c.acc_empty);
+            if (lane == 0) mbar_arrive(&c.acc_empty[ab]);
 
             if (reduce) {
                 // Stage the partial tile in the idle pipeline stages (every MMA
@@ -1273,6 +1282,16 @@ cudaError_t launch_tt(const GemmProblem& pr, const GemmSchedule& sch, int num_sm
     if (err != cudaSuccess) return err;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     if (static_cast<uint32_t>(per_sm) * a.tmem_cols > 512u) return cudaErrorInvalidConfiguration;
+    // Persistent tiles: a second accumulator per pipe where tensor memory
+    // allows it, so the next tile's MMAs overlap this tile's epilogue.
+    a.acc_bufs = 1;
+    if (sch.persistent) {
+        const uint32_t cols2 = pow2_cols(2 * PIPES * TT + PIPES * lp.stages * G::kSfSlotCols);
+        if (cols2 <= 512u && static_cast<uint32_t>(per_sm) * cols2 <= 512u) {
+            a.acc_bufs = 2;
+            a.tmem_cols = cols2;
+        }
+    }
 
     int grid;
     if (!sch.persistent) {

@@ -12,16 +12,18 @@
 //                       rounds of warp arg-max over the logits, the weights,
 //                       then per-expert token masks -> group counts and each
 //                       pair's rank inside its group;
-//   route_scan_kernel   one CTA: per-expert totals -> offsets, and per
-//                       (group, expert) the first sorted row of that group;
-//   route_assign_kernel row_of[t*k + s] and sorted_token[row].
+//   route_scan_assign_kernel  one CTA: per-expert totals -> offsets, per
+//                       (group, expert) the first sorted row of that group,
+//                       then row_of[t*k + s] and sorted_token[row].
 // Finalize sums each token's k expert outputs with its routing weights in
 // slot order (FP32) and rounds once to BF16.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <string.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace mxk {
 
@@ -35,19 +37,118 @@ __device__ __forceinline__ bool better(float v, int e, float bv, int be) {
     return v > bv || (v == bv && e < be);
 }
 
-// One CTA per group of 32 tokens, one warp per token.  Round r of a warp
-// picks the best (logit, id) among the candidates ranked below round r-1's
-// pick (so earlier picks are excluded without storing them) with a strided
-// scan per lane and a butterfly arg-max.  Then the group's picks go into
-// per-expert 32-bit token masks in shared memory (atomicOr: the result does
-// not depend on the order), which give the group count of every expert and
-// each pair's rank among the group's tokens.
+// Logits of one token held by its warp: lane l keeps experts l, l + 32, ...
+// (up to kRegLogits per lane, i.e. 256 experts) in registers so that the k
+// selection rounds do not reload them; wider layers read them each round.
+constexpr int kRegLogits = 8;
+
+struct TokenLogits {
+    float v[kRegLogits];
+};
+
+__device__ __forceinline__ void load_token_logits(const float* __restrict__ lg, int experts, int lane,
+                                                  TokenLogits& tl) {
+#pragma unroll
+    for (int i = 0; i < kRegLogits; ++i) {
+        const int e = lane + 32 * i;
+        tl.v[i] = e < experts ? lg[e] : -INFINITY;
+    }
+}
+
+// Top-k of one token by its warp (lane-strided scan + butterfly arg-max per
+// round, each round excluding earlier picks by order) and its weights.
+// Lane 0 writes ids (global, and sel_row if given); lanes < topk write the
+// weights.  tl holds the logits when experts <= 32 * kRegLogits.
+__device__ __forceinline__ void route_token(const float* __restrict__ lg, const TokenLogits& tl, int experts,
+                                            int topk, int method, int lane, int32_t* __restrict__ ids_t,
+                                            float* __restrict__ w_t, int* sel_row) {
+    const bool in_regs = experts <= 32 * kRegLogits;
+    float pv = INFINITY;
+    int pe = -1;  // previous pick; round 0 admits everything
+    float top[kMaxTopK];
+#pragma unroll
+    for (int r = 0; r < kMaxTopK; ++r) {
+        if (r >= topk) break;
+        float bv = -INFINITY;
+        int be = 0x7FFFFFFF;
+        if (in_regs) {
+#pragma unroll
+            for (int i = 0; i < kRegLogits; ++i) {
+                const int e = lane + 32 * i;
+                const float v = tl.v[i];
+                if (e < experts && better(pv, pe, v, e) && better(v, e, bv, be)) { bv = v; be = e; }
+            }
+        } else {
+            for (int e = lane; e < experts; e += 32) {
+                const float v = lg[e];
+                if (better(pv, pe, v, e) && better(v, e, bv, be)) { bv = v; be = e; }
+            }
+        }
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1) {
+            const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, d);
+            const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, d);
+            if (better(ov, oe, bv, be)) { bv = ov; be = oe; }
+        }
+        top[r] = bv;
+        if (lane == 0) {
+            ids_t[r] = be;
+            if (sel_row) sel_row[r] = be;
+        }
+        pv = bv;
+        pe = be;
+    }
+    // Weights (m = top[0] is the token's largest logit).
+    float z[kMaxTopK];
+    float zs = 0.0f;
+#pragma unroll
+    for (int r = 0; r < kMaxTopK; ++r) {
+        z[r] = r < topk ? expf(top[r] - top[0]) : 0.0f;
+        zs += z[r];
+    }
+    if (method == 1) {
+        // Softmax over all logits (lane-strided partial sums, then a fixed
+        // butterfly: deterministic), then renormalize the k picks.
+        float all = 0.0f;
+        if (in_regs) {
+#pragma unroll
+            for (int i = 0; i < kRegLogits; ++i)
+                if (lane + 32 * i < experts) all += expf(tl.v[i] - top[0]);
+        } else {
+            for (int e = lane; e < experts; e += 32) all += expf(lg[e] - top[0]);
+        }
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1) all += __shfl_xor_sync(0xFFFFFFFFu, all, d);
+        float ps = 0.0f;
+#pragma unroll
+        for (int r = 0; r < kMaxTopK; ++r) {
+            z[r] = z[r] / all;
+            ps += r < topk ? z[r] : 0.0f;
+        }
+        zs = ps;
+    }
+    if (lane < topk) {
+        float mine = 0.0f;
+#pragma unroll
+        for (int r = 0; r < kMaxTopK; ++r)
+            if (r == lane) mine = z[r];
+        w_t[lane] = mine / zs;
+    }
+}
+
+// One CTA per group of 32 tokens, one warp per token.  The group's picks
+// then go into per-expert 32-bit token masks in shared memory (atomicOr: the
+// result does not depend on the order), which give the group count of every
+// expert and each pair's rank among the group's tokens.
 __global__ void __launch_bounds__(1024)
     route_topk_kernel(const float* __restrict__ logits, int tokens, int experts, int topk, int method,
                       int32_t* __restrict__ ids, float* __restrict__ weights,
                       int32_t* __restrict__ grp_count, int32_t* __restrict__ rank) {
     __shared__ int sel[32][kMaxTopK];
     __shared__ unsigned bits[kMaxExpertsRoute];
+    // Waits for the kernel that produced the logits, but does not release its
+    // own dependents early (see launch_moe_route).
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int w = threadIdx.x >> 5;
     const int group = blockIdx.x;
@@ -55,62 +156,10 @@ __global__ void __launch_bounds__(1024)
     for (int e = threadIdx.x; e < experts; e += blockDim.x) bits[e] = 0u;
     if (t < tokens) {
         const float* lg = logits + static_cast<size_t>(t) * experts;
-        float pv = INFINITY;
-        int pe = -1;  // previous pick; round 0 admits everything
-        float top[kMaxTopK];
-#pragma unroll
-        for (int r = 0; r < kMaxTopK; ++r) {
-            if (r >= topk) break;
-            float bv = -INFINITY;
-            int be = 0x7FFFFFFF;
-            for (int e = lane; e < experts; e += 32) {
-                const float v = lg[e];
-                if (better(pv, pe, v, e) && better(v, e, bv, be)) { bv = v; be = e; }
-            }
-#pragma unroll
-            for (int d = 16; d > 0; d >>= 1) {
-                const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, d);
-                const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, d);
-                if (better(ov, oe, bv, be)) { bv = ov; be = oe; }
-            }
-            top[r] = bv;
-            if (lane == 0) {
-                ids[static_cast<size_t>(t) * topk + r] = be;
-                sel[w][r] = be;
-            }
-            pv = bv;
-            pe = be;
-        }
-        // Weights (m = top[0] is the token's largest logit).
-        float z[kMaxTopK];
-        float zs = 0.0f;
-#pragma unroll
-        for (int r = 0; r < kMaxTopK; ++r) {
-            z[r] = r < topk ? expf(top[r] - top[0]) : 0.0f;
-            zs += z[r];
-        }
-        if (method == 1) {
-            // Softmax over all logits (lane-strided partial sums, then a
-            // fixed butterfly: deterministic), then renormalize the k picks.
-            float all = 0.0f;
-            for (int e = lane; e < experts; e += 32) all += expf(lg[e] - top[0]);
-#pragma unroll
-            for (int d = 16; d > 0; d >>= 1) all += __shfl_xor_sync(0xFFFFFFFFu, all, d);
-            float ps = 0.0f;
-#pragma unroll
-            for (int r = 0; r < kMaxTopK; ++r) {
-                z[r] = z[r] / all;
-                ps += r < topk ? z[r] : 0.0f;
-            }
-            zs = ps;
-        }
-        if (lane < topk) {
-            float mine = 0.0f;
-#pragma unroll
-            for (int r = 0; r < kMaxTopK; ++r)
-                if (r == lane) mine = z[r];
-            weights[static_cast<size_t>(t) * topk + lane] = mine / zs;
-        }
+        TokenLogits tl;
+        if (experts <= 32 * kRegLogits) load_token_logits(lg, experts, lane, tl);
+        route_token(lg, tl, experts, topk, method, lane, ids + static_cast<size_t>(t) * topk,
+                    weights + static_cast<size_t>(t) * topk, sel[w]);
     }
     __syncthreads();
     const int live = min(32, tokens - group * 32);
@@ -125,16 +174,22 @@ __global__ void __launch_bounds__(1024)
         grp_count[static_cast<size_t>(group) * experts + e] = __popc(bits[e]);
 }
 
-// One CTA, thread e per expert (loops if experts > blockDim).  Replaces the
-// group counts by each group's first sorted row for that expert.
+// One CTA (thread e per expert, experts <= 1024): per-expert totals over the
+// groups -> offsets (block scan); each group's counts are replaced by the
+// group's first sorted row for that expert; then every pair gets its row
+// (group base + rank in the group) and each row its token.
 __global__ void __launch_bounds__(1024)
-    route_scan_kernel(int groups, int experts, int32_t* __restrict__ grp, int32_t* __restrict__ offsets) {
+    route_scan_assign_kernel(int tokens, int experts, int topk, const int32_t* __restrict__ ids,
+                             int32_t* __restrict__ grp, const int32_t* __restrict__ rank,
+                             int32_t* __restrict__ offsets, int32_t* __restrict__ row_of,
+                             int32_t* __restrict__ sorted_token) {
     __shared__ int warp_sum[32];
+    const int groups = (tokens + 31) / 32;
     const int e = threadIdx.x;
     int total = 0;
     if (e < experts)
         for (int g = 0; g < groups; ++g) total += grp[static_cast<size_t>(g) * experts + e];
-    // Block-wide exclusive scan of tot over experts.
+    // Block-wide exclusive scan of the totals over experts.
     const int lane = e & 31, w = e >> 5;
     int incl = total;
 #pragma unroll
@@ -145,13 +200,13 @@ __global__ void __launch_bounds__(1024)
     if (lane == 31) warp_sum[w] = incl;
     __syncthreads();
     if (w == 0) {
-        int s = lane < (blockDim.x >> 5) ? warp_sum[lane] : 0;
+        int sw = lane < (blockDim.x >> 5) ? warp_sum[lane] : 0;
 #pragma unroll
         for (int d = 1; d < 32; d <<= 1) {
-            const int y = __shfl_up_sync(0xFFFFFFFFu, s, d);
-            if (lane >= d) s += y;
+            const int y = __shfl_up_sync(0xFFFFFFFFu, sw, d);
+            if (lane >= d) sw += y;
         }
-        warp_sum[lane] = s;  // inclusive over warps
+        warp_sum[lane] = sw;  // inclusive over warps
     }
     __syncthreads();
     const int base = incl - total + (w > 0 ? warp_sum[w - 1] : 0);
@@ -166,18 +221,14 @@ __global__ void __launch_bounds__(1024)
         }
     }
     if (e == experts - 1) offsets[experts] = base + total;
-}
-
-__global__ void route_assign_kernel(int tokens, int experts, int topk, const int32_t* __restrict__ ids,
-                                    const int32_t* __restrict__ grp, const int32_t* __restrict__ rank,
-                                    int32_t* __restrict__ row_of, int32_t* __restrict__ sorted_token) {
-    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (i >= static_cast<int64_t>(tokens) * topk) return;
-    const int t = static_cast<int>(i / topk);
-    const int e = ids[i];
-    const int r = grp[static_cast<size_t>(t >> 5) * experts + e] + rank[i];
-    row_of[i] = r;
-    sorted_token[r] = t;
+    __syncthreads();  // this CTA's bases are visible to all of its threads
+    const int pairs = tokens * topk;
+    for (int i = threadIdx.x; i < pairs; i += blockDim.x) {
+        const int t = i / topk;
+        const int r = grp[static_cast<size_t>(t >> 5) * experts + ids[i]] + rank[i];
+        row_of[i] = r;
+        sorted_token[r] = t;
+    }
 }
 
 // One warp per (token, 256-column chunk): lane c8 sums 8 columns over the
@@ -187,6 +238,8 @@ __global__ void __launch_bounds__(kFinThreads)
     finalize_kernel(const __nv_bfloat16* __restrict__ y2, const int32_t* __restrict__ row_of,
                     const float* __restrict__ weights, int64_t tokens, int topk, int64_t hidden,
                     __nv_bfloat16* __restrict__ out) {
+    pdl_launch_dependents();
+    pdl_wait();  // y2 comes from the previous kernel
     const int lane = threadIdx.x & 31;
     const int64_t chunks = (hidden + 255) >> 8;
     const int64_t total = tokens * chunks;
@@ -221,22 +274,32 @@ __global__ void __launch_bounds__(kFinThreads)
 
 }  // namespace
 
+// The routing kernels are launched with programmatic stream serialization so
+// that their launch overlaps the previous kernel (they wait for it before
+// reading the logits), but they never trigger their dependents early: the
+// grouped GEMMs read the expert offsets in their prologue, before their own
+// griddepcontrol.wait, so every kernel after the router must start only once
+// the offsets are complete.
 cudaError_t launch_moe_route(const float* logits, int64_t tokens, int64_t experts, int64_t topk, int method,
                              int32_t* ids, float* weights, int32_t* offsets, int32_t* sorted_token,
                              int32_t* row_of, int32_t* ws, cudaStream_t s) {
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.blockDim = dim3(1024, 1, 1);
+    cfg.stream = s;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    const int T = static_cast<int>(tokens), E = static_cast<int>(experts), K = static_cast<int>(topk);
     const int groups = static_cast<int>((tokens + 31) / 32);
     int32_t* grp = ws;
     int32_t* rank = ws + static_cast<size_t>(groups) * experts;
-    route_topk_kernel<<<groups, 1024, 0, s>>>(logits, static_cast<int>(tokens), static_cast<int>(experts),
-                                              static_cast<int>(topk), method, ids, weights, grp, rank);
-    cudaError_t e = cudaGetLastError();
+    cfg.gridDim = dim3(groups, 1, 1);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, route_topk_kernel, logits, T, E, K, method, ids, weights, grp, rank);
     if (e != cudaSuccess) return e;
-    route_scan_kernel<<<1, 1024, 0, s>>>(groups, static_cast<int>(experts), grp, offsets);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const int64_t pairs = tokens * topk;
-    route_assign_kernel<<<static_cast<int>((pairs + 255) / 256), 256, 0, s>>>(
-        static_cast<int>(tokens), static_cast<int>(experts), static_cast<int>(topk), ids, grp, rank, row_of,
-        sorted_token);
+    route_scan_assign_kernel<<<1, 1024, 0, s>>>(T, E, K, ids, grp, rank, offsets, row_of, sorted_token);
     return cudaGetLastError();
 }
 
@@ -246,10 +309,18 @@ cudaError_t launch_moe_finalize(const void* y2, const int32_t* row_of, const flo
     int64_t blocks = (work + (kFinThreads / 32) - 1) / (kFinThreads / 32);
     if (blocks > static_cast<int64_t>(num_sms) * 8) blocks = static_cast<int64_t>(num_sms) * 8;
     if (blocks < 1) blocks = 1;
-    finalize_kernel<<<static_cast<int>(blocks), kFinThreads, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(y2), row_of, weights, tokens, static_cast<int>(topk), hidden,
-        static_cast<__nv_bfloat16*>(out));
-    return cudaGetLastError();
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+    cfg.blockDim = dim3(kFinThreads, 1, 1);
+    cfg.stream = s;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, finalize_kernel, static_cast<const __nv_bfloat16*>(y2), row_of, weights, tokens,
+                              static_cast<int>(topk), hidden, static_cast<__nv_bfloat16*>(out));
 }
 
 }  // namespace mxk

@@ -33,7 +33,9 @@ def _route_both(mx, logits, topk, method):
 
 @pytest.mark.parametrize("method", [M.RENORMALIZE, M.RENORMALIZE_NAIVE])
 @pytest.mark.parametrize("shape", [(256, 128, 8, False), (37, 8, 2, False), (64, 16, 16, False),
-                                   (33, 8, 8, False), (200, 32, 4, True), (1, 4, 1, False)])
+                                   (33, 8, 8, False), (200, 32, 4, True), (1, 4, 1, False),
+                                   # above 16384 (token, slot) pairs: the multi-CTA routing path
+                                   (3000, 64, 8, False), (2100, 32, 8, True)])
 def test_route_matches_oracle(lib, method, shape):
     t, e, k, ties = shape
     mw = workloads.moe(seed=20 + t, tokens=t, experts=e, topk=k, hidden=256, inter=256, logit_ties=ties)
