@@ -539,6 +539,9 @@ def main():
     clocks.start()
     ms = time_steps(setup.linear, args.steps, max(3, args.warmup), barrier=barrier)
     clk = clocks.stop()
+    # kernels per call of the timed schedule: the GEMM, plus the activation
+    # quantizer unless the GEMM quantizes its own tile
+    launches_per_step = 1 if mx.last_schedule()["fused"] else 2
     t_max = ms
     if ws > 1:
         import torch.distributed as dist
@@ -573,7 +576,7 @@ def main():
                             "(%.0f MB)" % (setup.R, setup.R * nbytes / 1e6),
                       "timing": "CUDA graphs of back-to-back calls, CUDA events"},
            "roofline": roof,
-           "gpu_launches": 2 * args.steps,
+           "gpu_launches": launches_per_step * args.steps,
            "clocks": clk,
            "e2e": e2e,
            "kernel_us": {"linear_call": t_max / args.steps * 1e3, "gemm": ms_g * 1e3,
