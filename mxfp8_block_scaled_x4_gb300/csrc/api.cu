@@ -318,14 +318,14 @@ namespace {
 // {tokens_per_tile (192 = two weight tiles), split_k (-1 = persistent),
 //  fuse_quant, pipes}
 void encode_tactic(const mxk::GemmSchedule& s, int32_t* t4) {
-    t4[0] = s.dual ? 192 : s.tokens_per_tile;
+    t4[0] = s.tokens_per_tile;
     t4[1] = s.persistent ? -1 : s.split_k;
     t4[2] = s.fuse_quant ? 1 : 0;
     t4[3] = s.pipes;
 }
 bool decode_tactic(const int32_t* t4, int kind, int64_t k, mxk::GemmSchedule* s) {
-    s->dual = t4[0] == 192;
-    s->tokens_per_tile = s->dual ? 192 : t4[0];
+    s->dual = (t4[0] == 192 || t4[0] == 160) && t4[1] == -1;
+    s->tokens_per_tile = t4[0];
     s->persistent = t4[1] == -1;
     s->split_k = s->persistent ? 1 : t4[1];
     s->fuse_quant = t4[2] != 0;
@@ -632,8 +632,10 @@ void mxfp8_last_schedule(int* out5) {
 }
 
 void mxfp8_set_schedule(int tokens_per_tile, int split_k, int fuse_quant) {
+    // 160 / 192: the dual weight-tile schedule (dense, persistent).
     const bool tt_ok = tokens_per_tile == 0 || tokens_per_tile == 16 || tokens_per_tile == 32 ||
-                       tokens_per_tile == 64 || tokens_per_tile == 128 || tokens_per_tile == 256;
+                       tokens_per_tile == 64 || tokens_per_tile == 128 || tokens_per_tile == 256 ||
+                       tokens_per_tile == 160 || tokens_per_tile == 192;
     g_force_tt = tt_ok ? tokens_per_tile : 0;
     g_force_split = (split_k >= -1 && split_k <= 8) ? split_k : 0;
     g_force_fuse = (fuse_quant >= -1 && fuse_quant <= 1) ? fuse_quant : -1;

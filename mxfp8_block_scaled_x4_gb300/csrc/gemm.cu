@@ -1423,14 +1423,18 @@ GemmSchedule choose_schedule(const GemmProblem& p, int num_sms, int force_tt, in
     }
     if (force_tt) tt = force_tt;
     if (p.gated && tt > 128) tt = 128;  // the gated exchange buffer holds 64 x TT FP32
-    // Dense large M: two weight tiles x 192 tokens per CTA tile whenever
-    // that still gives every SM a tile (measured on 8192^3).
+    // Dense large M: two weight tiles x 192 tokens per CTA tile whenever that
+    // still gives every SM a tile (measured on 8192^3).  160-token tiles
+    // leave a fuller last wave there (1664 tiles = 10.95 waves of 152,
+    // against 1376 = 9.05) but measured slower (409 against 393 us): the
+    // narrower MMAs cost more issue per FLOP.  They stay a tactic.
     bool dual = false;
-    if (p.offsets == nullptr && tt == 256 && force_tt == 0 &&
+    int dual_tt = 192;
+    if (p.offsets == nullptr && !p.gated && !p.sf128 && tt == 256 && force_tt == 0 &&
         ((p.n_pad / 128 + 1) / 2) * ((p.m + 191) / 192) >= num_sms)
         dual = true;
-    if (p.offsets == nullptr && force_tt == 192) dual = true;
-    if (dual) tt = 192;
+    if (p.offsets == nullptr && (force_tt == 192 || force_tt == 160)) { dual = true; dual_tt = force_tt; }
+    if (dual) tt = dual_tt;
     bool persistent = p.offsets != nullptr || tt > 128;
     int split = 1;
     if (!persistent) {
@@ -1481,7 +1485,10 @@ GemmSchedule choose_schedule(const GemmProblem& p, int num_sms, int force_tt, in
 cudaError_t launch_gemm(const GemmProblem& p, const GemmSchedule& sch, int num_sms, cudaStream_t s,
                         bool* encode_failed) {
     *encode_failed = false;
-    if (sch.dual) return launch_dual<192>(p, num_sms, s, encode_failed);
+    if (sch.dual) {
+        if (sch.tokens_per_tile == 160) return launch_dual<160>(p, num_sms, s, encode_failed);
+        return launch_dual<192>(p, num_sms, s, encode_failed);
+    }
     if (p.gated && p.sf128) return cudaErrorInvalidValue;
     if (p.gated) {  // grouped SwiGLU: tiles of <= 128 tokens
         if (sch.pipes == 2) {

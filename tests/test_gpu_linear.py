@@ -101,13 +101,16 @@ def test_multi_pipe_schedules(lib, tt, split, fuse, pipes):
     _run_dense(lib, d, schedule=(tt, split, fuse), pipes=pipes)
 
 
-@pytest.mark.parametrize("m,n,k", [(300, 300, 1024), (1000, 640, 512), (193, 128, 256)])
-def test_dual_weight_tile_schedule(lib, m, n, k):
-    """Two weight tiles x 192 tokens per CTA tile (the large-M schedule):
-    odd numbers of weight tiles (the pair's second tile out of range), ragged
-    token tails, a single weight tile."""
+@pytest.mark.parametrize("tt", [192, 160])
+@pytest.mark.parametrize("m,n,k", [(300, 300, 1024), (1000, 640, 512), (193, 128, 256), (161, 256, 512)])
+def test_dual_weight_tile_schedule(lib, m, n, k, tt):
+    """Two weight tiles x 160 or 192 tokens per CTA tile (the large-M
+    schedule): odd numbers of weight tiles (the pair's second tile out of
+    range), ragged token tails, a single weight tile."""
     d = workloads.dense(m=m, n=n, k=k, seed=m + n, bias=True)
-    _run_dense(lib, d, schedule=(192, -1, 0))
+    _run_dense(lib, d, schedule=(tt, -1, 0))
+    sched = lib.last_schedule()
+    assert sched["split"] == -2 and sched["tokens_per_tile"] == tt, sched
 
 
 def test_dual_schedule_unaligned_output(lib):
@@ -119,7 +122,7 @@ def test_dual_schedule_unaligned_output(lib):
     buf = torch.empty(d.m * d.n + 8, dtype=torch.bfloat16, device="cuda")
     y = buf[1:1 + d.m * d.n].view(d.m, d.n)  # 2-byte offset from a 256-byte aligned base
     import ctypes
-    lib.set_schedule(192, -1, 0)
+    lib.set_schedule(192, -1, 0)  # the dual weight-tile kernel
     try:
         ws = torch.empty(lib.linear_workspace_bytes(d.m, d.k), dtype=torch.uint8, device="cuda")
         st = lib.library().mxfp8_linear(ctypes.c_void_p(x.data_ptr()), d.m, ctypes.byref(pw.c),
