@@ -12,41 +12,52 @@
 // token count beyond 16 (FlashInfer PR #1214 names the same choice:
 // "shuffling for transposed MMA outputs").
 //
-// Per CTA (352 threads, 11 warps):
-//   warp 0      TMA producer: per 128-wide K block, one 128x128 weight tile,
-//               the weight scales (one 512-byte bulk copy, already in
-//               TMEM-copy order) and -- unless quantization is fused -- the
-//               token tile (TMA boxes of <= 32 rows) and the raw 8x4
-//               activation-scale groups (one TMA box).
-//   warp 1      TMEM allocator; its lane 0 alone is the MMA issuer: copies
-//               both scale tiles into TMEM (tcgen05.cp 32x128b.warpx4), issues
-//               four tcgen05.mma kind::mxf8f6f4 block_scale (K = 32 each) and
-//               commits the stage back to the producer.  The issue path holds no
-//               warp-wide synchronisation: its cost per stage bounds the whole
-//               kernel at small N.
-//   warps 2..9  epilogue: two warps per TMEM lane quadrant, each half of the
-//               token columns; tcgen05.ld, release the accumulator, then
-//               + bias, BF16 rounding and masked stores (j < N, token < M).
-//               With fused quantization they first quantize the BF16 token
-//               rows of each K block straight into the swizzled B tile and
-//               the TMEM-copy scale order (same arithmetic as quant.cu).
-//   warp 10     scale re-order (unfused only): token j of the raw 8x4 groups
-//               goes to word (j%32)*4 + (j%128)/32 of its 128-token chunk,
-//               the order tcgen05.cp 32x128b.warpx4 expects.
+// mxfp8_gemm_kernel<TT, PIPES, MODE> (TT tokens per tile, PIPES MMA
+// pipelines per CTA, MODE plain / gated SwiGLU / 128x4 activation scales):
+//   warp 0      TMA producer of pipe 0: per 128-wide K block, one 128x128
+//               weight tile, the weight scales (one 512-byte bulk copy,
+//               already in TMEM-copy order) and -- unless quantization is
+//               fused -- the token tile (one TMA box) and its scales (the
+//               raw 8x4 groups in one box, or the 128x4 tiles by bulk copy).
+//   warp 1      TMEM allocator; its lane 0 alone is the MMA issuer of pipe 0:
+//               copies both scale tiles into TMEM (tcgen05.cp 32x128b.warpx4),
+//               issues four tcgen05.mma kind::mxf8f6f4 block_scale (K = 32
+//               each) and commits the stage back to the producer.  Each
+//               tcgen05/TMA/mbarrier instruction costs its issuing thread
+//               ~55-170 cycles, which bounds one pipeline at small N.
+//   warps 2..   epilogue (4 warps for TT <= 32, else 8, one or two per TMEM
+//               lane quadrant): tcgen05.ld, release the accumulator, then
+//               + bias, BF16 rounding and masked stores (j < N, token < M);
+//               the gated mode passes the up half to the gate half through
+//               shared memory and stores silu(gate) * up.  With fused
+//               quantization they first quantize the BF16 token rows of
+//               each K block straight into the swizzled B tile and the
+//               TMEM-copy scale order (same arithmetic as quant.cu).
+//   next warp   8x4 scale re-order (unfused, 8x4 scales): token j of the
+//               raw groups goes to word (j%32)*4 + (j%128)/32 of its
+//               128-token chunk, the order tcgen05.cp 32x128b.warpx4 expects.
+//   last warps  producers and MMA issuers of pipes 1..PIPES-1: pipe q takes
+//               the local K blocks i with i % PIPES == q into its own stages
+//               and its own TMEM accumulator; the epilogue sums the pipes'
+//               accumulators in pipe order (deterministic).
 // Schedules:
 //   persistent   grid <= #SMs x occupancy, tiles strided over CTAs (large M,
-//                grouped).
+//                grouped); a second TMEM accumulator per pipe where tensor
+//                memory allows it, so the next tile's MMAs overlap this
+//                tile's epilogue.
 //   one tile     one output tile per cluster of `splits` CTAs, each a K range
 //                (small M).  With splits > 1 each rank owns a slice of the
-//                token columns; every rank pushes the FP32 partials of the
-//                other ranks' slices into their shared memory with st.async,
-//                which counts the bytes on the owner's mbarrier, and each owner
-//                sums its slice in rank order (deterministic) as soon as its
-//                bytes have landed -- no cluster-wide barrier on that path.
+//                token columns; every rank stages its FP32 partials in its
+//                idle pipeline stages and one bulk copy per peer moves the
+//                peer's slice into the peer's shared memory, counted on the
+//                peer's mbarrier; each owner sums its slice in rank order
+//                (deterministic) as soon as its bytes have landed.
+//   dual         mxfp8_gemm_dual_kernel<TT>: two 128-row weight tiles x 160
+//                or 192 tokens per CTA tile (dense, large M), below.
 // Programmatic dependent launch: the kernel lets the next grid start at once;
 // it reads nothing a previous grid may write before griddepcontrol.wait,
 // except the weights, their scales, the bias and the grouped offsets, which
-// are written before the layer's first kernel.
+// must be complete before the layer's first kernel may start.
 // Every wait is bounded (4 s by default); a timeout sets g_gemm_error, every role
 // unwinds, in-flight copies and MMAs are drained (again bounded), TMEM is
 // freed and the kernel returns.
