@@ -11,8 +11,9 @@ call reads them from HBM (copies x bytes >= 4x L2), and the K steps run as
 replays of CUDA graphs of back-to-back calls.
 
 Also reported on the same line:
-  e2e           the same metric through the public Python API with host
-                buffers: pinned H2D copy of x, the call, D2H copy of y, each step;
+  e2e           the same metric through the host-buffer call (mxfp8_linear_host
+                via its Python binding): each step copies x in from pinned host
+                memory, runs the layer and copies y back to pinned host memory;
   roofline      the dominant kernel (the GEMM) against measured HBM bandwidth;
   cpu_baseline  the CPU oracle (plain C, one core) on a bounded sample;
   configs       every workload of the layer (tiny, decode M=1/16, mid, prefill
@@ -610,26 +611,24 @@ def main():
 
 
 def measure_e2e(mx, setup, steps):
-    """Per step: pinned-host x -> device, mxfp8_linear, y -> pinned host."""
+    """Per step: one mxfp8_linear_host call on page-locked host buffers, which
+    enqueues the copy of x in, the layer and the copy of y out."""
     import torch
     d = setup.d
     xh = [torch.from_numpy(d.x).to(torch.bfloat16).pin_memory() for _ in range(2)]
     yh = torch.empty((d.m, d.n), dtype=torch.bfloat16).pin_memory()
-    xd = torch.empty((d.m, d.k), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty((mx.linear_host_workspace_bytes(d.m, d.n, d.k),), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
     pws = setup.pws
     b = setup.bias
     for i in range(10):
-        xd.copy_(xh[i % 2], non_blocking=True)
-        y = mx.linear(xd, pws[i % len(pws)], b, workspace=setup.ws)
-        yh.copy_(y, non_blocking=True)
+        mx.linear_host(xh[i % 2], pws[i % len(pws)], b, y_host=yh, workspace=ws, stream=stream)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record()
     for i in range(steps):
-        xd.copy_(xh[i % 2], non_blocking=True)
-        y = mx.linear(xd, pws[i % len(pws)], b, workspace=setup.ws)
-        yh.copy_(y, non_blocking=True)
+        mx.linear_host(xh[i % 2], pws[i % len(pws)], b, y_host=yh, workspace=ws, stream=stream)
     e1.record()
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1)
@@ -637,7 +636,7 @@ def measure_e2e(mx, setup, steps):
     return {"value": steps * wb / (ms * 1e-3) / 1e9, "unit": "GB/s",
             "h2d_bytes_per_step": d.m * d.k * 2, "d2h_bytes_per_step": d.m * d.n * 2,
             "us_per_step": ms * 1e3 / steps, "steps": steps,
-            "note": "eager Python API calls (host launch overhead included)"}
+            "note": "eager mxfp8_linear_host calls from Python (host launch overhead included)"}
 
 
 def load_traffic(kernel, workload):

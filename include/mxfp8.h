@@ -161,6 +161,23 @@ mxfp8_status mxfp8_grouped_linear(const void* x_sorted, int64_t rows,
                                   void* y, void* workspace,
                                   size_t workspace_bytes, void* stream);
 
+/* ------------------------------------------------ host activations/output
+ * The pages' layer reads and writes device tensors; this entry point serves
+ * a caller whose activations and results live in host memory.  It enqueues,
+ * on `stream`, the copy of x_host (bfloat16 [m][k], row-major) into the
+ * workspace, the layer exactly as mxfp8_linear computes it, and the copy of
+ * y (bfloat16 [m][n]) back to y_host.  It returns once that work is
+ * enqueued: y_host holds the result after the stream has completed it.
+ * Page-locked host buffers keep both copies asynchronous; pageable ones
+ * work, the copies then block the calling thread.  w (dense only) and bias
+ * stay on the device.  workspace: device, >=
+ * mxfp8_linear_host_workspace_bytes(m, n, k), 16-B aligned; its contents
+ * are scratch.  m = 0 enqueues nothing. */
+size_t mxfp8_linear_host_workspace_bytes(int64_t m, int64_t n, int64_t k);
+mxfp8_status mxfp8_linear_host(const void* x_host, int64_t m, const mxfp8_weight* w,
+                               const void* bias, void* y_host, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
 /* ------------------------------------------------ scratch-free variant
  * The pages have no counterpart to this entry point; it exists for callers
  * that cannot allocate device memory, so cannot hand mxfp8_linear a

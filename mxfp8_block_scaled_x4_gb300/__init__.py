@@ -20,7 +20,7 @@ import torch
 
 __all__ = [
     "Mxfp8Error", "PreparedWeight", "prepare_weight", "quantize_act", "gemm",
-    "linear", "grouped_linear", "act_scale_bytes", "weight_bytes",
+    "linear", "linear_host", "linear_host_workspace_bytes", "grouped_linear", "act_scale_bytes", "weight_bytes",
     "weight_scale_bytes", "linear_workspace_bytes", "set_schedule",
     "device_error", "library", "library_path",
 ]
@@ -86,6 +86,8 @@ def library():
         "mxfp8_gemm": (ctypes.c_int, [vp, vp, i64, W, vp, vp, vp]),
         "mxfp8_linear": (ctypes.c_int, [vp, i64, W, vp, vp, vp, sz, vp]),
         "mxfp8_grouped_linear": (ctypes.c_int, [vp, i64, vp, W, vp, vp, vp, sz, vp]),
+        "mxfp8_linear_host_workspace_bytes": (sz, [i64, i64, i64]),
+        "mxfp8_linear_host": (ctypes.c_int, [vp, i64, W, vp, vp, vp, sz, vp]),
         "mxfp8_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "mxfp8_last_cuda_error": (ctypes.c_int, []),
         "mxfp8_device_error": (ctypes.c_int, []),
@@ -252,6 +254,38 @@ def linear(x: torch.Tensor, pw: PreparedWeight, bias=None, workspace=None) -> to
     _check(library().mxfp8_linear(_ptr(x2), m, ctypes.byref(pw.c), _ptr(bias), _ptr(y),
                                   _ptr(workspace), workspace.numel(), _stream(x)), "mxfp8_linear")
     return y.reshape(*lead, pw.n)
+
+
+def linear_host_workspace_bytes(m: int, n: int, k: int) -> int:
+    return library().mxfp8_linear_host_workspace_bytes(m, n, k)
+
+
+def linear_host(x_host: torch.Tensor, pw: PreparedWeight, bias=None, y_host=None, workspace=None,
+                stream=None) -> torch.Tensor:
+    """The layer on host buffers: bf16 CPU x [m, k] -> bf16 CPU y [m, n].
+    One library call enqueues the copy in, the layer and the copy out on
+    `stream` (default: the current stream); y_host is valid after that
+    stream has synchronised.  Pass page-locked tensors (pin_memory()) to
+    keep the copies asynchronous."""
+    _need(not x_host.is_cuda and x_host.dtype == torch.bfloat16 and x_host.is_contiguous(),
+          "x_host must be a contiguous bfloat16 CPU tensor")
+    _need(x_host.dim() == 2 and x_host.shape[1] == pw.k, "x_host must be [m, k]")
+    m = x_host.shape[0]
+    if y_host is None:
+        y_host = torch.empty((m, pw.n), dtype=torch.bfloat16, pin_memory=x_host.is_pinned())
+    _need(not y_host.is_cuda and y_host.dtype == torch.bfloat16 and y_host.is_contiguous()
+          and tuple(y_host.shape) == (m, pw.n), "y_host must be a contiguous bfloat16 CPU tensor [m, n]")
+    if bias is not None:
+        _need(bias.is_cuda and bias.dtype == torch.bfloat16 and bias.numel() == pw.n, "bias must be bf16 CUDA [n]")
+    if workspace is None:
+        workspace = torch.empty((max(linear_host_workspace_bytes(m, pw.n, pw.k), 16),), dtype=torch.uint8,
+                                device="cuda")
+    if stream is None:
+        stream = torch.cuda.current_stream(workspace.device)
+    _check(library().mxfp8_linear_host(_ptr(x_host), m, ctypes.byref(pw.c), _ptr(bias), _ptr(y_host),
+                                       _ptr(workspace), workspace.numel(), ctypes.c_void_p(stream.cuda_stream)),
+           "mxfp8_linear_host")
+    return y_host
 
 
 def grouped_linear(x_sorted: torch.Tensor, offsets: torch.Tensor, pw: PreparedWeight,

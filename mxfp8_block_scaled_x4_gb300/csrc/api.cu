@@ -245,6 +245,35 @@ mxfp8_status mxfp8_grouped_linear(const void* x_sorted, int64_t rows, const int3
     return linear_common(x_sorted, rows, expert_offsets, w, bias, y, workspace, workspace_bytes, stream);
 }
 
+// -------------------------------------------------- host activations/output
+size_t mxfp8_linear_host_workspace_bytes(int64_t m, int64_t n, int64_t k) {
+    if (m < 0 || n < 1 || k <= 0 || k % 32 != 0) return 0;
+    return static_cast<size_t>(ceil_to(m * k * 2, 256) + ceil_to(m * n * 2, 256)) +
+           mxfp8_linear_workspace_bytes(m, k);
+}
+
+mxfp8_status mxfp8_linear_host(const void* x_host, int64_t m, const mxfp8_weight* w, const void* bias,
+                               void* y_host, void* workspace, size_t workspace_bytes, void* stream) {
+    mxfp8_status st = check_weight(w);
+    if (st != MXFP8_OK) return st;
+    if (w->num_experts != 1 || m < 0 || m > kMaxRows) return MXFP8_ERR_INVALID_ARG;
+    if (m == 0) return MXFP8_OK;
+    if (!x_host || !y_host || !workspace) return MXFP8_ERR_INVALID_ARG;
+    if (!aligned16(workspace)) return MXFP8_ERR_MISALIGNED;
+    if (workspace_bytes < mxfp8_linear_host_workspace_bytes(m, w->n, w->k)) return MXFP8_ERR_WORKSPACE_TOO_SMALL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* xd = static_cast<uint8_t*>(workspace);
+    uint8_t* yd = xd + ceil_to(m * w->k * 2, 256);
+    uint8_t* ws = yd + ceil_to(m * w->n * 2, 256);
+    const size_t x_bytes = static_cast<size_t>(m * w->k * 2), y_bytes = static_cast<size_t>(m * w->n * 2);
+    cudaError_t e = cudaMemcpyAsync(xd, x_host, x_bytes, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    st = linear_common(xd, m, nullptr, w, bias, yd, ws, mxfp8_linear_workspace_bytes(m, w->k), stream);
+    if (st != MXFP8_OK) return st;
+    e = cudaMemcpyAsync(y_host, yd, y_bytes, cudaMemcpyDeviceToHost, s);
+    return e == cudaSuccess ? MXFP8_OK : cuda_fail(e);
+}
+
 // -------------------------------------------------- 128x4 activation scales
 size_t mxfp8_act_scale_bytes_128x4(int64_t m, int64_t k) {
     if (m < 0 || k <= 0 || k % 128 != 0) return 0;

@@ -109,11 +109,20 @@ def test_argument_errors_before_launch(mx):
     assert lib.mxfp8_linear(A, 4, wp, None, A + 1, A, 1 << 20, None) == 3
     assert lib.mxfp8_linear(A, 4, wp, None, A, A, 16, None) == 5
     assert lib.mxfp8_linear(A, 4, None, None, A, A, 1 << 20, None) == 1
+    # host-buffer linear: sizes, M = 0 no-op, null / misaligned / small workspace
+    assert lib.mxfp8_linear_host_workspace_bytes(4, 130, 256) == 2048 + 1280 + 1024 + 64
+    assert lib.mxfp8_linear_host_workspace_bytes(4, 0, 256) == 0
+    assert lib.mxfp8_linear_host(A, 0, wp, None, A, A, 0, None) == 0
+    assert lib.mxfp8_linear_host(None, 4, wp, None, A, A, 1 << 20, None) == 1
+    assert lib.mxfp8_linear_host(A, 4, wp, None, None, A, 1 << 20, None) == 1
+    assert lib.mxfp8_linear_host(A, 4, wp, None, A, A + 8, 1 << 20, None) == 3
+    assert lib.mxfp8_linear_host(A, 4, wp, None, A, A, 4415, None) == 5
     # gemm: dense only
     st2, w2 = _view(mx, 2, 128, 256, A, A)
     assert st2 == 0
     assert lib.mxfp8_gemm(A, A, 4, ctypes.byref(w2), None, A, None) == 1
     assert lib.mxfp8_linear(A, 4, ctypes.byref(w2), None, A, A, 1 << 20, None) == 1
+    assert lib.mxfp8_linear_host(A, 4, ctypes.byref(w2), None, A, A, 1 << 20, None) == 1
     # grouped: offsets required
     assert lib.mxfp8_grouped_linear(A, 4, None, ctypes.byref(w2), None, A, A, 1 << 20, None) == 1
     assert lib.mxfp8_grouped_linear(A, 0, A, ctypes.byref(w2), None, A, A, 1 << 20, None) == 0

@@ -201,3 +201,27 @@ def test_leading_dims_and_m0(lib):
 
 def test_no_device_timeout_recorded(lib):
     assert lib.device_error() == 0
+
+
+@pytest.mark.parametrize("pinned", [True, False])
+@pytest.mark.parametrize("mk", ["decode", "mid"])
+def test_linear_host_buffers(lib, mk, pinned):
+    """mxfp8_linear_host: host x in, host y out, one call; the result is the
+    device call's, bit for bit, and within the oracle tolerance."""
+    d = workloads.decode(m=16) if mk == "decode" else workloads.mid(n=130, bias=True)
+    pw = lib.prepare_weight(to_dev_f32(d.w))
+    b = None if d.bias is None else to_dev_bf16(d.bias)
+    xh = torch.from_numpy(d.x).to(torch.bfloat16)
+    if pinned:
+        xh = xh.pin_memory()
+    yh = torch.full((d.m, d.n), float("nan"), dtype=torch.bfloat16)
+    if pinned:
+        yh = yh.pin_memory()
+    out = lib.linear_host(xh, pw, b, y_host=yh)
+    torch.cuda.synchronize()
+    assert out is yh
+    y_dev = lib.linear(xh.cuda(), pw, b)
+    torch.cuda.synchronize()
+    assert torch.equal(yh.view(torch.int16), y_dev.cpu().view(torch.int16))
+    wq, wsf = oracle_weight(d.w)
+    assert_close_to_oracle(yh, oracle.linear(d.x, wq, wsf, d.bias), d.name + "_host")
