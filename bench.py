@@ -14,6 +14,7 @@ Also reported on the same line:
   e2e           the same metric through the host-buffer call (mxfp8_linear_host
                 via its Python binding): each step copies x in from pinned host
                 memory, runs the layer and copies y back to pinned host memory;
+                steps alternate over two streams (two requests in flight);
   roofline      the dominant kernel (the GEMM) against measured HBM bandwidth;
   cpu_baseline  the CPU oracle (plain C, one core) on a bounded sample;
   configs       every workload of the layer (tiny, decode M=1/16, mid, prefill
@@ -612,31 +613,50 @@ def main():
 
 def measure_e2e(mx, setup, steps):
     """Per step: one mxfp8_linear_host call on page-locked host buffers, which
-    enqueues the copy of x in, the layer and the copy of y out."""
+    enqueues the copy of x in, the layer and the copy of y out.  Steps
+    alternate over two streams, each with its own workspace and host output
+    (two independent requests in flight, so one request's copies overlap the
+    other's kernel); the single-stream time is reported beside it."""
     import torch
     d = setup.d
     xh = [torch.from_numpy(d.x).to(torch.bfloat16).pin_memory() for _ in range(2)]
-    yh = torch.empty((d.m, d.n), dtype=torch.bfloat16).pin_memory()
-    ws = torch.empty((mx.linear_host_workspace_bytes(d.m, d.n, d.k),), dtype=torch.uint8, device="cuda")
-    stream = torch.cuda.current_stream()
+    yh = [torch.empty((d.m, d.n), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    ws = [torch.empty((mx.linear_host_workspace_bytes(d.m, d.n, d.k),), dtype=torch.uint8, device="cuda")
+          for _ in range(2)]
+    s0 = torch.cuda.current_stream()
+    s1 = torch.cuda.Stream()
     pws = setup.pws
     b = setup.bias
-    for i in range(10):
-        mx.linear_host(xh[i % 2], pws[i % len(pws)], b, y_host=yh, workspace=ws, stream=stream)
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for i in range(steps):
-        mx.linear_host(xh[i % 2], pws[i % len(pws)], b, y_host=yh, workspace=ws, stream=stream)
-    e1.record()
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1)
+
+    def run(nstreams, n):
+        streams = [s0, s1][:nstreams]
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(s0)
+        s1.wait_event(e0)
+        for i in range(n):
+            j = i % nstreams
+            mx.linear_host(xh[i % 2], pws[i % len(pws)], b, y_host=yh[j], workspace=ws[j], stream=streams[j])
+        if nstreams > 1:
+            done = torch.cuda.Event()
+            done.record(s1)
+            s0.wait_event(done)
+        e1.record(s0)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
+    run(2, 10)
+    run(1, 10)
+    ms = run(2, steps)
+    ms1 = run(1, steps)
     wb = weight_bytes(d.n, d.k)
     return {"value": steps * wb / (ms * 1e-3) / 1e9, "unit": "GB/s",
             "h2d_bytes_per_step": d.m * d.k * 2, "d2h_bytes_per_step": d.m * d.n * 2,
             "us_per_step": ms * 1e3 / steps, "steps": steps,
-            "note": "eager mxfp8_linear_host calls from Python (host launch overhead included)"}
+            "single_stream_us_per_step": ms1 * 1e3 / steps,
+            "note": "eager mxfp8_linear_host calls from Python, two streams in turn "
+                    "(host launch overhead included)"}
 
 
 def load_traffic(kernel, workload):

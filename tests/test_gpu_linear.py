@@ -150,6 +150,20 @@ def test_ragged_shapes(lib, m, n, k):
     _run_dense(lib, workloads.dense(m=m, n=n, k=k, seed=m + n + k, bias=(m % 2 == 1)))
 
 
+@pytest.mark.parametrize("m,n,k,schedule", [
+    (16, 1000, 16384, (0, 0, -1)),   # built-in choice: split-K clusters, fused quantization
+    (16, 1000, 16384, (16, 1, 1)),   # one CTA walks all 128 K blocks: every stage reused many times
+    (64, 520, 16384, (64, 2, 1)),    # 64-token tiles, fused, 64 K blocks per CTA
+    (200, 260, 16384, (0, 0, -1)),   # persistent tiles, separate quantizer
+    (8, 40960, 2048, (0, 0, -1)),    # 320 weight tiles: several waves of clusters
+])
+def test_long_k_and_wide_n(lib, m, n, k, schedule):
+    """Long K (the fused quantizer refills pipeline stages the MMA has
+    released) and wide N (more clusters than fit on the GPU at once), with
+    ragged N and bias."""
+    _run_dense(lib, workloads.dense(m=m, n=n, k=k, seed=m + n + k, bias=True), schedule=schedule)
+
+
 def test_gemm_matches_linear_bitwise(lib):
     d = workloads.dense(m=77, n=520, k=512, seed=31)
     pw = lib.prepare_weight(to_dev_f32(d.w))
