@@ -169,7 +169,8 @@ mxfp8_status mxfp8_grouped_linear(const void* x_sorted, int64_t rows,
  * y (bfloat16 [m][n]) back to y_host.  It returns once that work is
  * enqueued: y_host holds the result after the stream has completed it.
  * Page-locked host buffers keep both copies asynchronous; pageable ones
- * work, the copies then block the calling thread.  w (dense only) and bias
+ * work, the copies then block the calling thread, and the call cannot be
+ * captured in a CUDA graph.  w (dense only) and bias
  * stay on the device.  workspace: device, >=
  * mxfp8_linear_host_workspace_bytes(m, n, k), 16-B aligned; its contents
  * are scratch.  m = 0 enqueues nothing. */
