@@ -443,12 +443,11 @@ __device__ __forceinline__ void run_fused_quant(const GemmArgs& p, const Ctx& c,
                 for (int v = 0; v < 4; ++v) raw[u][v] = src[v];
             }
         }
-        // Quantize the whole batch first (independent register math that
-        // interleaves), then publish it.
+        // The batch's loads are all in flight; each patch is then quantized
+        // and published on its own, so the MMA of the first K blocks starts
+        // while the later patches are still being quantized.
         uint32_t qq[kBatch][8];
         uint32_t sc[kBatch];
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) sc[u] = quantize_block32(raw[u], qq[u]);
         auto store_patch = [&](int u, int ps) {
             const int i = ps / kPatches;
             const int row = (ps - i * kPatches) * 8 + r8;
@@ -469,22 +468,24 @@ __device__ __forceinline__ void run_fused_quant(const GemmArgs& p, const Ctx& c,
             return &c.full[(i % PIPES) * S + (i / PIPES) % S];
         };
         // A patch whose stage is in use again must wait for the MMA to free
-        // it, and that MMA may need an earlier patch of this very batch: such
-        // batches publish patch by patch.  Otherwise one proxy fence covers
-        // the batch.
+        // it, and that MMA may need an earlier patch of this very batch, so
+        // such batches quantize everything first and then wait, store and
+        // publish patch by patch.
         const bool reuse = (p0 + (kBatch - 1) * kEpi) / kPatches / PIPES >= S;
         if (!reuse) {
 #pragma unroll
-            for (int u = 0; u < kBatch; ++u)
-                if (p0 + u * kEpi < total) store_patch(u, p0 + u * kEpi);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-#pragma unroll
-                for (int u = 0; u < kBatch; ++u)
-                    if (p0 + u * kEpi < total) mbar_arrive(full_of(p0 + u * kEpi));
+            for (int u = 0; u < kBatch; ++u) {
+                if (p0 + u * kEpi < total) {
+                    sc[u] = quantize_block32(raw[u], qq[u]);
+                    store_patch(u, p0 + u * kEpi);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(full_of(p0 + u * kEpi));
+                }
             }
         } else {
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) sc[u] = quantize_block32(raw[u], qq[u]);
 #pragma unroll
             for (int u = 0; u < kBatch; ++u) {
                 const int ps = p0 + u * kEpi;
