@@ -1,0 +1,37 @@
+"""Host arithmetic of bench.py's step roofline (no GPU): algorithmic bytes
+per launch for the decode workload M=16, N=5120, K=2048 with bias, for the
+fused schedule (one launch per step) and the unfused one."""
+import os
+import sys
+import types
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+D = types.SimpleNamespace(m=16, n=5120, k=2048)
+WB = 5120 * 2048 + 5120 * 2048 // 32      # E4M3 weights + E8M0 scales
+ACT_SF = 16 * 2048 // 32                   # 8x4 scales of 16 rows
+
+
+def test_weight_bytes_helper():
+    assert bench.weight_bytes(5120, 2048) == WB == 10_813_440
+
+
+def test_fused_step_is_the_dominant_launch():
+    r = bench.step_roofline(D, WB, 1, 0.005, 0.004, 6800.0, None, ACT_SF)
+    nbytes = 2 * 16 * 2048 + WB + 2 * 5120 + 2 * 16 * 5120
+    assert r["alg_bytes_per_launch"] == nbytes == 11_053_056
+    assert abs(r["us_per_launch"] - 5.0) < 1e-9
+    assert abs(r["achieved"] - nbytes / 5e-6 / 1e9) < 1e-6
+    assert abs(r["frac"] - r["achieved"] / 6800.0) < 1e-12
+    g = r["gemm_prequantized_alone"]
+    assert g["alg_bytes_per_launch"] == 11_021_312 and abs(g["us_per_launch"] - 4.0) < 1e-9
+
+
+def test_unfused_step_reports_the_gemm():
+    r = bench.step_roofline(D, WB, 2, 0.005, 0.004, 6800.0, 123.0, ACT_SF)
+    assert r["alg_bytes_per_launch"] == 11_021_312
+    assert abs(r["us_per_launch"] - 4.0) < 1e-9
+    assert r["traffic"] == 123.0 and r["bound"] == "hbm" and r["unit"] == "GB/s"
