@@ -363,6 +363,26 @@ def test_prepare_weight_composes_quantize_and_layout():
     assert (q_pad == q2).all() and (sf_t == sf2).all()
 
 
+def test_act_128x4_places_each_rows_scales_in_the_weight_tiling():
+    """The 128x4 activation scales: byte offset_w128x4(r, b) holds row r's
+    block-b scale, the quantized bytes equal the 8x4 path's, and rows
+    m .. ceil128(m)-1 hold 0x00."""
+    rng = np.random.default_rng(17)
+    m, k = 130, 512
+    kb = k // 32
+    x = rng.standard_normal((m, k)).astype(np.float32)
+    x[5, 32:64] = 0.0
+    q, sf_t = oracle.quantize_act_128x4(x)
+    q8, _ = oracle.quantize_act(x)
+    _, sf_lin = oracle.quantize_rows(x)
+    assert (q == q8).all() and sf_t.size == 256 * kb
+    for r in range(m):
+        for b in range(kb):
+            assert sf_t[oracle.offset_w128x4(r, b, kb)] == sf_lin[r, b]
+    assert sf_t[oracle.offset_w128x4(5, 1, kb)] == 0
+    assert not any(sf_t[oracle.offset_w128x4(r, b, kb)] for r in range(m, 256) for b in range(kb))
+
+
 def test_tolerance_helper():
     y_ref = np.array([1.0, -2.0, 0.0, 100.0])
     ok, _ = oracle.within_tolerance(y_ref * (1 + 7e-3), y_ref)
