@@ -10,6 +10,8 @@
 #include <stdint.h>
 #include <stdlib.h>
 
+#include <atomic>
+
 #include "../../include/mxfp8.h"
 #include "../../include/mxfp8_moe.h"
 #include "internal.h"
@@ -17,15 +19,17 @@
 namespace {
 
 thread_local int t_last_cuda_error = 0;
-int g_force_tt = 0;
-int g_force_split = 0;
-int g_force_fuse = -1;
+// Testing hooks (mxfp8_set_schedule), read by every call on any thread.
+std::atomic<int> g_force_tt{0};
+std::atomic<int> g_force_split{0};
+std::atomic<int> g_force_fuse{-1};
 
+// Per-device capability cache, filled by whichever thread calls first.
 struct DeviceInfo {
-    int checked;  // 0 unknown, 1 supported, -1 unsupported
-    int sms;
+    std::atomic<int> checked;  // 0 unknown, 1 supported, -1 unsupported
+    std::atomic<int> sms;
 };
-DeviceInfo g_dev[64];
+DeviceInfo g_dev[64];  // static storage: starts zeroed
 
 mxfp8_status cuda_fail(cudaError_t e) {
     t_last_cuda_error = static_cast<int>(e);
@@ -39,17 +43,19 @@ mxfp8_status device_sms(int* sms) {
     if (e != cudaSuccess) return cuda_fail(e);
     if (dev < 0 || dev >= 64) return MXFP8_ERR_UNSUPPORTED_DEVICE;
     DeviceInfo& d = g_dev[dev];
-    if (d.checked == 0) {
+    int checked = d.checked.load(std::memory_order_acquire);
+    if (checked == 0) {  // racing first calls write the same values
         int major = 0, minor = 0, count = 0;
         if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
             (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
             (e = cudaDeviceGetAttribute(&count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
             return cuda_fail(e);
-        d.sms = count;
-        d.checked = (major == 10 && minor == 3) ? 1 : -1;
+        d.sms.store(count, std::memory_order_relaxed);
+        checked = (major == 10 && minor == 3) ? 1 : -1;
+        d.checked.store(checked, std::memory_order_release);
     }
-    if (d.checked < 0) return MXFP8_ERR_UNSUPPORTED_DEVICE;
-    *sms = d.sms;
+    if (checked < 0) return MXFP8_ERR_UNSUPPORTED_DEVICE;
+    *sms = d.sms.load(std::memory_order_relaxed);
     return MXFP8_OK;
 }
 
@@ -166,8 +172,10 @@ thread_local const mxk::GemmSchedule* t_override = nullptr;
 // set, else the tactic table, else the built-in heuristic.
 static mxk::GemmSchedule select_schedule(const mxk::GemmProblem& p, int sms, int kind) {
     if (t_override) return *t_override;
-    if (g_force_tt != 0 || g_force_split != 0 || g_force_fuse != -1)
-        return mxk::choose_schedule(p, sms, g_force_tt, g_force_split, g_force_fuse);
+    const int ftt = g_force_tt.load(std::memory_order_relaxed);
+    const int fsplit = g_force_split.load(std::memory_order_relaxed);
+    const int ffuse = g_force_fuse.load(std::memory_order_relaxed);
+    if (ftt != 0 || fsplit != 0 || ffuse != -1) return mxk::choose_schedule(p, sms, ftt, fsplit, ffuse);
     int dev = 0;
     mxk::GemmSchedule s;
     if (cudaGetDevice(&dev) == cudaSuccess && mxk::tactic_lookup(dev, kind, p.m, p.n, p.k, p.experts, &s)) {
@@ -665,9 +673,9 @@ void mxfp8_set_schedule(int tokens_per_tile, int split_k, int fuse_quant) {
     const bool tt_ok = tokens_per_tile == 0 || tokens_per_tile == 16 || tokens_per_tile == 32 ||
                        tokens_per_tile == 64 || tokens_per_tile == 128 || tokens_per_tile == 256 ||
                        tokens_per_tile == 160 || tokens_per_tile == 192;
-    g_force_tt = tt_ok ? tokens_per_tile : 0;
-    g_force_split = (split_k >= -1 && split_k <= 8) ? split_k : 0;
-    g_force_fuse = (fuse_quant >= -1 && fuse_quant <= 1) ? fuse_quant : -1;
+    g_force_tt.store(tt_ok ? tokens_per_tile : 0, std::memory_order_relaxed);
+    g_force_split.store((split_k >= -1 && split_k <= 8) ? split_k : 0, std::memory_order_relaxed);
+    g_force_fuse.store((fuse_quant >= -1 && fuse_quant <= 1) ? fuse_quant : -1, std::memory_order_relaxed);
 }
 
 }  // extern "C"
