@@ -75,7 +75,12 @@ size_t mxfp8_moe_gate_up_workspace_bytes(int64_t rows, int64_t k);
  * where [gate_r; up_r] = GEMM1 of expert e (off[e] <= r < off[e+1]) applied
  * to the MXFP8-quantized token row x[sorted_token[r]].
  * x: bfloat16 [tokens][k]; w13: prepared by mxfp8_prepare_gate_up_weight;
- * h: bfloat16 [rows][I] (I = w13->n / 2). */
+ * h: bfloat16 [rows][I] (I = w13->n / 2).
+ * sorted_token (int32 [rows]) and expert_offsets (int32 [E + 1]) are read
+ * on the device and not checked: every sorted_token value must lie in
+ * [0, tokens), and the offsets must follow mxfp8_grouped_linear's rules,
+ * including its ordering rule (mxfp8_moe_route's outputs satisfy both).
+ * ws: >= mxfp8_moe_gate_up_workspace_bytes(rows, k), 16-B aligned. */
 mxfp8_status mxfp8_moe_gate_up_swiglu(const void* x, const int32_t* sorted_token, int64_t rows,
                                       const int32_t* expert_offsets, const mxfp8_weight* w13, void* h,
                                       void* ws, size_t ws_bytes, void* stream);
@@ -83,7 +88,8 @@ mxfp8_status mxfp8_moe_gate_up_swiglu(const void* x, const int32_t* sorted_token
 /* Step 4: out[t][c] = bf16( sum_{s < topk} topk_weights[t][s] *
  * y2[row_of[t*topk + s]][c] ), summed in FP32 in slot order.
  * y2: bfloat16 [tokens*topk][hidden]; out: bfloat16 [tokens][hidden];
- * hidden % 8 == 0; y2 and out 16-byte aligned. */
+ * hidden % 8 == 0; y2 and out 16-byte aligned.  row_of values are read on
+ * the device and not checked: each must lie in [0, tokens*topk). */
 mxfp8_status mxfp8_moe_finalize(const void* y2, const int32_t* row_of, const float* topk_weights,
                                 int64_t tokens, int64_t topk, int64_t hidden, void* out, void* stream);
 
