@@ -138,6 +138,11 @@ def _check(status, where):
 
 
 def _stream(t: torch.Tensor):
+    """The current stream of t's device.  The library launches on the
+    current CUDA device, so t must live there."""
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError("tensor on %s but the current CUDA device is cuda:%d (use torch.cuda.device)"
+                         % (t.device, torch.cuda.current_device()))
     return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
 
 
@@ -280,6 +285,8 @@ def linear_host(x_host: torch.Tensor, pw: PreparedWeight, bias=None, y_host=None
     if workspace is None:
         workspace = torch.empty((max(linear_host_workspace_bytes(m, pw.n, pw.k), 16),), dtype=torch.uint8,
                                 device="cuda")
+    _need(workspace.is_cuda and workspace.device.index == torch.cuda.current_device(),
+          "workspace must be on the current CUDA device")
     if stream is None:
         stream = torch.cuda.current_stream(workspace.device)
     _check(library().mxfp8_linear_host(_ptr(x_host), m, ctypes.byref(pw.c), _ptr(bias), _ptr(y_host),
