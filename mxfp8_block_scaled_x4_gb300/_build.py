@@ -37,7 +37,8 @@ def build(force=False, verbose=False):
     os.makedirs(OBJ, exist_ok=True)
     os.makedirs(LIBDIR, exist_ok=True)
     nvcc = _nvcc()
-    hdrs = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(ROOT, "include", "mxfp8.h")]
+    hdrs = [os.path.join(CSRC, h) for h in HEADERS] + \
+        [os.path.join(ROOT, "include", h) for h in ("mxfp8.h", "mxfp8_moe.h")]
     jobs = []
     objs = []
     for src in SOURCES:
