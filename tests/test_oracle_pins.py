@@ -123,6 +123,40 @@ def test_e4m3_round_matches_ml_dtypes():
     assert (oracle.e4m3_round(v) == ref).all()
 
 
+def test_e4m3_round_is_monotone():
+    """Rounding to a grid is monotone: a larger input never decodes smaller
+    (decoded by torch; -0 and +0 compare equal)."""
+    rng = np.random.default_rng(321)
+    _, grid = _e4m3_grid()
+    g = grid[np.isfinite(grid)]
+    t = np.concatenate([rng.uniform(-470.0, 470.0, 100000),
+                        rng.standard_normal(50000) * 2.0 ** -7, g, (g[:-1] + g[1:]) / 2])
+    t = np.sort(t)
+    vals = _lib_decode(oracle.e4m3_round(t))
+    assert (np.diff(vals) >= 0).all()
+
+
+def test_quantization_error_within_half_an_e4m3_step():
+    """The format's error bound, per element of random blocks spanning 60
+    binades: with s = 2^(scale byte - 127) and t = |v|/s, an element that does
+    not saturate (t <= 448) decodes within half the E4M3 spacing at t, times
+    s (spacing 2^(floor(log2 t) - 3) for t >= 2^-6, 2^-9 below); one that
+    does decodes to 448*s with v's sign."""
+    rng = np.random.default_rng(77)
+    x = (rng.standard_normal((64, 256)) * np.exp2(rng.integers(-30, 30, (64, 1)))).astype(np.float32)
+    x[3, 32:64] *= 1.9  # more saturating blocks
+    q, sf = oracle.quantize_rows(x)
+    deq = _lib_dequant(q, sf)
+    v = x.astype(np.float64)
+    s = np.repeat(np.exp2(sf.astype(np.float64) - 127.0), 32, axis=1)
+    t = np.abs(v) / s
+    spacing = np.where(t >= 2.0 ** -6, np.exp2(np.floor(np.log2(np.maximum(t, 2.0 ** -6))) - 3), 2.0 ** -9)
+    sat = t > 448.0
+    assert sat.any() and (~sat).any()
+    assert (np.abs(deq - v)[~sat] <= (spacing * s / 2)[~sat]).all()
+    assert (deq[sat] == np.sign(v[sat]) * 448.0 * s[sat]).all()
+
+
 def test_e4m3_round_saturates():
     assert list(oracle.e4m3_round([448.0, 463.9, 464.0, 464.1, 500.0, 1e30, -1e30])) == \
         [0x7E, 0x7E, 0x7E, 0x7E, 0x7E, 0x7E, 0xFE]
