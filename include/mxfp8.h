@@ -276,6 +276,16 @@ mxfp8_status mxfp8_tactic_set(int kind, int64_t m, int64_t n, int64_t k, int64_t
                               const int32_t* tactic);
 void mxfp8_tactic_clear(void);
 int64_t mxfp8_tactic_count(void);
+/* The tactic a call of this kind and shape would run now, without launching
+ * anything: the table's entry for its class if there is one, else the
+ * built-in heuristic's choice (the testing hook of mxfp8_set_schedule, when
+ * set, wins as it does for calls).  m: activation rows (sorted rows for the
+ * grouped kinds); experts: 1 for the dense kinds; sms: the GPU's SM count,
+ * or <= 0 for the current device's (which then must be a GB300).  Writes the
+ * tactic encoding of mxfp8_tactic_get to tactic[4]; a dual weight-tile
+ * tactic reports 2 pipes.  Host only. */
+mxfp8_status mxfp8_plan_tactic(int kind, int64_t m, int64_t n, int64_t k, int64_t experts, int sms,
+                               int32_t* tactic);
 
 /* --------------------------------------------------------- status helpers */
 

@@ -107,6 +107,7 @@ def library():
         "mxfp8_tactic_get": (ctypes.c_int, [ctypes.c_int, i64, i64, i64, i64, vp]),
         "mxfp8_tactic_set": (ctypes.c_int, [ctypes.c_int, i64, i64, i64, i64, vp]),
         "mxfp8_tactic_clear": (None, []),
+        "mxfp8_plan_tactic": (ctypes.c_int, [ctypes.c_int, i64, i64, i64, i64, ctypes.c_int, vp]),
         "mxfp8_tactic_count": (i64, []),
         "mxfp8_moe_route_workspace_bytes": (sz, [i64, i64, i64]),
         "mxfp8_moe_route": (ctypes.c_int, [vp, i64, i64, i64, ctypes.c_int, vp, vp, vp, vp, vp, vp, sz, vp]),
@@ -407,6 +408,15 @@ def tactic_get(kind: int, m: int, n: int, k: int, experts: int = 1):
 
 def tactic_set(kind: int, m: int, n: int, k: int, experts: int, tactic) -> None:
     _check(library().mxfp8_tactic_set(kind, m, n, k, experts, _tactic_array(tactic)), "mxfp8_tactic_set")
+
+
+def plan_tactic(kind: int, m: int, n: int, k: int, experts: int = 1, sms: int = 0):
+    """The tactic (tokens_per_tile, split_k, fuse_quant, pipes) a call of
+    this kind and shape would run now: the table's entry, else the built-in
+    heuristic's choice.  sms <= 0 means the current device's SM count."""
+    out = (ctypes.c_int32 * 4)()
+    _check(library().mxfp8_plan_tactic(kind, m, n, k, experts, sms, out), "mxfp8_plan_tactic")
+    return tuple(out)
 
 
 def tactic_clear() -> None:

@@ -177,8 +177,9 @@ static mxk::GemmSchedule select_schedule(const mxk::GemmProblem& p, int sms, int
     const int ffuse = g_force_fuse.load(std::memory_order_relaxed);
     if (ftt != 0 || fsplit != 0 || ffuse != -1) return mxk::choose_schedule(p, sms, ftt, fsplit, ffuse);
     int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;  // as the table operations
     mxk::GemmSchedule s;
-    if (cudaGetDevice(&dev) == cudaSuccess && mxk::tactic_lookup(dev, kind, p.m, p.n, p.k, p.experts, &s)) {
+    if (mxk::tactic_lookup(dev, kind, p.m, p.n, p.k, p.experts, &s)) {
         if (s.fuse_quant && p.x == nullptr) s.fuse_quant = false;
         return s;
     }
@@ -358,7 +359,7 @@ void encode_tactic(const mxk::GemmSchedule& s, int32_t* t4) {
     t4[0] = s.tokens_per_tile;
     t4[1] = s.persistent ? -1 : s.split_k;
     t4[2] = s.fuse_quant ? 1 : 0;
-    t4[3] = s.pipes;
+    t4[3] = s.dual ? 2 : s.pipes;  // the dual kernel always runs two MMA issuers
 }
 bool decode_tactic(const int32_t* t4, int kind, int64_t k, mxk::GemmSchedule* s) {
     s->dual = (t4[0] == 192 || t4[0] == 160) && t4[1] == -1;
@@ -460,6 +461,36 @@ mxfp8_status mxfp8_tactic_set(int kind, int64_t m, int64_t n, int64_t k, int64_t
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;  // table operations need no device
     mxk::tactic_store(dev, kind, m, n, k, experts, s);
+    return MXFP8_OK;
+}
+
+mxfp8_status mxfp8_plan_tactic(int kind, int64_t m, int64_t n, int64_t k, int64_t experts, int sms,
+                               int32_t* tactic) {
+    const bool grouped = kind == mxk::kTacticGrouped || kind == mxk::kTacticGated;
+    if (!kind_ok(kind) || m < 1 || m > kMaxRows || n < 1 || k < 1 || k > kMaxK || experts < 1 ||
+        experts > 1024 || !tactic)
+        return MXFP8_ERR_INVALID_ARG;
+    if (k % 256 != 0) return MXFP8_ERR_K_NOT_MULTIPLE_OF_256;
+    if ((!grouped && experts != 1) || (kind == mxk::kTacticGated && n % 128 != 0))
+        return MXFP8_ERR_INVALID_ARG;
+    if (sms <= 0) {
+        mxfp8_status st = device_sms(&sms);
+        if (st != MXFP8_OK) return st;
+    }
+    // Only the presence of x (fusable quantization) and of offsets (grouped)
+    // matters to the choice; this marker is never dereferenced.
+    alignas(16) static const int32_t kPresent[4] = {0, 0, 0, 0};
+    mxk::GemmProblem p{};
+    p.m = m;
+    p.experts = experts;
+    p.n = n;
+    p.n_pad = ceil_to(n, 128);
+    p.k = k;
+    p.offsets = grouped ? kPresent : nullptr;
+    p.x = kind == mxk::kTacticLinear ? kPresent : nullptr;
+    p.gated = kind == mxk::kTacticGated;
+    p.sf128 = false;
+    encode_tactic(select_schedule(p, sms, kind), tactic);
     return MXFP8_OK;
 }
 

@@ -180,3 +180,53 @@ def test_tactic_table_host_operations(mx):
     assert mx.tactic_count() == 3
     mx.tactic_clear()
     assert mx.tactic_count() == 0
+
+
+def test_heuristic_schedules_on_the_workloads(mx):
+    """The built-in schedule rules on a 152-SM GB300, queried without a GPU:
+    (tokens per tile, split-K cluster or -1 = persistent, fused quantization,
+    MMA pipelines)."""
+    mx.tactic_clear()
+    L, G, GR, GA = mx.KIND_LINEAR, mx.KIND_GEMM, mx.KIND_GROUPED, mx.KIND_GATED
+    cases = [
+        # decode: 40 weight tiles x split 4 = 160 CTAs, quantization fused
+        ((L, 16, 5120, 2048, 1), (16, 4, 1, 2)),
+        ((L, 1, 5120, 2048, 1), (16, 4, 1, 2)),
+        # pre-quantized input: nothing to fuse
+        ((G, 16, 5120, 2048, 1), (16, 4, 0, 2)),
+        # mid batch: 64-token tiles, split 4, two pipes (128 CTAs <= 152)
+        ((L, 128, 2048, 4096, 1), (64, 4, 0, 2)),
+        ((L, 128, 130, 4096, 1), (64, 4, 0, 2)),
+        # tiny: K = 256 is two K blocks, so no split
+        ((L, 7, 130, 256, 1), (16, 1, 1, 2)),
+        # prefill: two weight tiles x 192 tokens, persistent
+        ((L, 8192, 8192, 8192, 1), (192, -1, 0, 2)),
+        # large M but too few tiles for the dual kernel: persistent 256
+        ((L, 1024, 256, 1024, 1), (256, -1, 0, 1)),
+        # grouped: mean segment 16 rows -> 32-token tiles, two pipes
+        ((GR, 2048, 1536, 2048, 128), (32, -1, 0, 2)),
+        ((GA, 2048, 1536, 2048, 128), (32, -1, 0, 2)),
+        # gated with long segments: capped at 128 tokens
+        ((GA, 12800, 1536, 2048, 128), (128, -1, 0, 1)),
+    ]
+    for args, want in cases:
+        assert mx.plan_tactic(*args, sms=152) == want, (args, mx.plan_tactic(*args, sms=152))
+    # a table entry takes precedence for its class only
+    mx.tactic_set(L, 16, 5120, 2048, 1, (64, 2, 0, 2))
+    assert mx.plan_tactic(L, 12, 5120, 2048, 1, sms=152) == (64, 2, 0, 2)
+    assert mx.plan_tactic(G, 16, 5120, 2048, 1, sms=152) == (16, 4, 0, 2)
+    mx.tactic_clear()
+    assert mx.plan_tactic(L, 12, 5120, 2048, 1, sms=152) == (16, 4, 1, 2)
+    # every heuristic choice is a valid tactic for its kind
+    for args, want in cases:
+        mx.tactic_set(args[0], args[1], args[2], args[3], args[4], want)
+    mx.tactic_clear()
+    # argument checks
+    lib = mx.library()
+    out = (ctypes.c_int32 * 4)()
+    assert lib.mxfp8_plan_tactic(9, 16, 5120, 2048, 1, 152, out) == 1        # unknown kind
+    assert lib.mxfp8_plan_tactic(L, 16, 5120, 2000, 1, 152, out) == 2        # K % 256
+    assert lib.mxfp8_plan_tactic(L, 16, 5120, 2048, 2, 152, out) == 1        # dense with experts
+    assert lib.mxfp8_plan_tactic(GA, 16, 1000, 2048, 4, 152, out) == 1       # gated n % 128
+    assert lib.mxfp8_plan_tactic(L, 0, 5120, 2048, 1, 152, out) == 1         # m < 1
+    assert lib.mxfp8_plan_tactic(L, 16, 5120, 2048, 1, 152, None) == 1
