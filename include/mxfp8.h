@@ -90,7 +90,9 @@ typedef struct mxfp8_weight {
 } mxfp8_weight;
 
 /* ------------------------------------------------------------ size helpers
- * Pure functions of the shape; return 0 for invalid shapes. */
+ * Pure functions of the shape; return 0 for invalid shapes, including
+ * shapes beyond the library's limits: at most 2^31 - 256 rows (M, or
+ * experts x N_pad), K <= 2^20. */
 
 /* Bytes of the 8x4 activation scale buffer: ceil(m/8)*8 * k/32. */
 size_t mxfp8_act_scale_bytes(int64_t m, int64_t k);

@@ -83,22 +83,22 @@ mxfp8_status check_weight(const mxfp8_weight* w) {
 extern "C" {
 
 size_t mxfp8_act_scale_bytes(int64_t m, int64_t k) {
-    if (m < 0 || k <= 0 || k % 32 != 0) return 0;
+    if (m < 0 || m > kMaxRows || k <= 0 || k > kMaxK || k % 32 != 0) return 0;
     return static_cast<size_t>(ceil_to(m, 8) * ceil_to(k / 32, 4));
 }
 
 size_t mxfp8_weight_bytes(int64_t n, int64_t k) {
-    if (n <= 0 || k <= 0) return 0;
+    if (n <= 0 || n > kMaxRows || k <= 0 || k > kMaxK) return 0;
     return static_cast<size_t>(ceil_to(n, 128) * k);
 }
 
 size_t mxfp8_weight_scale_bytes(int64_t n, int64_t k) {
-    if (n <= 0 || k <= 0 || k % 32 != 0) return 0;
+    if (n <= 0 || n > kMaxRows || k <= 0 || k > kMaxK || k % 32 != 0) return 0;
     return static_cast<size_t>(ceil_to(n, 128) * (k / 32));
 }
 
 size_t mxfp8_linear_workspace_bytes(int64_t m, int64_t k) {
-    if (m < 0 || k <= 0 || k % 32 != 0) return 0;
+    if (m < 0 || m > kMaxRows || k <= 0 || k > kMaxK || k % 32 != 0) return 0;
     return static_cast<size_t>(ceil_to(m * k, 256)) + mxfp8_act_scale_bytes(m, k);
 }
 
@@ -256,7 +256,7 @@ mxfp8_status mxfp8_grouped_linear(const void* x_sorted, int64_t rows, const int3
 
 // -------------------------------------------------- host activations/output
 size_t mxfp8_linear_host_workspace_bytes(int64_t m, int64_t n, int64_t k) {
-    if (m < 0 || n < 1 || k <= 0 || k % 32 != 0) return 0;
+    if (m < 0 || m > kMaxRows || n < 1 || n > kMaxRows || k <= 0 || k > kMaxK || k % 32 != 0) return 0;
     return static_cast<size_t>(ceil_to(m * k * 2, 256) + ceil_to(m * n * 2, 256)) +
            mxfp8_linear_workspace_bytes(m, k);
 }
@@ -285,12 +285,12 @@ mxfp8_status mxfp8_linear_host(const void* x_host, int64_t m, const mxfp8_weight
 
 // -------------------------------------------------- 128x4 activation scales
 size_t mxfp8_act_scale_bytes_128x4(int64_t m, int64_t k) {
-    if (m < 0 || k <= 0 || k % 128 != 0) return 0;
+    if (m < 0 || m > kMaxRows || k <= 0 || k > kMaxK || k % 128 != 0) return 0;
     return static_cast<size_t>(ceil_to(m, 128) * (k / 32));
 }
 
 size_t mxfp8_linear_128x4_workspace_bytes(int64_t m, int64_t k) {
-    if (m < 0 || k <= 0 || k % 128 != 0) return 0;
+    if (m < 0 || m > kMaxRows || k <= 0 || k > kMaxK || k % 128 != 0) return 0;
     return static_cast<size_t>(ceil_to(m * k, 256)) + mxfp8_act_scale_bytes_128x4(m, k);
 }
 
@@ -500,7 +500,7 @@ int64_t mxfp8_tactic_count(void) { return mxk::tactic_count(); }
 
 // ------------------------------------------------------------------- MoE
 size_t mxfp8_moe_route_workspace_bytes(int64_t tokens, int64_t experts, int64_t topk) {
-    if (tokens < 0 || experts < 1 || topk < 1) return 0;
+    if (tokens < 0 || tokens > kMaxRows || experts < 1 || experts > 1024 || topk < 1 || topk > 16) return 0;
     return static_cast<size_t>(((tokens + 31) / 32 * experts + tokens * topk) * 4);
 }
 
@@ -627,7 +627,7 @@ MoeWs moe_layout(int64_t tokens, int64_t experts, int64_t topk, int64_t hidden, 
 
 size_t mxfp8_moe_workspace_bytes(int64_t tokens, int64_t experts, int64_t topk, int64_t hidden, int64_t inter) {
     if (check_route_shape(tokens, experts, topk) != MXFP8_OK || hidden <= 0 || inter <= 0 || hidden % 32 ||
-        inter % 32)
+        inter % 32 || hidden > kMaxK || inter > kMaxK)
         return 0;
     return moe_layout(tokens, experts, topk, hidden, inter).total;
 }

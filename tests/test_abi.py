@@ -63,6 +63,21 @@ def test_size_helpers(mx):
     assert mx.weight_bytes(5120, 2048) == 5120 * 2048
     assert mx.act_scale_bytes(-1, 256) == 0
     assert mx.weight_bytes(0, 256) == 0
+    # beyond the library's limits (rows < 2^31 - 256, K <= 2^20): invalid, no overflow
+    lib = mx.library()
+    big = 1 << 62
+    assert mx.act_scale_bytes(big, 256) == 0 and mx.linear_workspace_bytes(big, 256) == 0
+    assert mx.linear_workspace_bytes(16, 1 << 40) == 0
+    assert mx.weight_bytes(big, 256) == 0 and mx.weight_scale_bytes(130, 1 << 40) == 0
+    assert lib.mxfp8_linear_host_workspace_bytes(16, big, 2048) == 0
+    assert lib.mxfp8_act_scale_bytes_128x4(big, 256) == 0
+    assert lib.mxfp8_linear_128x4_workspace_bytes(16, 1 << 40) == 0
+    assert lib.mxfp8_moe_route_workspace_bytes(big, 128, 8) == 0
+    assert lib.mxfp8_moe_workspace_bytes(256, 128, 8, 1 << 40, 768) == 0
+    # the largest valid shapes still give exact sizes
+    m_max = (1 << 31) - 256
+    assert mx.act_scale_bytes(m_max, 256) == m_max * 8
+    assert mx.linear_workspace_bytes(m_max, 1 << 20) == m_max * (1 << 20) + m_max * (1 << 15)
 
 
 def test_status_strings(mx):
