@@ -113,3 +113,22 @@ def test_autotune_refuses_capturing_stream(mx):
             raised = True
     assert raised
     assert mx.tactic_count() == 0
+
+
+@pytest.mark.parametrize("m,n,k", [(16, 5120, 2048), (1, 5120, 2048), (128, 2048, 4096), (7, 130, 256),
+                                   (300, 390, 1024), (2000, 4096, 512)])
+def test_plan_tactic_is_what_the_call_runs(mx, m, n, k):
+    """mxfp8_plan_tactic (this device's SM count) names the schedule that the
+    next call of that shape launches, with and without a table entry."""
+    d = workloads.dense(m=m, n=n, k=k, seed=m + k, bias=False)
+    pw, x, _, _, _ = _dense(mx, d)
+    plan = mx.plan_tactic(mx.KIND_LINEAR, m, n, k)
+    mx.linear(x, pw)
+    torch.cuda.synchronize()
+    assert _schedule_matches(mx.last_schedule(), plan), (plan, mx.last_schedule())
+    if m <= 128:
+        mx.tactic_set(mx.KIND_LINEAR, m, n, k, 1, (32, 2, 0, 2))
+        assert mx.plan_tactic(mx.KIND_LINEAR, m, n, k) == (32, 2, 0, 2)
+        mx.linear(x, pw)
+        torch.cuda.synchronize()
+        assert _schedule_matches(mx.last_schedule(), (32, 2, 0, 2)), mx.last_schedule()
