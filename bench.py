@@ -20,7 +20,9 @@ Also reported on the same line:
   cpu_baseline  the CPU oracle (plain C, one core) on a bounded sample;
   configs       every workload of the layer (tiny, decode M=1/16, mid, prefill
                 8192^3, grouped MoE gate_up): time, TFLOP/s, GB/s, roofline;
-  clocks        SM clocks and throttle reasons sampled during the timed region.
+  clocks        SM clocks and throttle reasons sampled during the timed region;
+  weight_prep   the load-time weight preparation of the headline's weight, a
+                one-off outside the metric: time and HBM rate.
 
 ``--impl reference`` times the CPU oracle on the same workload instead
 (bounded per step) and prints the same kind of line with "impl": "reference".
@@ -267,6 +269,37 @@ class DenseSetup:
         import ctypes
         import torch
         return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def measure_prepare(mx, d, peaks, reps=12):
+    """Load-time weight preparation (quantize + pad N + lay out), a one-off
+    per weight and not part of the per-call metric: CUDA-event time of
+    mxfp8_prepare_weight on the FP32 weight, re-preparing in place over
+    enough source copies that every repetition reads HBM (more than 4x L2),
+    and its rate over the algorithmic bytes (4NK read; N_pad*K data and
+    N_pad*K/32 scales written)."""
+    import torch
+    w0 = torch.from_numpy(d.w).cuda()
+    src_bytes = 4 * d.n * d.k
+    copies = min(64, max(2, -(-4 * L2_BYTES // src_bytes) + 1))
+    ws = [w0] + [w0.clone() for _ in range(copies - 1)]
+    pw = mx.prepare_weight(w0)
+    for i in range(3):
+        mx.prepare_weight(ws[i % copies], out=pw)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(reps):
+        mx.prepare_weight(ws[(i + 3) % copies], out=pw)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    n_pad = (d.n + 127) // 128 * 128
+    nbytes = src_bytes + n_pad * d.k + n_pad * (d.k // 32)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"us": ms * 1e3, "alg_bytes": nbytes, "gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"],
+            "reps": reps, "source_copies": copies, "source": "float32 [%d, %d]" % (d.n, d.k)}
 
 
 def measure_config(mx, name, d, peaks, calls=2000, tune=False):
@@ -621,6 +654,11 @@ def main():
            "kernel_us": {"linear_call": t_max / args.steps * 1e3, "gemm": ms_g * 1e3,
                          "quant_act": ms_q * 1e3}}
     del setup
+    torch.cuda.empty_cache()
+    try:  # auxiliary: a failure here must not cost the contract line
+        out["weight_prep"] = measure_prepare(mx, d, peaks)
+    except Exception as exc:  # noqa: BLE001
+        out["weight_prep"] = {"error": repr(exc)}
     torch.cuda.empty_cache()
 
     if rank == 0 and not args.no_configs:
