@@ -133,6 +133,15 @@ def _lib_status_string(status):
         return "?"
 
 
+def status_string(status: int) -> str:
+    return library().mxfp8_status_string(int(status)).decode()
+
+
+def last_cuda_error() -> int:
+    """cudaError_t of this thread's last call that returned MXFP8_ERR_CUDA."""
+    return library().mxfp8_last_cuda_error()
+
+
 def _check(status, where):
     if status != OK:
         raise Mxfp8Error(status, where)
@@ -316,7 +325,30 @@ def grouped_linear(x_sorted: torch.Tensor, offsets: torch.Tensor, pw: PreparedWe
     return y
 
 
+def linear_static_scratch(x: torch.Tensor, pw: PreparedWeight, bias=None) -> torch.Tensor:
+    """The layer with the library's own static scratch instead of a caller
+    workspace (the library allocates nothing; calls whose kernels overlap on
+    the GPU must not share it).  bf16 [m, k] -> bf16 [m, n]."""
+    _need(x.is_cuda and x.dtype == torch.bfloat16, "x must be a bfloat16 CUDA tensor")
+    _need(x.dim() == 2 and x.shape[1] == pw.k, "x must be [m, k]")
+    if bias is not None:
+        _need(bias.dtype == torch.bfloat16 and bias.numel() == pw.n, "bias must be bf16 [n]")
+    x2 = x.contiguous()
+    y = torch.empty((x2.shape[0], pw.n), dtype=torch.bfloat16, device=x.device)
+    _check(library().mxfp8_linear_static_scratch(_ptr(x2), x2.shape[0], ctypes.byref(pw.c), _ptr(bias),
+                                                 _ptr(y), _stream(x)), "mxfp8_linear_static_scratch")
+    return y
+
+
 # -------------------------------------------------- 128x4 activation scales
+def act_scale_bytes_128x4(m: int, k: int) -> int:
+    return library().mxfp8_act_scale_bytes_128x4(m, k)
+
+
+def linear_128x4_workspace_bytes(m: int, k: int) -> int:
+    return library().mxfp8_linear_128x4_workspace_bytes(m, k)
+
+
 def quantize_act_128x4(x: torch.Tensor):
     """BF16 [m, k] -> (E4M3 bytes [m, k], scales in the 128x4 layout
     [ceil128(m) * k/32])."""

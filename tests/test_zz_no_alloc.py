@@ -47,6 +47,10 @@ def test_static_scratch_matches_linear_on_two_calls(lib):
     torch.cuda.synchronize()
     assert_close_to_oracle(y1, r1.float().cpu().numpy().astype(np.float64), "static scratch call 1")
     assert_close_to_oracle(y2, r2.float().cpu().numpy().astype(np.float64), "static scratch call 2")
+    # the Python wrapper is the same call
+    y1b = lib.linear_static_scratch(x1, pw, b)
+    torch.cuda.synchronize()
+    assert torch.equal(y1b, y1)
 
 
 def test_static_scratch_rejects_oversize(lib):
