@@ -67,6 +67,16 @@ def test_grouped_multi_pipe(lib, tt, pipes):
     _run_grouped(lib, g, schedule=(tt, 0, -1), pipes=pipes)
 
 
+def test_grouped_max_experts(lib):
+    """The limit of 1024 experts (the per-expert tile-count table is full):
+    mostly empty experts, rows in the first, last and two middle ones,
+    ragged N, bias."""
+    counts = [0] * 1024
+    counts[0], counts[511], counts[700], counts[1023] = 3, 40, 1, 17
+    g = workloads.grouped_from_counts(counts, n=130, k=256, seed=54, bias=True)
+    _run_grouped(lib, g)
+
+
 def test_grouped_all_rows_one_expert(lib):
     g = workloads.grouped_from_counts([0, 0, 70, 0], n=128, k=256, seed=52)
     _run_grouped(lib, g)
