@@ -48,6 +48,22 @@ def test_route_matches_oracle(lib, method, shape):
     assert np.array_equal(r.row_of.cpu().numpy(), row_of)
 
 
+@pytest.mark.parametrize("method", [M.RENORMALIZE, M.RENORMALIZE_NAIVE])
+@pytest.mark.parametrize("shape", [(40, 512, 8, False), (70, 300, 4, True), (17, 1024, 16, False)])
+def test_route_wide_expert_counts(lib, method, shape):
+    """More experts than a warp keeps in registers (256): every selection
+    round reads the logits again; 1024 experts and top-16 are the limits."""
+    t, e, k, ties = shape
+    logits = workloads.router_logits(90 + e, t, e, logit_ties=ties)
+    r, ids, w = _route_both(lib, logits, k, method)
+    assert np.array_equal(r.ids.cpu().numpy(), ids)
+    assert np.allclose(r.weights.cpu().numpy(), w, rtol=1e-6, atol=1e-7)
+    off, stok, row_of = M.sort_by_expert(ids, e)
+    assert np.array_equal(r.offsets.cpu().numpy(), off)
+    assert np.array_equal(r.sorted_token.cpu().numpy(), stok)
+    assert np.array_equal(r.row_of.cpu().numpy(), row_of)
+
+
 def test_route_is_deterministic(lib):
     mw = workloads.moe(seed=3, tokens=300, experts=64, topk=6, hidden=256, inter=256, logit_ties=True)
     a = lib.moe_route(to_dev_f32(mw.logits), 6)

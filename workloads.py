@@ -190,6 +190,15 @@ class Moe:
     seed: int = 0
 
 
+def router_logits(seed, tokens, experts, logit_ties=False) -> np.ndarray:
+    """Router logits alone (float32 [tokens, experts]): N(0, 1), or with
+    logit_ties integer values in [-3, 3]."""
+    rng = np.random.default_rng(seed)
+    if logit_ties:
+        return rng.integers(-3, 4, size=(tokens, experts)).astype(np.float32)
+    return normal(rng, (tokens, experts))
+
+
 def moe(seed=6, tokens=256, experts=128, topk=8, hidden=2048, inter=768, logit_ties=False) -> Moe:
     """Inputs of one MoE expert-MLP layer.  logit_ties: integer-valued logits
     in [-3, 3] (many equal logits, to exercise the tie rule)."""
