@@ -10,19 +10,25 @@ starts; the weights (and activations) rotate over enough copies that every
 call reads them from HBM (copies x bytes >= 4x L2), and the K steps run as
 replays of CUDA graphs of back-to-back calls.
 
-Also reported on the same line:
+Before the contract line, one compact JSON line per workload of the layer
+(key "bench_config": tiny, decode M=1/16, mid, mid N=130, prefill 8192^3 with
+8x4 and 128x4 activation scales, grouped MoE gate_up, MoE expert MLP,
+autotuned decode/mid): time per call, TFLOP/s, GB/s, roofline fraction, and
+the CPU oracle's time on the same workload.  The contract line (last) holds:
   e2e           the same metric through the host-buffer call (mxfp8_linear_host
                 via its Python binding): each step copies x in from pinned host
                 memory, runs the layer and copies y back to pinned host memory;
                 steps alternate over two streams (two requests in flight);
   roofline      the dominant kernel of the timed step (the GEMM, which at
                 decode fuses the activation quantization) against HBM bandwidth;
-  cpu_baseline  the CPU oracle (plain C, one core) on a bounded sample;
-  configs       every workload of the layer (tiny, decode M=1/16, mid, prefill
-                8192^3, grouped MoE gate_up): time, TFLOP/s, GB/s, roofline;
+  large_m       the large-M half of the metric: the 8x4 prefill layer and its
+                GEMM alone in TFLOP/s and as a fraction of the FP8 tensor peak;
+  cpu_baseline  the CPU oracle (plain C, one core) on the full decode call,
+                with the host's core count and CPU model;
   clocks        SM clocks and throttle reasons sampled during the timed region;
   weight_prep   the load-time weight preparation of the headline's weight, a
                 one-off outside the metric: time and HBM rate.
+Floats on the printed lines carry 4 significant digits.
 
 ``--impl reference`` times the CPU oracle on the same workload instead
 (bounded per step) and prints the same kind of line with "impl": "reference".
@@ -48,6 +54,7 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 FP8_PER_BF16 = 2.0  # nominal dense FP8 / BF16 tensor-rate ratio (4.5 / 2.25 PF)
 L2_BYTES = 126 * 1024 * 1024
+GPU_DELAY_CYCLES = 2_000_000  # ~1 ms at 2 GHz, queued ahead of each timed region
 
 
 def parse_args():
@@ -57,7 +64,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=2000)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-workload table")
-    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle CPU-baseline budget")
+    ap.add_argument("--cpu-seconds", type=float, default=5.0, help="oracle CPU-baseline budget")
     ap.add_argument("--workload", default="decode16",
                     choices=["decode16", "decode1", "tiny", "mid", "mid130", "prefill", "grouped", "moe",
                              "prefill128x4"],
@@ -176,6 +183,11 @@ def time_steps(fn, steps, warmup, chunk=1000, barrier=None):
     stream = torch.cuda.current_stream()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    # A bounded GPU delay (a fixed number of clock cycles, ~1 ms) ahead of the
+    # start event: the host submits the graph replays while the GPU is still
+    # busy with it, so the timed region holds device work only and not the
+    # host's submission latency of the first replay.
+    torch.cuda._sleep(GPU_DELAY_CYCLES)
     e0.record(stream)
     for _ in range(steps // chunk):
         g_main.replay()
@@ -377,10 +389,11 @@ def measure_128x4(mx, d, peaks, calls=40):
     return out
 
 
-def measure_grouped(mx, peaks, calls=200):
+def measure_grouped(mx, peaks, calls=200, g=None):
     import torch
     import workloads
-    g = workloads.grouped()
+    if g is None:
+        g = workloads.grouped()
     w = torch.from_numpy(g.w).cuda()
     pw = mx.prepare_weight(w)
     del w
@@ -454,32 +467,122 @@ def measure_moe(mx, peaks, calls=200):
 
 
 # ------------------------------------------------------------ CPU baseline
-def oracle_sample(d, budget_s, max_calls=None):
-    """Time the CPU oracle (one core) on whole output column blocks of the
-    workload: each sample computes all M rows for a block of weight rows, so
-    the weight bytes it covers are fully processed."""
+def host_description():
+    """Host core count and CPU model (lscpu, else /proc/cpuinfo)."""
+    import platform
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:  # noqa: BLE001
+        pass
+    if not model:
+        try:
+            for line in open("/proc/cpuinfo"):
+                if line.lower().startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except OSError:
+            pass
+    return {"host_cores": os.cpu_count(), "cpu_model": model or platform.machine()}
+
+
+def _timed(fn, min_s):
+    """Mean seconds per call of fn(), repeated until min_s has elapsed (at
+    least once)."""
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        fn()
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= min_s:
+            return el / n, n
+
+
+def oracle_dense(d, min_s, rows=None):
+    """The CPU oracle (plain C, one core) on one dense call: quantize x, the
+    block-scaled product in double, bias.  The weight is quantized first and
+    outside the timed region (it is load-time work).  rows: time only these
+    output rows and scale the time to all M rows (labelled)."""
     import oracle
     wq, wsf = oracle.quantize_rows(d.w)
-    # calibrate on a small block
-    t0 = time.perf_counter()
-    oracle.linear(d.x, wq[:8], wsf[:8], None if d.bias is None else d.bias[:8])
-    per_row = (time.perf_counter() - t0) / 8
-    nb = int(max(1, min(d.n, budget_s / max(per_row, 1e-9))))
-    t0 = time.perf_counter()
-    done = 0
-    c0 = 0
-    while True:
-        c1 = min(d.n, c0 + nb)
-        oracle.linear(d.x, wq[c0:c1], wsf[c0:c1], None if d.bias is None else d.bias[c0:c1])
-        done += c1 - c0
-        c0 = c1 % d.n
-        if time.perf_counter() - t0 >= budget_s or (max_calls and done >= max_calls):
-            break
-    el = time.perf_counter() - t0
-    wb = done * (d.k + d.k // 32)
-    return {"value": wb / el / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": "%d of %d weight rows x all %d tokens (K=%d) of the workload, %.1f s" %
-                      (done, d.n, d.m, d.k, el)}
+    if rows is None:
+        sec, n = _timed(lambda: oracle.linear(d.x, wq, wsf, d.bias), min_s)
+        scale, sample = 1.0, "full call (all %d rows), %d repetitions" % (d.m, n)
+    else:
+        sec, n = _timed(lambda: oracle.linear(d.x, wq, wsf, d.bias, rows=rows), min_s)
+        scale = d.m / len(rows)
+        sample = ("%d sampled rows of %d (all N columns), time scaled by %d to the full call"
+                  % (len(rows), d.m, int(scale)))
+    sec *= scale
+    flops = 2.0 * d.m * d.n * d.k
+    return {"us_per_call": sec * 1e6, "tflops": flops / sec / 1e12,
+            "weight_gbs": weight_bytes(d.n, d.k) / sec / 1e9, "cores": 1, "kind": "oracle",
+            "sample": sample}
+
+
+def oracle_grouped(g, n_experts):
+    """The CPU oracle on the grouped gate_up call, timed on the rows of the
+    first n_experts experts (their weights quantized outside the timed region)
+    and scaled to all rows by the row count."""
+    import oracle
+    import oracle.moe as moe
+    e = n_experts
+    r1 = int(g.offsets[e])
+    gq, gsf = moe.prepare_experts(g.w[:e])
+    off = np.ascontiguousarray(g.offsets[:e + 1])
+    sec, n = _timed(lambda: oracle.grouped_linear(g.x_sorted[:r1], off, gq, gsf), 0.5)
+    scale = g.rows / max(r1, 1)
+    sec *= scale
+    flops = 2.0 * g.rows * g.n * g.k
+    return {"us_per_call": sec * 1e6, "tflops": flops / sec / 1e12,
+            "weight_gbs": weight_bytes(g.n, g.k, g.experts) / sec / 1e9, "cores": 1, "kind": "oracle",
+            "sample": "rows of experts 0..%d (%d of %d rows), time scaled by the row count"
+                      % (e - 1, r1, g.rows)}
+
+
+def cpu_baselines(wl):
+    """The oracle on every dense workload and the grouped one: configs 1-3 in
+    full; prefill on 64 sampled rows; grouped on the rows of 16 experts."""
+    out = {}
+    out["tiny_m7_n130_k256"] = oracle_dense(wl["tiny"], 0.5)
+    out["decode_m1_n5120_k2048"] = oracle_dense(wl["decode1"], 1.0)
+    out["decode_m16_n5120_k2048"] = oracle_dense(wl["decode16"], 1.0)
+    out["mid_m128_n2048_k4096"] = oracle_dense(wl["mid"], 0.5)
+    out["mid_m128_n130_k4096_bias"] = oracle_dense(wl["mid130"], 0.5)
+    rng = np.random.default_rng(7)
+    pre = wl["prefill"]
+    rows = np.unique(np.concatenate([np.arange(32), [pre.m - 1], rng.choice(pre.m, 31, replace=False)]))
+    out["prefill_m8192_n8192_k8192"] = oracle_dense(pre, 0.0, rows=rows)
+    out["grouped_t256_e128_top8_n1536_k2048"] = oracle_grouped(wl["grouped"], 16)
+    return out
+
+
+def headline_cpu_baseline(d, budget_s):
+    """The contract line's baseline: the oracle on the full decode call (all
+    16 tokens x all 5120 weight rows), repeated for about budget_s."""
+    import oracle
+    wq, wsf = oracle.quantize_rows(d.w)
+    sec, n = _timed(lambda: oracle.linear(d.x, wq, wsf, d.bias), budget_s)
+    res = {"value": weight_bytes(d.n, d.k) / sec / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+           "sample": "the full decode call (M=16, N=5120, K=2048) %d times, %.1f s" % (n, sec * n)}
+    res.update(host_description())
+    return res
+
+
+def compact(v):
+    """Floats to 4 significant digits (keeps the printed lines short)."""
+    if isinstance(v, float):
+        return float("%.4g" % v)
+    if isinstance(v, dict):
+        return {k: compact(x) for k, x in v.items()}
+    if isinstance(v, (list, tuple)):
+        return [compact(x) for x in v]
+    return v
 
 
 # ------------------------------------------------------------------- main
@@ -565,10 +668,50 @@ def run_reference(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": d.name, "m": d.m, "n": d.n, "k": d.k,
                                             "bias": True},
-            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": sample},
+            "cpu_baseline": dict({"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                  "sample": sample}, **host_description()),
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def large_m_block(cfgs, peaks):
+    """The large-M half of the metric: the 8x4 prefill layer and its GEMM
+    alone against the FP8 tensor peak (measured BF16 x the nominal ratio)."""
+    p = cfgs.get("prefill_m8192_n8192_k8192")
+    if not p:
+        return None
+    fp8 = peaks["bf16_tflops"] * FP8_PER_BF16
+    return {"workload": "prefill_m8192_n8192_k8192", "us_per_call": p["us_per_call"], "tflops": p["tflops"],
+            "frac": p["tflops"] / fp8, "gemm_us": p["gemm_us"], "gemm_tflops": p["gemm_tflops"],
+            "gemm_frac": p["gemm_tflops"] / fp8, "peak_tflops": fp8,
+            "peak": "fp8 = 2 x bf16 %s" % peaks["source"]}
+
+
+def build_workloads():
+    import workloads
+    return {"tiny": workloads.tiny(), "decode1": workloads.decode(m=1), "decode16": workloads.decode(m=16),
+            "mid": workloads.mid(), "mid130": workloads.mid(n=130, bias=True), "prefill": workloads.prefill(),
+            "grouped": workloads.grouped()}
+
+
+def measure_configs(mx, wl, peaks):
+    """Every workload of the layer on the GPU (time per call, TFLOP/s, GB/s,
+    roofline), each timed as CUDA-graph replays over rotating copies."""
+    cfgs = {}
+    cfgs["tiny_m7_n130_k256"] = measure_config(mx, "tiny", wl["tiny"], peaks, 2000)
+    cfgs["decode_m1_n5120_k2048"] = measure_config(mx, "d1", wl["decode1"], peaks, 4000)
+    cfgs["decode_m16_n5120_k2048"] = measure_config(mx, "d16", wl["decode16"], peaks, 4000)
+    cfgs["mid_m128_n2048_k4096"] = measure_config(mx, "mid", wl["mid"], peaks, 2000)
+    cfgs["mid_m128_n130_k4096_bias"] = measure_config(mx, "mid130", wl["mid130"], peaks, 2000)
+    cfgs["prefill_m8192_n8192_k8192"] = measure_config(mx, "prefill", wl["prefill"], peaks, 40)
+    cfgs["prefill_m8192_n8192_k8192_128x4"] = measure_128x4(mx, wl["prefill"], peaks, 40)
+    cfgs["grouped_t256_e128_top8_n1536_k2048"] = measure_grouped(mx, peaks, 200, g=wl["grouped"])
+    cfgs["moe_mlp_t256_e128_top8_h2048_i768"] = measure_moe(mx, peaks, 200)
+    cfgs["decode_m16_n5120_k2048_autotuned"] = measure_config(mx, "d16", wl["decode16"], peaks, 4000, tune=True)
+    cfgs["mid_m128_n2048_k4096_autotuned"] = measure_config(mx, "mid", wl["mid"], peaks, 2000, tune=True)
+    for v in cfgs.values():
+        v["peaks"] = "of %s" % peaks["source"]
+    return cfgs
 
 
 def main():
@@ -626,10 +769,9 @@ def main():
     g_steps = min(args.steps, 20000)
     ms_g = time_steps(setup.gemm, g_steps, 100) / g_steps
     roof = step_roofline(d, wb, launches_per_step, t_max / args.steps, ms_g, peaks["hbm_gbs"],
-                          load_traffic("gemm", d.name), mx.act_scale_bytes(d.m, d.k))
+                         load_traffic("gemm", d.name), mx.act_scale_bytes(d.m, d.k))
     roof["peak_source"] = peak_src
-    q_steps = min(args.steps, 20000)
-    ms_q = time_steps(setup.quant, q_steps, 100) / q_steps
+    roof.pop("gemm_prequantized_alone", None)
 
     # ---- e2e through the public API with host buffers
     e2e = measure_e2e(mx, setup, steps=min(args.steps, 3000))
@@ -644,15 +786,13 @@ def main():
            "data": "synthetic",
            "config": {"workload": d.name, "m": d.m, "n": d.n, "k": d.k, "bias": True,
                       "parallelism": "replicas" if ws > 1 else "single",
-                      "l2": "inputs larger than L2: weights+activations rotate over %d copies "
-                            "(%.0f MB)" % (setup.R, setup.R * nbytes / 1e6),
-                      "timing": "CUDA graphs of back-to-back calls, CUDA events"},
+                      "l2": "inputs larger than L2: %d rotating copies (%.0f MB)" % (setup.R, setup.R * nbytes / 1e6),
+                      "timing": "CUDA-graph replays, CUDA events; 1 ms GPU delay queued before the start event"},
            "roofline": roof,
            "gpu_launches": launches_per_step * args.steps,
            "clocks": clk,
-           "e2e": e2e,
-           "kernel_us": {"linear_call": t_max / args.steps * 1e3, "gemm": ms_g * 1e3,
-                         "quant_act": ms_q * 1e3}}
+           "e2e": e2e}
+    gemm_alone_us = ms_g * 1e3
     del setup
     torch.cuda.empty_cache()
     try:  # auxiliary: a failure here must not cost the contract line
@@ -661,26 +801,33 @@ def main():
         out["weight_prep"] = {"error": repr(exc)}
     torch.cuda.empty_cache()
 
-    if rank == 0 and not args.no_configs:
-        cfgs = {}
-        cfgs["tiny_m7_n130_k256"] = measure_config(mx, "tiny", workloads.tiny(), peaks, 2000)
-        cfgs["decode_m1_n5120_k2048"] = measure_config(mx, "d1", workloads.decode(m=1), peaks, 4000)
-        cfgs["decode_m16_n5120_k2048"] = measure_config(mx, "d16", workloads.decode(m=16), peaks, 4000)
-        cfgs["mid_m128_n2048_k4096"] = measure_config(mx, "mid", workloads.mid(), peaks, 2000)
-        cfgs["mid_m128_n130_k4096_bias"] = measure_config(mx, "mid130", workloads.mid(n=130, bias=True), peaks, 2000)
-        cfgs["prefill_m8192_n8192_k8192"] = measure_config(mx, "prefill", workloads.prefill(), peaks, 40)
-        cfgs["prefill_m8192_n8192_k8192_128x4"] = measure_128x4(mx, workloads.prefill(), peaks, 40)
-        cfgs["grouped_t256_e128_top8_n1536_k2048"] = measure_grouped(mx, peaks, 200)
-        cfgs["moe_mlp_t256_e128_top8_h2048_i768"] = measure_moe(mx, peaks, 200)
-        cfgs["decode_m16_n5120_k2048_autotuned"] = measure_config(mx, "d16", workloads.decode(m=16), peaks, 4000,
-                                                                  tune=True)
-        cfgs["mid_m128_n2048_k4096_autotuned"] = measure_config(mx, "mid", workloads.mid(), peaks, 2000, tune=True)
-        for v in cfgs.values():
-            v["peaks"] = peak_src
-        out["configs"] = cfgs
     if rank == 0:
-        out["cpu_baseline"] = oracle_sample(d, args.cpu_seconds)
-        print(json.dumps(out), flush=True)
+        wl = build_workloads() if not args.no_configs else {}
+        cfgs = {}
+        if not args.no_configs:
+            cfgs = measure_configs(mx, wl, peaks)
+        cpu = {}
+        if not args.no_configs:
+            try:
+                cpu = cpu_baselines(wl)
+            except Exception as exc:  # noqa: BLE001
+                cpu = {"error": {"error": repr(exc)}}
+        # one compact line per workload before the contract line
+        for name, v in cfgs.items():
+            line = {"bench_config": name}
+            line.update(v)
+            if name in cpu:
+                line["cpu_baseline"] = cpu[name]
+            print(json.dumps(compact(line)), flush=True)
+        for name, v in cpu.items():
+            if name not in cfgs:
+                print(json.dumps(compact({"bench_config": name, "cpu_baseline": v})), flush=True)
+        lm = large_m_block(cfgs, peaks)
+        if lm:
+            out["large_m"] = lm
+        out["kernel_us"] = {"linear_call": t_max / args.steps * 1e3, "gemm_prequantized": gemm_alone_us}
+        out["cpu_baseline"] = headline_cpu_baseline(d, args.cpu_seconds)
+        print(json.dumps(compact(out)), flush=True)
     if ws > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

@@ -26,7 +26,7 @@ def test_fused_step_is_the_dominant_launch():
     assert abs(r["us_per_launch"] - 5.0) < 1e-9
     assert abs(r["achieved"] - nbytes / 5e-6 / 1e9) < 1e-6
     assert abs(r["frac"] - r["achieved"] / 6800.0) < 1e-12
-    g = r["gemm_prequantized_alone"]
+    g = r["gemm_prequantized_alone"]  # dropped from the printed line by main()
     assert g["alg_bytes_per_launch"] == 11_021_312 and abs(g["us_per_launch"] - 4.0) < 1e-9
 
 
@@ -35,3 +35,24 @@ def test_unfused_step_reports_the_gemm():
     assert r["alg_bytes_per_launch"] == 11_021_312
     assert abs(r["us_per_launch"] - 4.0) < 1e-9
     assert r["traffic"] == 123.0 and r["bound"] == "hbm" and r["unit"] == "GB/s"
+
+
+def test_compact_keeps_four_significant_digits():
+    v = bench.compact({"a": 1599.9999875, "b": [0.241178353, 3], "c": {"d": 1e-7 / 3}, "e": "s"})
+    assert v == {"a": 1600.0, "b": [0.2412, 3], "c": {"d": 3.333e-08}, "e": "s"}
+
+
+def test_large_m_block_uses_the_fp8_peak():
+    peaks = {"bf16_tflops": 1897.8, "source": "measured"}
+    cfg = {"prefill_m8192_n8192_k8192": {"us_per_call": 424.0, "tflops": 2593.2, "gemm_us": 387.0,
+                                         "gemm_tflops": 2841.1}}
+    lm = bench.large_m_block(cfg, peaks)
+    assert abs(lm["peak_tflops"] - 3795.6) < 1e-9
+    assert abs(lm["frac"] - 2593.2 / 3795.6) < 1e-12
+    assert abs(lm["gemm_frac"] - 2841.1 / 3795.6) < 1e-12
+    assert bench.large_m_block({}, peaks) is None
+
+
+def test_host_description_names_cores_and_model():
+    h = bench.host_description()
+    assert h["host_cores"] == os.cpu_count() and isinstance(h["cpu_model"], str) and h["cpu_model"]
