@@ -70,7 +70,9 @@ typedef enum mxfp8_status {
     MXFP8_ERR_UNSUPPORTED_DEVICE = 4,    /* current device is not compute capability 10.3 */
     MXFP8_ERR_WORKSPACE_TOO_SMALL = 5,   /* workspace_bytes below the size helper's value */
     MXFP8_ERR_DEVICE_TIMEOUT = 6,        /* a kernel gave up waiting (see mxfp8_device_error) */
-    MXFP8_ERR_CUDA = 7                   /* a CUDA call failed: mxfp8_last_cuda_error() */
+    MXFP8_ERR_CUDA = 7,                  /* a CUDA call failed: mxfp8_last_cuda_error() */
+    MXFP8_ERR_OUT_OF_BOUNDS = 8          /* debug build only: a kernel computed a store index outside
+                                            its buffer and skipped the store (see mxfp8_device_error) */
 } mxfp8_status;
 
 typedef enum mxfp8_in_dtype {
@@ -189,7 +191,9 @@ mxfp8_status mxfp8_linear_host(const void* x_host, int64_t m, const mxfp8_weight
  * paths that must never allocate once running.
  *
  * mxfp8_linear_static_scratch computes what mxfp8_linear computes, always by
- * the unfused path (quantizer -> scratch -> GEMM), with the scratch in an
+ * the unfused path (quantizer -> scratch -> GEMM; its schedule is a stored
+ * unfused tactic of the mxfp8_linear class when the tactic table holds one,
+ * else the built-in heuristic's unfused choice), with the scratch in an
  * array of MXFP8_STATIC_SCRATCH_BYTES inside the library: every GPU that
  * loads the library holds that array until the process exits.  It allocates
  * nothing and calls no allocating routine.  The caller still passes x, the
@@ -204,7 +208,8 @@ mxfp8_status mxfp8_linear_host(const void* x_host, int64_t m, const mxfp8_weight
  *    (nothing needs clearing: each call writes every byte it reads).  Calls
  *    whose kernels overlap on the GPU race on it: serialise them.
  *  - Errors and other conventions as mxfp8_linear; a failed CUDA call's code
- *    is returned by mxfp8_static_scratch_last_cuda_error(). */
+ *    is returned by mxfp8_last_cuda_error() and by
+ *    mxfp8_static_scratch_last_cuda_error(). */
 #define MXFP8_STATIC_SCRATCH_BYTES (16u << 20)
 mxfp8_status mxfp8_linear_static_scratch(const void* x, int64_t m, const mxfp8_weight* w,
                                          const void* bias, void* y, void* stream);
@@ -294,37 +299,16 @@ mxfp8_status mxfp8_plan_tactic(int kind, int64_t m, int64_t n, int64_t k, int64_
 const char* mxfp8_status_string(mxfp8_status status);
 /* cudaError_t of the last call that returned MXFP8_ERR_CUDA (per thread). */
 int mxfp8_last_cuda_error(void);
-/* Reads and clears the device-side error word that the GEMM kernels set when
- * a wait gives up (a hang turned into an error).  SYNCHRONISES the current
- * device.  Returns MXFP8_OK or MXFP8_ERR_DEVICE_TIMEOUT. */
+/* Reads and clears the device-side error words: the one the GEMM kernels set
+ * when a wait gives up (a hang turned into an error), and, in the debug
+ * build (libmxfp8_gb300_debug.so, compiled with MXFP8_DEBUG), the ones every
+ * kernel sets when a computed store index falls outside its buffer (the
+ * store is skipped).  SYNCHRONISES the current device.  Returns MXFP8_OK,
+ * MXFP8_ERR_DEVICE_TIMEOUT or MXFP8_ERR_OUT_OF_BOUNDS (timeout first). */
 mxfp8_status mxfp8_device_error(void);
 
-/* Testing hook: pin the GEMM schedule, process-wide.
- * tokens_per_tile: 0 (automatic) or 16, 32, 64, 128, 256 (256 needs split_k -1);
- * split_k: 0 automatic, -1 persistent tiles, 1..8 one tile per cluster of
- * split_k CTAs (K split among them, tokens_per_tile <= 128);
- * fuse_quant: -1 automatic, 0 never, 1 whenever the schedule allows
- * (one-tile schedules of mxfp8_linear) -- the GEMM then quantizes x itself. */
-void mxfp8_set_schedule(int tokens_per_tile, int split_k, int fuse_quant);
-
-/* Testing hook for failure detection: limit, in nanoseconds, of every
- * pipeline wait of later GEMM launches (0 restores the default, 4 s).  A wait
- * that runs out sets the device error word read by mxfp8_device_error(); the
- * kernel then unwinds (in-flight copies and MMAs drained, TMEM freed) and
- * returns, so the context stays usable.  Process-wide. */
-void mxfp8_set_wait_limit_ns(uint64_t ns);
-
-/* Testing hook: MMA pipelines per CTA for later launches (0 = automatic, 1,
- * 2, or 4; more than one only for tiles of <= 64 tokens, 4 only for 16).
- * Each pipeline has its own producer and MMA-issuing thread, owns every
- * pipes-th K block of a tile and accumulates in its own TMEM columns; the
- * epilogue sums them in pipeline order.  Process-wide. */
-void mxfp8_set_pipes(int pipes);
-
-/* Testing hook: the schedule of the calling thread's last GEMM launch, as
- * out5[0..4] = {tokens per tile + 1000 * (pipelines - 1), split (-1 =
- * persistent), fused quantization (0/1), grid size, stages per pipeline}. */
-void mxfp8_last_schedule(int* out5);
+/* The process-wide testing hooks (schedule pinning, wait limit, pipelines,
+ * last schedule) are declared in mxfp8_testing.h. */
 
 #ifdef __cplusplus
 }

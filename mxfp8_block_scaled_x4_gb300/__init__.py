@@ -26,13 +26,17 @@ __all__ = [
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_LIB_PATH = os.path.join(_HERE, "_lib", "libmxfp8_gb300.so")
+# MXFP8_DEBUG_LIBRARY=1 in the environment selects the debug build (every
+# computed store index checked; see mxfp8_device_error) for this process.
+_LIB_PATH = os.path.join(_HERE, "_lib", "libmxfp8_gb300_debug.so" if os.environ.get("MXFP8_DEBUG_LIBRARY") == "1"
+                         else "libmxfp8_gb300.so")
 
 OK = 0
 STATUS_NAMES = {
     0: "MXFP8_OK", 1: "MXFP8_ERR_INVALID_ARG", 2: "MXFP8_ERR_K_NOT_MULTIPLE_OF_256",
     3: "MXFP8_ERR_MISALIGNED", 4: "MXFP8_ERR_UNSUPPORTED_DEVICE",
     5: "MXFP8_ERR_WORKSPACE_TOO_SMALL", 6: "MXFP8_ERR_DEVICE_TIMEOUT", 7: "MXFP8_ERR_CUDA",
+    8: "MXFP8_ERR_OUT_OF_BOUNDS",
 }
 IN_F32 = 0
 IN_BF16 = 1
@@ -56,6 +60,24 @@ class mxfp8_weight(ctypes.Structure):
 
 
 _lib = None
+
+
+_allocator = None
+
+
+def _alloc(shape, dtype, device):
+    """Every device output and workspace this module allocates comes from here."""
+    if _allocator is not None:
+        return _allocator(shape, dtype, device)
+    return torch.empty(shape, dtype=dtype, device=device)
+
+
+def set_allocator(fn=None) -> None:
+    """Testing aid: allocate every device output and workspace of this module
+    with fn(shape, dtype, device) instead of torch.empty (None restores it).
+    The GPU tests use it to place each buffer between guard bytes."""
+    global _allocator
+    _allocator = fn
 
 
 def library_path() -> str:
@@ -117,6 +139,7 @@ def library():
         "mxfp8_moe_finalize": (ctypes.c_int, [vp, vp, vp, i64, i64, i64, vp, vp]),
         "mxfp8_moe_workspace_bytes": (sz, [i64, i64, i64, i64, i64]),
         "mxfp8_moe_expert_mlp": (ctypes.c_int, [vp, vp, i64, i64, ctypes.c_int, W, W, vp, vp, sz, vp]),
+        "mxfp8_debug_build": (ctypes.c_int, []),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -221,8 +244,8 @@ def prepare_weight(w: torch.Tensor, out: PreparedWeight = None) -> PreparedWeigh
         _need((out.num_experts, out.n, out.k) == (e, n, k), "refit needs a weight of the same shape")
         pw = out
     else:
-        q = torch.empty((e, n_pad, k), dtype=torch.uint8, device=w.device)
-        sf = torch.empty((e, n_pad * (k // 32)), dtype=torch.uint8, device=w.device)
+        q = _alloc((e, n_pad, k), torch.uint8, w.device)
+        sf = _alloc((e, n_pad * (k // 32)), torch.uint8, w.device)
         pw = PreparedWeight(q, sf, n)
     dt = IN_BF16 if w3.dtype == torch.bfloat16 else IN_F32
     _check(library().mxfp8_prepare_weight(_ptr(w3), dt, ctypes.byref(pw.c), _stream(w)),
@@ -231,30 +254,48 @@ def prepare_weight(w: torch.Tensor, out: PreparedWeight = None) -> PreparedWeigh
 
 
 # -------------------------------------------------------------- activations
-def quantize_act(x: torch.Tensor):
-    """BF16 [m, k] -> (E4M3 bytes uint8 [m, k], 8x4 scales uint8 [ceil8(m)*k/32])."""
+def _out(t, shape, dtype, dev, what):
+    """A caller-given output tensor (checked) or a new one."""
+    if t is None:
+        return _alloc(shape, dtype, dev)
+    _need(t.is_cuda and t.dtype == dtype and t.is_contiguous() and t.numel() >= _numel(shape),
+          "%s must be a contiguous %s CUDA tensor of at least %s elements" % (what, dtype, _numel(shape)))
+    return t
+
+
+def _numel(shape):
+    n = 1
+    for d in shape:
+        n *= int(d)
+    return n
+
+
+def quantize_act(x: torch.Tensor, q=None, sf=None):
+    """BF16 [m, k] -> (E4M3 bytes uint8 [m, k], 8x4 scales uint8 [ceil8(m)*k/32]).
+    q, sf: optional caller buffers to write into."""
     _need(x.is_cuda and x.dtype == torch.bfloat16, "x must be a bfloat16 CUDA tensor")
     x2 = x.reshape(-1, x.shape[-1]).contiguous()
     m, k = x2.shape
-    q = torch.empty((m, k), dtype=torch.uint8, device=x.device)
-    sf = torch.empty((max(act_scale_bytes(m, k), 1),), dtype=torch.uint8, device=x.device)
+    q = _out(q, (m, k), torch.uint8, x.device, "q")
+    sf = _out(sf, (max(act_scale_bytes(m, k), 1),), torch.uint8, x.device, "sf")
     _check(library().mxfp8_quantize_act(_ptr(x2), m, k, _ptr(q), _ptr(sf), _stream(x)),
            "mxfp8_quantize_act")
     return q, sf[:act_scale_bytes(m, k)]
 
 
-def gemm(qa: torch.Tensor, sfa: torch.Tensor, pw: PreparedWeight, bias=None) -> torch.Tensor:
-    """Block-scaled GEMM on pre-quantized activations -> BF16 [m, n]."""
+def gemm(qa: torch.Tensor, sfa: torch.Tensor, pw: PreparedWeight, bias=None, out=None) -> torch.Tensor:
+    """Block-scaled GEMM on pre-quantized activations -> BF16 [m, n]
+    (written into `out` when given)."""
     m = qa.shape[0]
-    y = torch.empty((m, pw.n), dtype=torch.bfloat16, device=qa.device)
+    y = _out(out, (m, pw.n), torch.bfloat16, qa.device, "out")
     _check(library().mxfp8_gemm(_ptr(qa), _ptr(sfa), m, ctypes.byref(pw.c), _ptr(bias), _ptr(y),
                                 _stream(qa)), "mxfp8_gemm")
     return y
 
 
-def linear(x: torch.Tensor, pw: PreparedWeight, bias=None, workspace=None) -> torch.Tensor:
+def linear(x: torch.Tensor, pw: PreparedWeight, bias=None, workspace=None, out=None) -> torch.Tensor:
     """The layer: BF16 x [..., k] -> BF16 [..., n] (leading dims kept, as
-    apply_weights does)."""
+    apply_weights does).  out: optional contiguous BF16 buffer for y."""
     _need(x.is_cuda and x.dtype == torch.bfloat16, "x must be a bfloat16 CUDA tensor")
     _need(x.shape[-1] == pw.k, "x's last dim must equal the weight's K")
     lead = x.shape[:-1]
@@ -264,11 +305,11 @@ def linear(x: torch.Tensor, pw: PreparedWeight, bias=None, workspace=None) -> to
         _need(bias.dtype == torch.bfloat16 and bias.numel() == pw.n, "bias must be bf16 [n]")
     ws_need = linear_workspace_bytes(m, pw.k)
     if workspace is None:
-        workspace = torch.empty((max(ws_need, 16),), dtype=torch.uint8, device=x.device)
-    y = torch.empty((m, pw.n), dtype=torch.bfloat16, device=x.device)
+        workspace = _alloc((max(ws_need, 16),), torch.uint8, x.device)
+    y = _out(out, (m, pw.n), torch.bfloat16, x.device, "out")
     _check(library().mxfp8_linear(_ptr(x2), m, ctypes.byref(pw.c), _ptr(bias), _ptr(y),
                                   _ptr(workspace), workspace.numel(), _stream(x)), "mxfp8_linear")
-    return y.reshape(*lead, pw.n)
+    return y.view(-1)[:m * pw.n].view(*lead, pw.n)
 
 
 def linear_host_workspace_bytes(m: int, n: int, k: int) -> int:
@@ -293,8 +334,8 @@ def linear_host(x_host: torch.Tensor, pw: PreparedWeight, bias=None, y_host=None
     if bias is not None:
         _need(bias.is_cuda and bias.dtype == torch.bfloat16 and bias.numel() == pw.n, "bias must be bf16 CUDA [n]")
     if workspace is None:
-        workspace = torch.empty((max(linear_host_workspace_bytes(m, pw.n, pw.k), 16),), dtype=torch.uint8,
-                                device="cuda")
+        workspace = _alloc((max(linear_host_workspace_bytes(m, pw.n, pw.k), 16),), torch.uint8,
+                           torch.device("cuda", torch.cuda.current_device()))
     _need(workspace.is_cuda and workspace.device.index == torch.cuda.current_device(),
           "workspace must be on the current CUDA device")
     if stream is None:
@@ -306,7 +347,7 @@ def linear_host(x_host: torch.Tensor, pw: PreparedWeight, bias=None, y_host=None
 
 
 def grouped_linear(x_sorted: torch.Tensor, offsets: torch.Tensor, pw: PreparedWeight,
-                   bias=None, workspace=None) -> torch.Tensor:
+                   bias=None, workspace=None, out=None) -> torch.Tensor:
     """Per-expert layer over expert-sorted rows: x_sorted bf16 [rows, k],
     offsets int32 [e+1] (device) -> bf16 [rows, n]."""
     _need(x_sorted.is_cuda and x_sorted.dtype == torch.bfloat16, "x_sorted must be bf16 CUDA")
@@ -316,8 +357,8 @@ def grouped_linear(x_sorted: torch.Tensor, offsets: torch.Tensor, pw: PreparedWe
     x2 = x_sorted.contiguous()
     ws_need = linear_workspace_bytes(rows, pw.k)
     if workspace is None:
-        workspace = torch.empty((max(ws_need, 16),), dtype=torch.uint8, device=x_sorted.device)
-    y = torch.empty((rows, pw.n), dtype=torch.bfloat16, device=x_sorted.device)
+        workspace = _alloc((max(ws_need, 16),), torch.uint8, x_sorted.device)
+    y = _out(out, (rows, pw.n), torch.bfloat16, x_sorted.device, "out")
     _check(library().mxfp8_grouped_linear(_ptr(x2), rows, _ptr(offsets.contiguous()),
                                           ctypes.byref(pw.c), _ptr(bias), _ptr(y),
                                           _ptr(workspace), workspace.numel(), _stream(x_sorted)),
@@ -325,7 +366,7 @@ def grouped_linear(x_sorted: torch.Tensor, offsets: torch.Tensor, pw: PreparedWe
     return y
 
 
-def linear_static_scratch(x: torch.Tensor, pw: PreparedWeight, bias=None) -> torch.Tensor:
+def linear_static_scratch(x: torch.Tensor, pw: PreparedWeight, bias=None, out=None) -> torch.Tensor:
     """The layer with the library's own static scratch instead of a caller
     workspace (the library allocates nothing; calls whose kernels overlap on
     the GPU must not share it).  bf16 [m, k] -> bf16 [m, n]."""
@@ -334,7 +375,7 @@ def linear_static_scratch(x: torch.Tensor, pw: PreparedWeight, bias=None) -> tor
     if bias is not None:
         _need(bias.dtype == torch.bfloat16 and bias.numel() == pw.n, "bias must be bf16 [n]")
     x2 = x.contiguous()
-    y = torch.empty((x2.shape[0], pw.n), dtype=torch.bfloat16, device=x.device)
+    y = _out(out, (x2.shape[0], pw.n), torch.bfloat16, x.device, "out")
     _check(library().mxfp8_linear_static_scratch(_ptr(x2), x2.shape[0], ctypes.byref(pw.c), _ptr(bias),
                                                  _ptr(y), _stream(x)), "mxfp8_linear_static_scratch")
     return y
@@ -349,29 +390,29 @@ def linear_128x4_workspace_bytes(m: int, k: int) -> int:
     return library().mxfp8_linear_128x4_workspace_bytes(m, k)
 
 
-def quantize_act_128x4(x: torch.Tensor):
+def quantize_act_128x4(x: torch.Tensor, q=None, sf=None):
     """BF16 [m, k] -> (E4M3 bytes [m, k], scales in the 128x4 layout
-    [ceil128(m) * k/32])."""
+    [ceil128(m) * k/32]); q, sf: optional caller buffers."""
     _need(x.is_cuda and x.dtype == torch.bfloat16, "x must be a bfloat16 CUDA tensor")
     x2 = x.reshape(-1, x.shape[-1]).contiguous()
     m, k = x2.shape
     nsf = library().mxfp8_act_scale_bytes_128x4(m, k)
-    q = torch.empty((m, k), dtype=torch.uint8, device=x.device)
-    sf = torch.empty((max(nsf, 1),), dtype=torch.uint8, device=x.device)
+    q = _out(q, (m, k), torch.uint8, x.device, "q")
+    sf = _out(sf, (max(nsf, 1),), torch.uint8, x.device, "sf")
     _check(library().mxfp8_quantize_act_128x4(_ptr(x2), m, k, _ptr(q), _ptr(sf), _stream(x)),
            "mxfp8_quantize_act_128x4")
     return q, sf[:nsf]
 
 
-def gemm_128x4(qa: torch.Tensor, sfa: torch.Tensor, pw: PreparedWeight, bias=None) -> torch.Tensor:
+def gemm_128x4(qa: torch.Tensor, sfa: torch.Tensor, pw: PreparedWeight, bias=None, out=None) -> torch.Tensor:
     m = qa.shape[0]
-    y = torch.empty((m, pw.n), dtype=torch.bfloat16, device=qa.device)
+    y = _out(out, (m, pw.n), torch.bfloat16, qa.device, "out")
     _check(library().mxfp8_gemm_128x4(_ptr(qa.contiguous()), _ptr(sfa.contiguous()), m, ctypes.byref(pw.c),
                                       _ptr(bias), _ptr(y), _stream(qa)), "mxfp8_gemm_128x4")
     return y
 
 
-def linear_128x4(x: torch.Tensor, pw: PreparedWeight, bias=None, workspace=None) -> torch.Tensor:
+def linear_128x4(x: torch.Tensor, pw: PreparedWeight, bias=None, workspace=None, out=None) -> torch.Tensor:
     """The layer with 128x4 activation scales (the high-M variant)."""
     _need(x.is_cuda and x.dtype == torch.bfloat16, "x must be bf16 CUDA")
     lead = x.shape[:-1]
@@ -379,11 +420,11 @@ def linear_128x4(x: torch.Tensor, pw: PreparedWeight, bias=None, workspace=None)
     m = x2.shape[0]
     need = library().mxfp8_linear_128x4_workspace_bytes(m, pw.k)
     if workspace is None:
-        workspace = torch.empty((max(need, 16),), dtype=torch.uint8, device=x.device)
-    y = torch.empty((m, pw.n), dtype=torch.bfloat16, device=x.device)
+        workspace = _alloc((max(need, 16),), torch.uint8, x.device)
+    y = _out(out, (m, pw.n), torch.bfloat16, x.device, "out")
     _check(library().mxfp8_linear_128x4(_ptr(x2), m, ctypes.byref(pw.c), _ptr(bias), _ptr(y), _ptr(workspace),
                                         workspace.numel(), _stream(x)), "mxfp8_linear_128x4")
-    return y.reshape(*lead, pw.n)
+    return y.view(-1)[:m * pw.n].view(*lead, pw.n)
 
 
 # ----------------------------------------------------------------- tactics
@@ -406,8 +447,8 @@ def autotune_linear(x: torch.Tensor, pw: PreparedWeight, bias=None, iters: int =
     x2 = x.reshape(-1, x.shape[-1]).contiguous()
     m = x2.shape[0]
     if workspace is None:
-        workspace = torch.empty((max(linear_workspace_bytes(m, pw.k), 16),), dtype=torch.uint8, device=x.device)
-    y = torch.empty((m, pw.n), dtype=torch.bfloat16, device=x.device)
+        workspace = _alloc((max(linear_workspace_bytes(m, pw.k), 16),), torch.uint8, x.device)
+    y = _alloc((m, pw.n), torch.bfloat16, x.device)
     out = _tactic_array()
     _check(library().mxfp8_autotune_linear(_ptr(x2), m, ctypes.byref(pw.c), _ptr(bias), _ptr(y), _ptr(workspace),
                                            workspace.numel(), iters, _stream(x), out), "mxfp8_autotune_linear")
@@ -421,9 +462,8 @@ def autotune_grouped_linear(x_sorted: torch.Tensor, offsets: torch.Tensor, pw: P
     x2 = x_sorted.contiguous()
     rows = x2.shape[0]
     if workspace is None:
-        workspace = torch.empty((max(linear_workspace_bytes(rows, pw.k), 16),), dtype=torch.uint8,
-                                device=x_sorted.device)
-    y = torch.empty((rows, pw.n), dtype=torch.bfloat16, device=x_sorted.device)
+        workspace = _alloc((max(linear_workspace_bytes(rows, pw.k), 16),), torch.uint8, x_sorted.device)
+    y = _alloc((rows, pw.n), torch.bfloat16, x_sorted.device)
     out = _tactic_array()
     _check(library().mxfp8_autotune_grouped_linear(_ptr(x2), rows, _ptr(offsets.contiguous()), ctypes.byref(pw.c),
                                                    _ptr(bias), _ptr(y), _ptr(workspace), workspace.numel(), iters,
@@ -482,13 +522,13 @@ def moe_route(logits: torch.Tensor, topk: int, method: int = ROUTE_RENORMALIZE) 
     lg = logits.contiguous()
     t, e = lg.shape
     dev = logits.device
-    ids = torch.empty((t, topk), dtype=torch.int32, device=dev)
-    w = torch.empty((t, topk), dtype=torch.float32, device=dev)
-    off = torch.empty((e + 1,), dtype=torch.int32, device=dev)
-    stok = torch.empty((max(t * topk, 1),), dtype=torch.int32, device=dev)
-    row_of = torch.empty((max(t * topk, 1),), dtype=torch.int32, device=dev)
+    ids = _alloc((t, topk), torch.int32, dev)
+    w = _alloc((t, topk), torch.float32, dev)
+    off = _alloc((e + 1,), torch.int32, dev)
+    stok = _alloc((max(t * topk, 1),), torch.int32, dev)
+    row_of = _alloc((max(t * topk, 1),), torch.int32, dev)
     nws = library().mxfp8_moe_route_workspace_bytes(t, e, topk)
-    ws = torch.empty((max(nws, 16),), dtype=torch.uint8, device=dev)
+    ws = _alloc((max(nws, 16),), torch.uint8, dev)
     _check(library().mxfp8_moe_route(_ptr(lg), t, e, topk, method, _ptr(ids), _ptr(w), _ptr(off),
                                      _ptr(stok), _ptr(row_of), _ptr(ws), ws.numel(), _stream(logits)),
            "mxfp8_moe_route")
@@ -506,8 +546,8 @@ def prepare_gate_up_weight(w13: torch.Tensor, out: PreparedWeight = None) -> Pre
         _need((out.num_experts, out.n, out.k) == (e, n, k), "refit needs a weight of the same shape")
         pw = out
     else:
-        q = torch.empty((e, n, k), dtype=torch.uint8, device=w13.device)
-        sf = torch.empty((e, n * (k // 32)), dtype=torch.uint8, device=w13.device)
+        q = _alloc((e, n, k), torch.uint8, w13.device)
+        sf = _alloc((e, n * (k // 32)), torch.uint8, w13.device)
         pw = PreparedWeight(q, sf, n)
     dt = IN_BF16 if w3.dtype == torch.bfloat16 else IN_F32
     _check(library().mxfp8_prepare_gate_up_weight(_ptr(w3), dt, ctypes.byref(pw.c), _stream(w13)),
@@ -515,15 +555,15 @@ def prepare_gate_up_weight(w13: torch.Tensor, out: PreparedWeight = None) -> Pre
     return pw
 
 
-def moe_gate_up_swiglu(x: torch.Tensor, routing: Routing, w13: PreparedWeight) -> torch.Tensor:
+def moe_gate_up_swiglu(x: torch.Tensor, routing: Routing, w13: PreparedWeight, out=None, workspace=None) -> torch.Tensor:
     """h [t*k, I] bf16 = silu(gate) * up of GEMM1 on the expert-sorted,
     MXFP8-quantized token rows."""
     _need(x.is_cuda and x.dtype == torch.bfloat16, "x must be bf16 CUDA")
     x2 = x.contiguous()
     rows = routing.sorted_token.numel()
-    h = torch.empty((rows, w13.n // 2), dtype=torch.bfloat16, device=x.device)
+    h = _out(out, (rows, w13.n // 2), torch.bfloat16, x.device, "out")
     nws = library().mxfp8_moe_gate_up_workspace_bytes(rows, w13.k)
-    ws = torch.empty((max(nws, 16),), dtype=torch.uint8, device=x.device)
+    ws = workspace if workspace is not None else _alloc((max(nws, 16),), torch.uint8, x.device)
     _check(library().mxfp8_moe_gate_up_swiglu(_ptr(x2), _ptr(routing.sorted_token), rows,
                                               _ptr(routing.offsets), ctypes.byref(w13.c), _ptr(h),
                                               _ptr(ws), ws.numel(), _stream(x)),
@@ -531,12 +571,12 @@ def moe_gate_up_swiglu(x: torch.Tensor, routing: Routing, w13: PreparedWeight) -
     return h
 
 
-def moe_finalize(y2: torch.Tensor, routing: Routing) -> torch.Tensor:
+def moe_finalize(y2: torch.Tensor, routing: Routing, out=None) -> torch.Tensor:
     """out [t, hidden] bf16 = per token, the routing-weighted sum of its k
     expert outputs y2 [t*k, hidden] (expert-sorted rows)."""
     t, k = routing.ids.shape
     hidden = y2.shape[1]
-    out = torch.empty((t, hidden), dtype=torch.bfloat16, device=y2.device)
+    out = _out(out, (t, hidden), torch.bfloat16, y2.device, "out")
     _check(library().mxfp8_moe_finalize(_ptr(y2.contiguous()), _ptr(routing.row_of), _ptr(routing.weights),
                                         t, k, hidden, _ptr(out), _stream(y2)),
            "mxfp8_moe_finalize")
@@ -544,7 +584,7 @@ def moe_finalize(y2: torch.Tensor, routing: Routing) -> torch.Tensor:
 
 
 def moe_expert_mlp(x: torch.Tensor, logits: torch.Tensor, topk: int, w13: PreparedWeight,
-                   w2: PreparedWeight, method: int = ROUTE_RENORMALIZE, workspace=None) -> torch.Tensor:
+                   w2: PreparedWeight, method: int = ROUTE_RENORMALIZE, workspace=None, out=None) -> torch.Tensor:
     """The whole expert MLP: route -> gate_up + SwiGLU -> down -> finalize."""
     _need(x.is_cuda and x.dtype == torch.bfloat16, "x must be bf16 CUDA")
     _need(logits.is_cuda and logits.dtype == torch.float32, "logits must be float32 CUDA")
@@ -552,8 +592,8 @@ def moe_expert_mlp(x: torch.Tensor, logits: torch.Tensor, topk: int, w13: Prepar
     e = w13.num_experts
     nws = library().mxfp8_moe_workspace_bytes(t, e, topk, hdim, w13.n // 2)
     if workspace is None:
-        workspace = torch.empty((max(nws, 16),), dtype=torch.uint8, device=x.device)
-    out = torch.empty((t, hdim), dtype=torch.bfloat16, device=x.device)
+        workspace = _alloc((max(nws, 16),), torch.uint8, x.device)
+    out = _out(out, (t, hdim), torch.bfloat16, x.device, "out")
     _check(library().mxfp8_moe_expert_mlp(_ptr(x.contiguous()), _ptr(logits.contiguous()), t, topk, method,
                                           ctypes.byref(w13.c), ctypes.byref(w2.c), _ptr(out),
                                           _ptr(workspace), workspace.numel(), _stream(x)),
@@ -594,5 +634,11 @@ def set_wait_limit_ns(ns: int = 0) -> None:
 
 
 def device_error() -> int:
-    """Synchronise and read/clear the kernels' device-side timeout word."""
+    """Synchronise and read/clear the kernels' device-side error words
+    (timeout; out-of-bounds store in the debug build)."""
     return library().mxfp8_device_error()
+
+
+def debug_build() -> bool:
+    """True when the loaded library is the debug build."""
+    return bool(library().mxfp8_debug_build())

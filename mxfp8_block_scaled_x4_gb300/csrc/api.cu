@@ -14,6 +14,7 @@
 
 #include "../../include/mxfp8.h"
 #include "../../include/mxfp8_moe.h"
+#include "../../include/mxfp8_testing.h"
 #include "internal.h"
 
 namespace {
@@ -35,6 +36,14 @@ mxfp8_status cuda_fail(cudaError_t e) {
     t_last_cuda_error = static_cast<int>(e);
     return MXFP8_ERR_CUDA;
 }
+
+}  // namespace
+
+// The code mxfp8_last_cuda_error() reports on this thread (other entry
+// points of the library record their failed CUDA calls here too).
+void mxk::record_cuda_error(int e) { t_last_cuda_error = e; }
+
+namespace {
 
 // Current device must be compute capability 10.3 (GB300).
 mxfp8_status device_sms(int* sms) {
@@ -676,6 +685,7 @@ const char* mxfp8_status_string(mxfp8_status s) {
         case MXFP8_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
         case MXFP8_ERR_DEVICE_TIMEOUT: return "a kernel gave up waiting (device timeout)";
         case MXFP8_ERR_CUDA: return "CUDA error (see mxfp8_last_cuda_error)";
+        case MXFP8_ERR_OUT_OF_BOUNDS: return "a kernel computed a store index outside its buffer (debug build)";
     }
     return "unknown status";
 }
@@ -688,7 +698,23 @@ mxfp8_status mxfp8_device_error(void) {
     if (e != cudaSuccess) return cuda_fail(e);
     e = mxk::read_and_clear_gemm_error(&v);
     if (e != cudaSuccess) return cuda_fail(e);
-    return v ? MXFP8_ERR_DEVICE_TIMEOUT : MXFP8_OK;
+    unsigned int oob = 0, w = 0;
+    if ((e = mxk::read_and_clear_oob_gemm(&w)) != cudaSuccess) return cuda_fail(e);
+    oob |= w;
+    if ((e = mxk::read_and_clear_oob_quant(&w)) != cudaSuccess) return cuda_fail(e);
+    oob |= w;
+    if ((e = mxk::read_and_clear_oob_moe(&w)) != cudaSuccess) return cuda_fail(e);
+    oob |= w;
+    if (v) return MXFP8_ERR_DEVICE_TIMEOUT;
+    return oob ? MXFP8_ERR_OUT_OF_BOUNDS : MXFP8_OK;
+}
+
+int mxfp8_debug_build(void) {
+#ifdef MXFP8_DEBUG
+    return 1;
+#else
+    return 0;
+#endif
 }
 
 void mxfp8_set_wait_limit_ns(uint64_t ns) { mxk::set_wait_limit_ns(ns); }

@@ -67,6 +67,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include "debug_check.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 #include "quant_block.cuh"
@@ -748,7 +749,9 @@ __global__ void __launch_bounds__(32 * num_warps(TT, PIPES),
                     for (int j = 0; j < kCols; ++j) {
                         const float g = acc[j];
                         const float hv = g / (1.0f + expf(-g)) * xbuf[(col0 + j) * 64 + nl];
-                        if (j < jmax) hp[static_cast<size_t>(j) * inter] = __float2bfloat16_rn(hv);
+                        if (j < jmax && store_ok(static_cast<int64_t>(ti.tok0 + col0 + j) * inter + f, 1,
+                                                 static_cast<int64_t>(p.m) * inter))
+                            hp[static_cast<size_t>(j) * inter] = __float2bfloat16_rn(hv);
                     }
                     __syncwarp();
                     if (lane == 0) mbar_arrive(xempty);
@@ -758,7 +761,9 @@ __global__ void __launch_bounds__(32 * num_warps(TT, PIPES),
                 __nv_bfloat16* yp = p.y + static_cast<size_t>(ti.tok0 + col0) * p.n + n;
 #pragma unroll
                 for (int j = 0; j < kCols; ++j)
-                    if (j < jmax) yp[static_cast<size_t>(j) * p.n] = __float2bfloat16_rn(acc[j] + b);
+                    if (j < jmax && store_ok(static_cast<int64_t>(ti.tok0 + col0 + j) * p.n + n, 1,
+                                             static_cast<int64_t>(p.m) * p.n))
+                        yp[static_cast<size_t>(j) * p.n] = __float2bfloat16_rn(acc[j] + b);
             }
         }
         if (reduce) {
@@ -815,7 +820,10 @@ __global__ void __launch_bounds__(32 * num_warps(TT, PIPES),
                     __nv_bfloat16* yq = p.y + static_cast<size_t>(ti.tok0 + o0 + q * 4) * p.n + n;
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
-                        if (q * 4 + i < cmax) yq[static_cast<size_t>(i) * p.n] = __float2bfloat16_rn(sv[i] + bn);
+                        if (q * 4 + i < cmax &&
+                            store_ok(static_cast<int64_t>(ti.tok0 + o0 + q * 4 + i) * p.n + n, 1,
+                                     static_cast<int64_t>(p.m) * p.n))
+                            yq[static_cast<size_t>(i) * p.n] = __float2bfloat16_rn(sv[i] + bn);
                 }
             }
         }
@@ -1128,13 +1136,15 @@ __global__ void __launch_bounds__(kDualThreads, 1) mxfp8_gemm_dual_kernel(const 
                     for (int i = 0; i < 4; ++i) {
                         const int j = i * 8 + (lane >> 2);
                         const int part = lane & 3;
-                        if (j < jmax)
+                        if (j < jmax && store_ok(static_cast<int64_t>(ti.tok0 + c0 + j) * p.n + n0 + part * 8, 8,
+                                                 static_cast<int64_t>(p.m) * p.n))
                             *reinterpret_cast<uint4*>(p.y + static_cast<size_t>(ti.tok0 + c0 + j) * p.n + n0 + part * 8) =
                                 *reinterpret_cast<const uint4*>(blk + j * 32 + part * 8);
                     }
                 } else if (n < p.n) {
                     for (int j = 0; j < jmax; ++j)
-                        p.y[static_cast<size_t>(ti.tok0 + c0 + j) * p.n + n] = blk[j * 32 + lane];
+                        if (store_ok(static_cast<int64_t>(ti.tok0 + c0 + j) * p.n + n, 1, static_cast<int64_t>(p.m) * p.n))
+                            p.y[static_cast<size_t>(ti.tok0 + c0 + j) * p.n + n] = blk[j * 32 + lane];
                 }
                 __syncwarp();
             }
@@ -1555,6 +1565,8 @@ void set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns = ns; }
 void last_schedule(int* out5) {
     for (int i = 0; i < 5; ++i) out5[i] = t_last_schedule[i];
 }
+
+cudaError_t read_and_clear_oob_gemm(unsigned int* out) { return read_and_clear_oob_word(out); }
 
 cudaError_t read_and_clear_gemm_error(unsigned int* out) {
     unsigned int zero = 0;

@@ -91,7 +91,16 @@ void last_schedule(int* out5);
 // Limit of every pipeline wait of later GEMM launches (0 = the default).
 void set_wait_limit_ns(uint64_t ns);
 
+// Records a failed CUDA call's code for mxfp8_last_cuda_error() (this thread).
+void record_cuda_error(int e);
+
 // Reads and clears the device error word of the GEMM kernels.
 cudaError_t read_and_clear_gemm_error(unsigned int* out);
+
+// Read and clear the out-of-bounds-store words of the debug build (one per
+// kernel translation unit; always 0 in the normal build).
+cudaError_t read_and_clear_oob_gemm(unsigned int* out);
+cudaError_t read_and_clear_oob_quant(unsigned int* out);
+cudaError_t read_and_clear_oob_moe(unsigned int* out);
 
 }  // namespace mxk

@@ -23,6 +23,7 @@
 #include <string.h>
 
 #include "internal.h"
+#include "debug_check.cuh"
 #include "ptx.cuh"
 
 namespace mxk {
@@ -61,7 +62,7 @@ __device__ __forceinline__ void load_token_logits(const float* __restrict__ lg, 
 // weights.  tl holds the logits when experts <= 32 * kRegLogits.
 __device__ __forceinline__ void route_token(const float* __restrict__ lg, const TokenLogits& tl, int experts,
                                             int topk, int method, int lane, int32_t* __restrict__ ids_t,
-                                            float* __restrict__ w_t, int* sel_row) {
+                                            float* __restrict__ w_t, int* sel_row, int64_t base, int64_t extent) {
     const bool in_regs = experts <= 32 * kRegLogits;
     float pv = INFINITY;
     int pe = -1;  // previous pick; round 0 admits everything
@@ -92,7 +93,7 @@ __device__ __forceinline__ void route_token(const float* __restrict__ lg, const 
         }
         top[r] = bv;
         if (lane == 0) {
-            ids_t[r] = be;
+            if (store_ok(base + r, 1, extent)) ids_t[r] = be;  // ids_t = ids + base
             if (sel_row) sel_row[r] = be;
         }
         pv = bv;
@@ -132,7 +133,7 @@ __device__ __forceinline__ void route_token(const float* __restrict__ lg, const 
 #pragma unroll
         for (int r = 0; r < kMaxTopK; ++r)
             if (r == lane) mine = z[r];
-        w_t[lane] = mine / zs;
+        if (store_ok(base + lane, 1, extent)) w_t[lane] = mine / zs;
     }
 }
 
@@ -159,19 +160,23 @@ __global__ void __launch_bounds__(1024)
         TokenLogits tl;
         if (experts <= 32 * kRegLogits) load_token_logits(lg, experts, lane, tl);
         route_token(lg, tl, experts, topk, method, lane, ids + static_cast<size_t>(t) * topk,
-                    weights + static_cast<size_t>(t) * topk, sel[w]);
+                    weights + static_cast<size_t>(t) * topk, sel[w], static_cast<int64_t>(t) * topk,
+                    static_cast<int64_t>(tokens) * topk);
     }
     __syncthreads();
     const int live = min(32, tokens - group * 32);
     for (int i = threadIdx.x; i < live * topk; i += blockDim.x) atomicOr(&bits[sel[i / topk][i % topk]], 1u << (i / topk));
     __syncthreads();
+    const int64_t pairs = static_cast<int64_t>(tokens) * topk;
+    const int64_t groups = (tokens + 31) / 32;
     for (int i = threadIdx.x; i < live * topk; i += blockDim.x) {
         const int tw = i / topk;
-        rank[static_cast<size_t>(group * 32 + tw) * topk + (i % topk)] =
-            __popc(bits[sel[tw][i % topk]] & ((1u << tw) - 1u));
+        const int64_t o = static_cast<int64_t>(group * 32 + tw) * topk + (i % topk);
+        if (store_ok(o, 1, pairs)) rank[o] = __popc(bits[sel[tw][i % topk]] & ((1u << tw) - 1u));
     }
     for (int e = threadIdx.x; e < experts; e += blockDim.x)
-        grp_count[static_cast<size_t>(group) * experts + e] = __popc(bits[e]);
+        if (store_ok(static_cast<int64_t>(group) * experts + e, 1, groups * experts))
+            grp_count[static_cast<size_t>(group) * experts + e] = __popc(bits[e]);
 }
 
 // One CTA (thread e per expert, experts <= 1024): per-expert totals over the
@@ -211,12 +216,12 @@ __global__ void __launch_bounds__(1024)
     __syncthreads();
     const int base = incl - total + (w > 0 ? warp_sum[w - 1] : 0);
     if (e < experts) {
-        offsets[e] = base;
+        if (store_ok(e, 1, experts + 1)) offsets[e] = base;
         int run = base;
         for (int g = 0; g < groups; ++g) {
             const size_t i = static_cast<size_t>(g) * experts + e;
             const int c = grp[i];
-            grp[i] = run;
+            if (store_ok(static_cast<int64_t>(i), 1, static_cast<int64_t>(groups) * experts)) grp[i] = run;
             run += c;
         }
     }
@@ -226,8 +231,8 @@ __global__ void __launch_bounds__(1024)
     for (int i = threadIdx.x; i < pairs; i += blockDim.x) {
         const int t = i / topk;
         const int r = grp[static_cast<size_t>(t >> 5) * experts + ids[i]] + rank[i];
-        row_of[i] = r;
-        sorted_token[r] = t;
+        if (store_ok(i, 1, pairs)) row_of[i] = r;
+        if (store_ok(r, 1, pairs)) sorted_token[r] = t;
     }
 }
 
@@ -268,11 +273,14 @@ __global__ void __launch_bounds__(kFinThreads)
             const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * i + 1]));
             o[i] = lo | (hi << 16);
         }
-        *reinterpret_cast<uint4*>(out + t * hidden + c0) = make_uint4(o[0], o[1], o[2], o[3]);
+        if (store_ok(t * hidden + c0, 8, tokens * hidden))
+            *reinterpret_cast<uint4*>(out + t * hidden + c0) = make_uint4(o[0], o[1], o[2], o[3]);
     }
 }
 
 }  // namespace
+
+cudaError_t read_and_clear_oob_moe(unsigned int* out) { return read_and_clear_oob_word(out); }
 
 // The routing kernels are launched with programmatic stream serialization so
 // that their launch overlaps the previous kernel (they wait for it before

@@ -22,6 +22,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "debug_check.cuh"
 #include "quant_block.cuh"
 
 namespace mxk {
@@ -97,18 +98,20 @@ __global__ void __launch_bounds__(kThreads) quant_act_kernel(const __nv_bfloat16
             if (t >= total) break;  // warp-uniform
             uint32_t qq[8];
             const uint32_t s = quantize_block32(raw[u], qq);
-            if (row[u] < m) {
+            if (row[u] < m && store_ok(row[u] * k + col[u], 32, m * k)) {
                 uint4* dst = reinterpret_cast<uint4*>(q + row[u] * k + col[u]);
                 dst[0] = make_uint4(qq[0], qq[1], qq[2], qq[3]);
                 dst[1] = make_uint4(qq[4], qq[5], qq[6], qq[7]);
             }
+            const int64_t sf_extent = m8 * (k >> 5);  // 8x4: ceil8(m) rows; 128x4: ceil128(m) rows
             if constexpr (!kLayout128) {
-                sf[t * 32 + lane] = static_cast<uint8_t>(s);  // 8x4 tile (g, quad) = t
+                if (store_ok(t * 32 + lane, 1, sf_extent))
+                    sf[t * 32 + lane] = static_cast<uint8_t>(s);  // 8x4 tile (g, quad) = t
             } else {
                 const int64_t g = t / quads;
                 const int64_t r = row[u];
-                sf[((r >> 7) * quads + (t - g * quads)) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 + b4] =
-                    static_cast<uint8_t>(s);
+                const int64_t o = ((r >> 7) * quads + (t - g * quads)) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 + b4;
+                if (store_ok(o, 1, sf_extent)) sf[o] = static_cast<uint8_t>(s);
             }
         }
     }
@@ -159,13 +162,14 @@ __global__ void __launch_bounds__(kThreads)
         uint32_t s;
         quantize_lane8(v, qq, s);
         const uint32_t word = gather_scale_word(s);
-        st_v2(q + rowp * k + chunk * 256 + lane * 8, qq);  // zero bytes for padding rows
+        if (store_ok(rowp * k + chunk * 256 + lane * 8, 8, experts * n_pad * k))
+            st_v2(q + rowp * k + chunk * 256 + lane * 8, qq);  // zero bytes for padding rows
         if ((lane & 15) == 0) {
             const int64_t grp = chunk * 2 + (lane >> 4);
             const int64_t tile = e * (n_pad >> 7) + (r >> 7);
             const int64_t rr = r & 127;
-            *reinterpret_cast<uint32_t*>(sf + (tile * kq + grp) * 512 + (rr & 31) * 16 +
-                                         (rr >> 5) * 4) = word;
+            const int64_t o = (tile * kq + grp) * 512 + (rr & 31) * 16 + (rr >> 5) * 4;
+            if (store_ok(o, 4, experts * n_pad * (k >> 5))) *reinterpret_cast<uint32_t*>(sf + o) = word;
         }
     }
 }
@@ -180,6 +184,8 @@ int grid_for(int64_t warps_of_work, int num_sms, int per_warp) {
 }
 
 }  // namespace
+
+cudaError_t read_and_clear_oob_quant(unsigned int* out) { return read_and_clear_oob_word(out); }
 
 cudaError_t launch_quant_act(const void* x, int64_t m, int64_t k, uint8_t* q, uint8_t* sf,
                              int num_sms, cudaStream_t s, const int32_t* src_rows, bool layout_128x4) {

@@ -24,7 +24,7 @@
  *    floor(log2(amax)) - emax(E4M3)=8) follow the public OCP Microscaling
  *    Formats (MX) v1.0 specification, which the pages name by format only.
  *
- * Readings where the pages are silent (each one is listed in the design doc):
+ * Readings where the pages are silent (labels S1-S12 of the readings):
  *  S1 scale rule (A) = OCP floor rule; rule (B) = smallest power of two that
  *     avoids saturation, kept behind a flag and not used by the layer.
  *  S2 an all-zero block gets scale byte 0x00; its elements keep their sign.
