@@ -371,7 +371,7 @@ void encode_tactic(const mxk::GemmSchedule& s, int32_t* t4) {
     t4[3] = s.dual ? 2 : s.pipes;  // the dual kernel always runs two MMA issuers
 }
 bool decode_tactic(const int32_t* t4, int kind, int64_t k, mxk::GemmSchedule* s) {
-    s->dual = (t4[0] == 192 || t4[0] == 160) && t4[1] == -1;
+    s->dual = (t4[0] == 192 || t4[0] == 176 || t4[0] == 160 || t4[0] == 144) && t4[1] == -1;
     s->tokens_per_tile = t4[0];
     s->persistent = t4[1] == -1;
     s->split_k = s->persistent ? 1 : t4[1];
@@ -729,7 +729,8 @@ void mxfp8_set_schedule(int tokens_per_tile, int split_k, int fuse_quant) {
     // 160 / 192: the dual weight-tile schedule (dense, persistent).
     const bool tt_ok = tokens_per_tile == 0 || tokens_per_tile == 16 || tokens_per_tile == 32 ||
                        tokens_per_tile == 64 || tokens_per_tile == 128 || tokens_per_tile == 256 ||
-                       tokens_per_tile == 160 || tokens_per_tile == 192;
+                       tokens_per_tile == 144 || tokens_per_tile == 160 || tokens_per_tile == 176 ||
+                       tokens_per_tile == 192;
     g_force_tt.store(tt_ok ? tokens_per_tile : 0, std::memory_order_relaxed);
     g_force_split.store((split_k >= -1 && split_k <= 8) ? split_k : 0, std::memory_order_relaxed);
     g_force_fuse.store((fuse_quant >= -1 && fuse_quant <= 1) ? fuse_quant : -1, std::memory_order_relaxed);

@@ -418,9 +418,17 @@ __device__ __forceinline__ void run_reorder(const GemmArgs& p, const Ctx& c, int
 template <int TT, int PIPES>
 __device__ __forceinline__ void run_fused_quant(const GemmArgs& p, const Ctx& c, int ew, int lane) {
     using G = Geometry<TT>;
-    pdl_wait();
     const TileInfo ti = decode_tile<TT>(c.tile_first, p, c.prefix, c.offs);
     const int nk = c.kb_end - c.kb_begin;
+    // While the previous grid still runs, pull this CTA's K slice of x into
+    // L2 (one bulk prefetch per token row, spread over the epilogue warps, so
+    // the producer's weight loads are not delayed).  A prefetch only warms
+    // L2, which every write reaches first: the loads below, issued after the
+    // wait, still see what the previous grid wrote.
+    for (int r = ew * 32 + lane; r < ti.count; r += epi_warps(TT) * 32)
+        prefetch_l2_bulk(p.x + static_cast<size_t>(ti.tok0 + r) * p.k + c.kb_begin * 128,
+                         static_cast<uint32_t>(nk) * 256u);
+    pdl_wait();
     const int S = c.stages;
     constexpr int kEpi = epi_warps(TT);
     constexpr int kPatches = TT / 8;  // per K block
@@ -851,7 +859,8 @@ __global__ void __launch_bounds__(32 * num_warps(TT, PIPES),
 
 // ------------------------------------------------------- dual-tile kernel
 // Large-M dense schedule.  A CTA tile is two adjacent 128-row weight tiles
-// (256 output features) x TT tokens.  The token tile and its scales are loaded
+// (256 output features) x TT tokens (TT = 144, 160, 176 or 192; a multiple
+// of 16, the MMA's N step, and of 8, the activation scale groups).  The token tile and its scales are loaded
 // once per K block and serve both weight tiles; one MMA-issuing thread per
 // weight tile runs over all K blocks into its own TMEM accumulator.  Both
 // issuers feed the same tensor core, so together they keep it busy although
@@ -1118,8 +1127,20 @@ __global__ void __launch_bounds__(kDualThreads, 1) mxfp8_gemm_dual_kernel(const 
             const uint32_t taddr = tmem_base + q * TT + (static_cast<uint32_t>(quad * 32) << 16);
 #pragma unroll 1
             for (int c0 = 0; c0 < TT; c0 += 32) {
+                // 32 columns at a time; a tile width that is an odd multiple
+                // of 16 ends with a 16-column load, so no load reaches past
+                // this accumulator's own columns.
                 uint32_t r[32];
-                tmem_load_32(taddr + c0, r);
+                if (TT % 32 == 0 || c0 + 32 <= TT) {
+                    tmem_load_32(taddr + c0, r);
+                } else {
+                    uint32_t r16[16];
+                    tmem_load_16(taddr + c0, r16);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) r[i] = r16[i];
+#pragma unroll
+                    for (int i = 16; i < 32; ++i) r[i] = 0u;
+                }
                 tmem_load_wait();
                 if (c0 + 32 >= TT) {  // accumulator fully read: the issuer may go on
                     tc_fence_before();
@@ -1445,17 +1466,29 @@ GemmSchedule choose_schedule(const GemmProblem& p, int num_sms, int force_tt, in
     }
     if (force_tt) tt = force_tt;
     if (p.gated && tt > 128) tt = 128;  // the gated exchange buffer holds 64 x TT FP32
-    // Dense large M: two weight tiles x 192 tokens per CTA tile whenever that
-    // still gives every SM a tile (measured on 8192^3).  160-token tiles
-    // leave a fuller last wave there (1664 tiles = 10.95 waves of 152,
-    // against 1376 = 9.05) but measured slower (409 against 393 us): the
-    // narrower MMAs cost more issue per FLOP.  They stay a tactic.
+    // Dense large M: two weight tiles x TT tokens per CTA tile whenever that
+    // still gives every SM a tile.  TT is the width with the least predicted
+    // time, waves x (fixed + per-token cost of a tile): on 8192^3 a tile of
+    // TT tokens measured about 27 us + 0.0625 us x TT (192: 391 us in 10
+    // waves, 176: 382 us in 10, 160: 406 us in 11, 144: 433 us in 12), i.e.
+    // a fixed cost worth ~434 tokens.  So 176-token tiles win there (1504
+    // tiles = 9.9 waves of 152, against 1376 = 9.05 for 192).
     bool dual = false;
     int dual_tt = 192;
     if (p.offsets == nullptr && !p.gated && !p.sf128 && tt == 256 && force_tt == 0 &&
-        ((p.n_pad / 128 + 1) / 2) * ((p.m + 191) / 192) >= num_sms)
+        ((p.n_pad / 128 + 1) / 2) * ((p.m + 191) / 192) >= num_sms) {
         dual = true;
-    if (p.offsets == nullptr && (force_tt == 192 || force_tt == 160)) { dual = true; dual_tt = force_tt; }
+        int64_t best = -1;
+        for (int w : {192, 176, 160}) {
+            const int64_t tiles = ((p.n_pad / 128 + 1) / 2) * ((p.m + w - 1) / w);
+            const int64_t cost = ((tiles + num_sms - 1) / num_sms) * (434 + w);
+            if (best < 0 || cost < best) { best = cost; dual_tt = w; }
+        }
+    }
+    if (p.offsets == nullptr && (force_tt == 192 || force_tt == 176 || force_tt == 160 || force_tt == 144)) {
+        dual = true;
+        dual_tt = force_tt;
+    }
     if (dual) tt = dual_tt;
     bool persistent = p.offsets != nullptr || tt > 128;
     int split = 1;
@@ -1508,8 +1541,12 @@ cudaError_t launch_gemm(const GemmProblem& p, const GemmSchedule& sch, int num_s
                         bool* encode_failed) {
     *encode_failed = false;
     if (sch.dual) {
-        if (sch.tokens_per_tile == 160) return launch_dual<160>(p, num_sms, s, encode_failed);
-        return launch_dual<192>(p, num_sms, s, encode_failed);
+        switch (sch.tokens_per_tile) {
+            case 144: return launch_dual<144>(p, num_sms, s, encode_failed);
+            case 160: return launch_dual<160>(p, num_sms, s, encode_failed);
+            case 176: return launch_dual<176>(p, num_sms, s, encode_failed);
+            default: return launch_dual<192>(p, num_sms, s, encode_failed);
+        }
     }
     if (p.gated && p.sf128) return cudaErrorInvalidValue;
     if (p.gated) {  // grouped SwiGLU: tiles of <= 128 tokens

@@ -36,6 +36,14 @@ ScratchSlot g_slot[64];
 std::mutex g_slot_mu;
 thread_local int t_static_cuda_error = 0;
 
+// A failed CUDA call: its code goes to both mxfp8_static_scratch_last_cuda_error()
+// and mxfp8_last_cuda_error(), as for every other entry point.
+mxfp8_status cuda_error(cudaError_t e) {
+    t_static_cuda_error = static_cast<int>(e);
+    mxk::record_cuda_error(static_cast<int>(e));
+    return MXFP8_ERR_CUDA;
+}
+
 int64_t round_up(int64_t v, int64_t q) { return (v + q - 1) / q * q; }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -45,7 +53,7 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 mxfp8_status scratch_for_current_device(uint8_t** ptr, int* sms) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) { t_static_cuda_error = static_cast<int>(e); return MXFP8_ERR_CUDA; }
+    if (e != cudaSuccess) return cuda_error(e);
     if (dev < 0 || dev >= 64) return MXFP8_ERR_UNSUPPORTED_DEVICE;
     std::lock_guard<std::mutex> lock(g_slot_mu);
     ScratchSlot& s = g_slot[dev];
@@ -53,17 +61,12 @@ mxfp8_status scratch_for_current_device(uint8_t** ptr, int* sms) {
         int major = 0, minor = 0, count = 0;
         if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
             (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
-            (e = cudaDeviceGetAttribute(&count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) {
-            t_static_cuda_error = static_cast<int>(e);
-            return MXFP8_ERR_CUDA;
-        }
+            (e = cudaDeviceGetAttribute(&count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return cuda_error(e);
         if (major != 10 || minor != 3) return MXFP8_ERR_UNSUPPORTED_DEVICE;
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_static_scratch);
-        if (e != cudaSuccess || p == nullptr) {
-            t_static_cuda_error = static_cast<int>(e);
-            return MXFP8_ERR_CUDA;
-        }
+        if (e != cudaSuccess || p == nullptr) return cuda_error(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
         s.ptr = static_cast<uint8_t*>(p);
         s.sms = count;
         s.ready = true;
@@ -102,7 +105,7 @@ extern "C" mxfp8_status mxfp8_linear_static_scratch(const void* x, int64_t m, co
     uint8_t* qa = scratch;
     uint8_t* sfa = scratch + q_bytes;
     cudaError_t e = mxk::launch_quant_act(x, m, w->k, qa, sfa, sms, s);
-    if (e != cudaSuccess) { t_static_cuda_error = static_cast<int>(e); return MXFP8_ERR_CUDA; }
+    if (e != cudaSuccess) return cuda_error(e);
 
     mxk::GemmProblem p;
     p.qa = qa;
@@ -120,11 +123,18 @@ extern "C" mxfp8_status mxfp8_linear_static_scratch(const void* x, int64_t m, co
     p.x = nullptr;  // the GEMM reads the quantized activations from the array
     p.gated = false;
     p.sf128 = false;
-    const mxk::GemmSchedule sch = mxk::choose_schedule(p, sms, 0, 0, 0);
+    // The schedule of an unfused mxfp8_linear call of this class: a stored
+    // tactic if the table holds an unfused one for it, else the built-in
+    // heuristic with quantization not fused.
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_error(e);
+    mxk::GemmSchedule sch;
+    if (!mxk::tactic_lookup(dev, mxk::kTacticLinear, m, w->n, w->k, 1, &sch) || sch.fuse_quant)
+        sch = mxk::choose_schedule(p, sms, 0, 0, 0);
     bool enc_fail = false;
     e = mxk::launch_gemm(p, sch, sms, s, &enc_fail);
     if (enc_fail) return MXFP8_ERR_INVALID_ARG;
-    if (e != cudaSuccess) { t_static_cuda_error = static_cast<int>(e); return MXFP8_ERR_CUDA; }
+    if (e != cudaSuccess) return cuda_error(e);
     return MXFP8_OK;
 }
 

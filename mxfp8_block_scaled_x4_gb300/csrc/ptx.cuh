@@ -98,6 +98,15 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
         : "memory");
 }
 
+// Prefetch `bytes` of global memory at `src` into L2 (16-B aligned address,
+// size % 16 == 0).  A hint: it moves no data into this CTA and orders
+// nothing; L2 is the GPU's point of coherence, so a later write by any
+// kernel still lands in the prefetched lines.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
+                 : "memory");
+}
+
 // L2 eviction-priority policies (createpolicy.fractional, fraction 1.0).
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;

@@ -46,7 +46,9 @@ int64_t m_bucket(int64_t m) {
 bool schedule_valid(const GemmSchedule& s, int kind, int64_t k) {
     const int tt = s.tokens_per_tile;
     const bool grouped = kind == kTacticGrouped || kind == kTacticGated;
-    if (s.dual) return (kind == kTacticLinear || kind == kTacticGemm) && (tt == 160 || tt == 192) && s.pipes == 2;
+    if (s.dual)
+        return (kind == kTacticLinear || kind == kTacticGemm) && (tt == 144 || tt == 160 || tt == 176 || tt == 192) &&
+               s.pipes == 2;
     if (tt != 16 && tt != 32 && tt != 64 && tt != 128 && tt != 256) return false;
     if (s.pipes == 2 && tt > 64) return false;
     if (s.pipes == 4 && tt != 16) return false;
@@ -112,8 +114,7 @@ std::vector<GemmSchedule> candidate_schedules(int kind, int64_t m, int64_t k) {
             }
     }
     if (!grouped && m > 128) {
-        add(192, 1, true, false, 2, true);
-        add(160, 1, true, false, 2, true);
+        for (int tt : {192, 176, 160, 144}) add(tt, 1, true, false, 2, true);
     }
     return out;
 }

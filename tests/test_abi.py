@@ -218,8 +218,11 @@ def test_heuristic_schedules_on_the_workloads(mx):
         ((L, 128, 130, 4096, 1), (64, 4, 0, 2)),
         # tiny: K = 256 is two K blocks, so no split
         ((L, 7, 130, 256, 1), (16, 1, 1, 2)),
-        # prefill: two weight tiles x 192 tokens, persistent
-        ((L, 8192, 8192, 8192, 1), (192, -1, 0, 2)),
+        # prefill: two weight tiles x 176 tokens, persistent (1504 tiles =
+        # 9.9 waves of 152; the tile-cost model prefers it to 192 tokens)
+        ((L, 8192, 8192, 8192, 1), (176, -1, 0, 2)),
+        # M = 4096: 192-token tiles (704 tiles = 4.6 waves; 176 would need 6)
+        ((L, 4096, 8192, 8192, 1), (192, -1, 0, 2)),
         # large M but too few tiles for the dual kernel: persistent 256
         ((L, 1024, 256, 1024, 1), (256, -1, 0, 1)),
         # grouped: mean segment 16 rows -> 32-token tiles, two pipes

@@ -101,7 +101,7 @@ def test_multi_pipe_schedules(lib, tt, split, fuse, pipes):
     _run_dense(lib, d, schedule=(tt, split, fuse), pipes=pipes)
 
 
-@pytest.mark.parametrize("tt", [192, 160])
+@pytest.mark.parametrize("tt", [192, 176, 160, 144])
 @pytest.mark.parametrize("m,n,k", [(300, 300, 1024), (1000, 640, 512), (193, 128, 256), (161, 256, 512)])
 def test_dual_weight_tile_schedule(lib, m, n, k, tt):
     """Two weight tiles x 160 or 192 tokens per CTA tile (the large-M

@@ -29,7 +29,7 @@ def _dense(mx, d):
 
 def _schedule_matches(sched, tactic):
     tt, split, fuse, pipes = tactic
-    if tt in (160, 192):
+    if tt in (144, 160, 176, 192):
         return sched["split"] == -2
     return (sched["tokens_per_tile"] == tt and sched["pipes"] == pipes and sched["split"] == split
             and int(sched["fused"]) == fuse)
