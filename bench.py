@@ -709,8 +709,11 @@ def measure_configs(mx, wl, peaks):
     cfgs["moe_mlp_t256_e128_top8_h2048_i768"] = measure_moe(mx, peaks, 200)
     cfgs["decode_m16_n5120_k2048_autotuned"] = measure_config(mx, "d16", wl["decode16"], peaks, 4000, tune=True)
     cfgs["mid_m128_n2048_k4096_autotuned"] = measure_config(mx, "mid", wl["mid"], peaks, 2000, tune=True)
-    for v in cfgs.values():
+    for name, v in cfgs.items():
         v["peaks"] = "of %s" % peaks["source"]
+        # DRAM bytes of one GEMM launch from the committed ncu capture of this
+        # workload (None when absent or captured on other kernel sources)
+        v["traffic"] = load_traffic("gemm", name)
     return cfgs
 
 
