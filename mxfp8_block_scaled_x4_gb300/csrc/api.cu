@@ -171,6 +171,8 @@ static mxk::GemmProblem make_problem(const void* qa, const void* sfa, int64_t m,
     p.x = x;
     p.gated = false;
     p.sf128 = false;
+    p.hq = nullptr;
+    p.hsf = nullptr;
     return p;
 }
 
@@ -499,6 +501,8 @@ mxfp8_status mxfp8_plan_tactic(int kind, int64_t m, int64_t n, int64_t k, int64_
     p.x = kind == mxk::kTacticLinear ? kPresent : nullptr;
     p.gated = kind == mxk::kTacticGated;
     p.sf128 = false;
+    p.hq = nullptr;
+    p.hsf = nullptr;
     encode_tactic(select_schedule(p, sms, kind), tactic);
     return MXFP8_OK;
 }
@@ -564,6 +568,26 @@ mxfp8_status mxfp8_prepare_gate_up_weight(const void* src, mxfp8_in_dtype dtype,
 
 size_t mxfp8_moe_gate_up_workspace_bytes(int64_t rows, int64_t k) { return mxfp8_linear_workspace_bytes(rows, k); }
 
+// Gather-quantize the expert-sorted rows of x, then GEMM1 with the SwiGLU
+// epilogue: h as BF16 into h, or (hq != null) quantized to MXFP8 into hq and
+// its 8x4 scales into hsf.  Arguments checked by the callers.
+static mxfp8_status gate_up_launch(const void* x, const int32_t* sorted_token, int64_t rows,
+                                   const int32_t* expert_offsets, const mxfp8_weight* w13, void* h, uint8_t* hq,
+                                   uint8_t* hsf, void* ws, int sms, cudaStream_t s) {
+    uint8_t* qa = static_cast<uint8_t*>(ws);
+    uint8_t* sfa = qa + ceil_to(rows * w13->k, 256);
+    cudaError_t e = mxk::launch_quant_act(x, rows, w13->k, qa, sfa, sms, s, sorted_token);
+    if (e != cudaSuccess) return cuda_fail(e);
+    mxk::GemmProblem p = make_problem(qa, sfa, rows, w13, nullptr, h, expert_offsets, nullptr);
+    p.gated = true;
+    p.hq = hq;
+    p.hsf = hsf;
+    const mxk::GemmSchedule sch = select_schedule(p, sms, mxk::kTacticGated);
+    bool enc_fail = false;
+    e = mxk::launch_gemm(p, sch, sms, s, &enc_fail);
+    return launch_status(e, enc_fail);
+}
+
 mxfp8_status mxfp8_moe_gate_up_swiglu(const void* x, const int32_t* sorted_token, int64_t rows,
                                       const int32_t* expert_offsets, const mxfp8_weight* w13, void* h, void* ws,
                                       size_t ws_bytes, void* stream) {
@@ -578,17 +602,8 @@ mxfp8_status mxfp8_moe_gate_up_swiglu(const void* x, const int32_t* sorted_token
     if (ws_bytes < mxfp8_moe_gate_up_workspace_bytes(rows, w13->k)) return MXFP8_ERR_WORKSPACE_TOO_SMALL;
     int sms = 0;
     if ((st = device_sms(&sms)) != MXFP8_OK) return st;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    uint8_t* qa = static_cast<uint8_t*>(ws);
-    uint8_t* sfa = qa + ceil_to(rows * w13->k, 256);
-    cudaError_t e = mxk::launch_quant_act(x, rows, w13->k, qa, sfa, sms, s, sorted_token);
-    if (e != cudaSuccess) return cuda_fail(e);
-    mxk::GemmProblem p = make_problem(qa, sfa, rows, w13, nullptr, h, expert_offsets, nullptr);
-    p.gated = true;
-    const mxk::GemmSchedule sch = select_schedule(p, sms, mxk::kTacticGated);
-    bool enc_fail = false;
-    e = mxk::launch_gemm(p, sch, sms, s, &enc_fail);
-    return launch_status(e, enc_fail);
+    return gate_up_launch(x, sorted_token, rows, expert_offsets, w13, h, nullptr, nullptr, ws, sms,
+                          static_cast<cudaStream_t>(stream));
 }
 
 mxfp8_status mxfp8_moe_finalize(const void* y2, const int32_t* row_of, const float* topk_weights,
@@ -666,12 +681,28 @@ mxfp8_status mxfp8_moe_expert_mlp(const void* x, const float* logits, int64_t to
     st = mxfp8_moe_route(logits, tokens, experts, topk, method, ids, wts, off, stok, row_of, b + l.route,
                          mxfp8_moe_route_workspace_bytes(tokens, experts, topk), stream);
     if (st != MXFP8_OK) return st;
-    st = mxfp8_moe_gate_up_swiglu(x, stok, r, off, w13, b + l.h, b + l.g1, mxfp8_linear_workspace_bytes(r, hidden),
-                                  stream);
+    // GEMM1's SwiGLU epilogue writes h already quantized (E4M3 + 8x4 scales,
+    // the bytes the activation quantizer would make of the BF16 h) into the
+    // GEMM2 activation buffers, so GEMM2 runs on them directly.
+    int sms = 0;
+    if ((st = device_sms(&sms)) != MXFP8_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* hq = b + l.g2;
+    uint8_t* hsf = hq + ceil_to(r * inter, 256);
+    if (r % 8 != 0) {
+        // Rows r..ceil8(r)-1 of h's last 8-row scale group hold 0x00, as the
+        // quantizer writes them: clear that group; GEMM1 then fills rows < r.
+        const int64_t grp = ceil_to(inter / 32, 4) * 8;
+        cudaError_t e = cudaMemsetAsync(hsf + (r / 8) * grp, 0, static_cast<size_t>(grp), s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    st = gate_up_launch(x, stok, r, off, w13, nullptr, hq, hsf, b + l.g1, sms, s);
     if (st != MXFP8_OK) return st;
-    st = mxfp8_grouped_linear(b + l.h, r, off, w2, nullptr, b + l.y2, b + l.g2, mxfp8_linear_workspace_bytes(r, inter),
-                              stream);
-    if (st != MXFP8_OK) return st;
+    mxk::GemmProblem p2 = make_problem(hq, hsf, r, w2, nullptr, b + l.y2, off, nullptr);
+    const mxk::GemmSchedule sch2 = select_schedule(p2, sms, mxk::kTacticGrouped);
+    bool enc_fail = false;
+    cudaError_t e = mxk::launch_gemm(p2, sch2, sms, s, &enc_fail);
+    if ((st = launch_status(e, enc_fail)) != MXFP8_OK) return st;
     return mxfp8_moe_finalize(b + l.y2, row_of, wts, tokens, topk, hidden, out, stream);
 }
 

@@ -104,6 +104,8 @@ struct GemmArgs {
     int num_tiles;           // dense (grouped counts tiles on the device)
     uint32_t tmem_cols;
     uint64_t wait_ns;        // limit of every pipeline wait
+    uint8_t* hq;             // gated: h quantized to MXFP8 (E4M3 [m][n/2]) instead of BF16 y, or null
+    uint8_t* hsf;            // gated: its 8x4 scales
 };
 
 template <int TT>
@@ -551,7 +553,10 @@ __global__ void __launch_bounds__(32 * num_warps(TT, PIPES),
     // Gated epilogue: the up half of each tile's accumulator passes through
     // xbuf [TT columns][64 rows] FP32 to the gate half.
     float* xbuf = reinterpret_cast<float*>(partial + (reduce ? splits * per * 512 : 0));
-    uint8_t* ctrl = reinterpret_cast<uint8_t*>(xbuf) + (kGated ? 64 * TT * 4 : 0);
+    // Gated epilogue quantizing h (p.hq): one [tokens][80 bytes] BF16 block per
+    // gate-half warp, 2 x TT rows in all.
+    uint8_t* hbuf = reinterpret_cast<uint8_t*>(xbuf) + (kGated ? 64 * TT * 4 : 0);
+    uint8_t* ctrl = hbuf + (kGated ? 160 * TT : 0);
     Ctx c;
     c.smem = smem;
     c.full = reinterpret_cast<uint64_t*>(ctrl);
@@ -752,14 +757,53 @@ __global__ void __launch_bounds__(32 * num_warps(TT, PIPES),
                     if (!okx) { if (lane == 0) record_timeout(c.abort_flag); break; }
                     const int f = ti.n_tile * 64 + nl;
                     const int jmax = min(kCols, ti.count - col0);
-                    __nv_bfloat16* hp = p.y + static_cast<size_t>(ti.tok0 + col0) * inter + f;
+                    if (p.hq != nullptr) {
+                        // h goes straight to MXFP8 for the next GEMM, exactly as
+                        // the activation quantizer turns the BF16 h: this warp's
+                        // 32 features (one K block of h, f/32) x its tokens are
+                        // written to its shared-memory block as BF16, one
+                        // 80-byte row per token (16-byte reads of different rows
+                        // then hit different banks), and lane l quantizes token
+                        // row l with quant_block.cuh's routine: two 16-byte
+                        // stores of E4M3 bytes and one scale byte (8x4 layout).
+                        uint8_t* tp = hbuf + ((quad & 1) + 2 * half) * (kCols * 80);
 #pragma unroll
-                    for (int j = 0; j < kCols; ++j) {
-                        const float g = acc[j];
-                        const float hv = g / (1.0f + expf(-g)) * xbuf[(col0 + j) * 64 + nl];
-                        if (j < jmax && store_ok(static_cast<int64_t>(ti.tok0 + col0 + j) * inter + f, 1,
-                                                 static_cast<int64_t>(p.m) * inter))
-                            hp[static_cast<size_t>(j) * inter] = __float2bfloat16_rn(hv);
+                        for (int j = 0; j < kCols; ++j) {
+                            const float g = acc[j];
+                            const float hv = g / (1.0f + expf(-g)) * xbuf[(col0 + j) * 64 + nl];
+                            *reinterpret_cast<unsigned short*>(tp + j * 80 + lane * 2) =
+                                __bfloat16_as_ushort(__float2bfloat16_rn(hv));
+                        }
+                        __syncwarp();
+                        const int kb = inter >> 5;
+                        const int fb = f - lane;  // first feature of the block
+                        const int b = fb >> 5;
+                        for (int jj = lane; jj < jmax; jj += 32) {
+                            const uint4* src = reinterpret_cast<const uint4*>(tp + jj * 80);
+                            const uint4 raw[4] = {src[0], src[1], src[2], src[3]};
+                            uint32_t qq[8];
+                            const uint32_t sc = quantize_block32(raw, qq);
+                            const int64_t row = ti.tok0 + col0 + jj;
+                            if (store_ok(row * inter + fb, 32, static_cast<int64_t>(p.m) * inter)) {
+                                uint4* dst = reinterpret_cast<uint4*>(p.hq + row * inter + fb);
+                                dst[0] = make_uint4(qq[0], qq[1], qq[2], qq[3]);
+                                dst[1] = make_uint4(qq[4], qq[5], qq[6], qq[7]);
+                            }
+                            const int64_t o = ((row >> 3) * (kb >> 2) + (b >> 2)) * 32 + (row & 7) * 4 + (b & 3);
+                            if (store_ok(o, 1, ((static_cast<int64_t>(p.m) + 7) >> 3) * 8 * kb))
+                                p.hsf[o] = static_cast<uint8_t>(sc);
+                        }
+                        __syncwarp();  // the block is rewritten for the next tile
+                    } else {
+                        __nv_bfloat16* hp = p.y + static_cast<size_t>(ti.tok0 + col0) * inter + f;
+#pragma unroll
+                        for (int j = 0; j < kCols; ++j) {
+                            const float g = acc[j];
+                            const float hv = g / (1.0f + expf(-g)) * xbuf[(col0 + j) * 64 + nl];
+                            if (j < jmax && store_ok(static_cast<int64_t>(ti.tok0 + col0 + j) * inter + f, 1,
+                                                     static_cast<int64_t>(p.m) * inter))
+                                hp[static_cast<size_t>(j) * inter] = __float2bfloat16_rn(hv);
+                        }
                     }
                     __syncwarp();
                     if (lane == 0) mbar_arrive(xempty);
@@ -1236,7 +1280,7 @@ LaunchPlan plan_for(int splits, bool persistent, int kq, bool gated) {
     // one-tile CTA never needs more than its K blocks).
     const int ctrl = 8 * 64 + 8 + 4 * 2 * (kMaxExperts + 1) + 64;  // barriers, slots, prefix/offsets
     lp.partial = splits > 1 ? splits * tokens_per_owner(TT, splits) * 512 : 0;
-    const int xbuf = gated ? 64 * TT * 4 : 0;
+    const int xbuf = gated ? 64 * TT * 4 + 160 * TT : 0;  // up-half exchange + h quantization blocks
     const int budget = 227 * 1024 - 1024 - ctrl - lp.partial - xbuf;
     int stages = budget / (PIPES * G::kStageBytes);
     if (stages * PIPES > 8) stages = 8 / PIPES;
@@ -1309,6 +1353,8 @@ cudaError_t launch_tt(const GemmProblem& pr, const GemmSchedule& sch, int num_sm
     a.splits = splits;
     a.persistent = sch.persistent ? 1 : 0;
     a.asf128 = pr.sf128 ? pr.sfa : nullptr;
+    a.hq = pr.gated ? pr.hq : nullptr;
+    a.hsf = pr.gated ? pr.hsf : nullptr;
     a.stages = lp.stages;
     a.tmem_cols = lp.tmem_cols;
     a.wait_ns = g_wait_limit_ns ? g_wait_limit_ns : kWaitNs;

@@ -46,6 +46,8 @@ struct GemmProblem {
     const int32_t* offsets;    // grouped: device [experts + 1]; dense: null
     const void* x;             // bf16 [m][k] activations when the GEMM may quantize them itself
     bool gated;                // grouped only: SwiGLU epilogue, y = silu(gate) * up, bf16 [m][n/2]
+    uint8_t* hq;               // gated only, or null: write h quantized to MXFP8 instead of BF16 y:
+    uint8_t* hsf;              //   E4M3 [m][n/2] and its 8x4 scales (rows past m untouched)
     bool sf128;                // sfa uses the 128x4 layout (dense, persistent tiles of 128/256 tokens)
 };
 

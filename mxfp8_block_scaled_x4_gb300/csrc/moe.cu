@@ -147,8 +147,10 @@ __global__ void __launch_bounds__(1024)
                       int32_t* __restrict__ grp_count, int32_t* __restrict__ rank) {
     __shared__ int sel[32][kMaxTopK];
     __shared__ unsigned bits[kMaxExpertsRoute];
-    // Waits for the kernel that produced the logits, but does not release its
-    // own dependents early (see launch_moe_route).
+    // Its one dependent, route_scan_assign_kernel, may start at once (it waits
+    // for this grid before reading anything); this grid itself waits for the
+    // kernel that produced the logits.
+    pdl_launch_dependents();
     pdl_wait();
     const int lane = threadIdx.x & 31;
     const int w = threadIdx.x >> 5;
@@ -189,6 +191,9 @@ __global__ void __launch_bounds__(1024)
                              int32_t* __restrict__ offsets, int32_t* __restrict__ row_of,
                              int32_t* __restrict__ sorted_token) {
     __shared__ int warp_sum[32];
+    // Waits for route_topk_kernel; never releases its own dependents early:
+    // the grouped GEMMs read the offsets in their prologue.
+    pdl_wait();
     const int groups = (tokens + 31) / 32;
     const int e = threadIdx.x;
     int total = 0;
@@ -282,9 +287,10 @@ __global__ void __launch_bounds__(kFinThreads)
 
 cudaError_t read_and_clear_oob_moe(unsigned int* out) { return read_and_clear_oob_word(out); }
 
-// The routing kernels are launched with programmatic stream serialization so
-// that their launch overlaps the previous kernel (they wait for it before
-// reading the logits), but they never trigger their dependents early: the
+// Both routing kernels are launched with programmatic stream serialization so
+// that their launches overlap the kernel before them (each waits for it
+// before reading its inputs).  route_topk_kernel releases its dependent (the
+// second routing kernel) at once; route_scan_assign_kernel never does: the
 // grouped GEMMs read the expert offsets in their prologue, before their own
 // griddepcontrol.wait, so every kernel after the router must start only once
 // the offsets are complete.
@@ -307,8 +313,9 @@ cudaError_t launch_moe_route(const float* logits, int64_t tokens, int64_t expert
     cfg.gridDim = dim3(groups, 1, 1);
     cudaError_t e = cudaLaunchKernelEx(&cfg, route_topk_kernel, logits, T, E, K, method, ids, weights, grp, rank);
     if (e != cudaSuccess) return e;
-    route_scan_assign_kernel<<<1, 1024, 0, s>>>(T, E, K, ids, grp, rank, offsets, row_of, sorted_token);
-    return cudaGetLastError();
+    cfg.gridDim = dim3(1, 1, 1);
+    return cudaLaunchKernelEx(&cfg, route_scan_assign_kernel, T, E, K, static_cast<const int32_t*>(ids), grp,
+                              static_cast<const int32_t*>(rank), offsets, row_of, sorted_token);
 }
 
 cudaError_t launch_moe_finalize(const void* y2, const int32_t* row_of, const float* weights, int64_t tokens,

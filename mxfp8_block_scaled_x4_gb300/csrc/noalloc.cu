@@ -123,6 +123,8 @@ extern "C" mxfp8_status mxfp8_linear_static_scratch(const void* x, int64_t m, co
     p.x = nullptr;  // the GEMM reads the quantized activations from the array
     p.gated = false;
     p.sf128 = false;
+    p.hq = nullptr;
+    p.hsf = nullptr;
     // The schedule of an unfused mxfp8_linear call of this class: a stored
     // tactic if the table holds an unfused one for it, else the built-in
     // heuristic with quantization not fused.

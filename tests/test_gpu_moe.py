@@ -226,3 +226,39 @@ def test_moe_arguments_rejected(lib):
         lib.moe_expert_mlp(x, lg, 2, w2, w13)     # weights swapped: shapes do not chain
     with pytest.raises(lib.Mxfp8Error):
         lib.moe_route(lg, 17)                     # topk > 16
+
+
+@pytest.mark.parametrize("shape", [(37, 8, 2, 256, 256), (100, 16, 4, 512, 512), (256, 128, 8, 2048, 768)])
+def test_expert_mlp_is_the_stage_chain_and_each_stage_is_strict(lib, shape):
+    """The whole layer equals, bit for bit, its stages run one by one (inside
+    the layer GEMM1's epilogue quantizes h to MXFP8; the chain rounds h to
+    BF16 and GEMM2's call quantizes it: the same bytes).  Each stage of that
+    chain is then held to the single-layer tolerance on the GPU's own input:
+    GEMM1 + SwiGLU from x (test_gate_up_swiglu_matches_oracle), GEMM2 from the
+    GPU's h against the oracle's GEMM2, and finalize from the GPU's y2 against
+    the exact weighted sum.  (GEMM2 and finalize composed carry two roundings,
+    y2 to BF16 and the sum, so they are checked one at a time.)"""
+    t, e, k, h, inter = shape
+    mw = workloads.moe(seed=60 + t, tokens=t, experts=e, topk=k, hidden=h, inter=inter)
+    w13 = lib.prepare_gate_up_weight(to_dev_f32(mw.w13))
+    w2 = lib.prepare_weight(to_dev_f32(mw.w2))
+    x, lg = to_dev_bf16(mw.x), to_dev_f32(mw.logits)
+    out = lib.moe_expert_mlp(x, lg, k, w13, w2)
+    r = lib.moe_route(lg, k)
+    hv = lib.moe_gate_up_swiglu(x, r, w13)
+    y2 = lib.grouped_linear(hv, r.offsets, w2)
+    chain = lib.moe_finalize(y2, r)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), chain.view(torch.int16))
+    ids, w = M.route(mw.logits, k)
+    off, _, row_of = M.sort_by_expert(ids, e)
+    rows = np.arange(t * k) if t * k <= 512 else np.sort(np.random.default_rng(2).choice(t * k, 256, replace=False))
+    h_gpu = hv.float().cpu().numpy()
+    y2_ref = oracle.grouped_linear(h_gpu, off, *M.prepare_experts(mw.w2), rows=rows)
+    assert_close_to_oracle(y2[torch.as_tensor(rows, device=y2.device)], y2_ref, mw.name + " GEMM2 from its own h")
+    y2_gpu = y2.float().cpu().numpy().astype(np.float64)
+    ref = np.zeros((t, h))
+    for i in range(t):
+        for s in range(k):
+            ref[i] += w[i, s] * y2_gpu[row_of[i * k + s]]
+    assert_close_to_oracle(out, ref, mw.name + " finalize from its own y2")
