@@ -197,8 +197,10 @@ __global__ void __launch_bounds__(1024)
     const int groups = (tokens + 31) / 32;
     const int e = threadIdx.x;
     int total = 0;
-    if (e < experts)
+    if (e < experts) {
+#pragma unroll 8
         for (int g = 0; g < groups; ++g) total += grp[static_cast<size_t>(g) * experts + e];
+    }
     // Block-wide exclusive scan of the totals over experts.
     const int lane = e & 31, w = e >> 5;
     int incl = total;
@@ -223,6 +225,7 @@ __global__ void __launch_bounds__(1024)
     if (e < experts) {
         if (store_ok(e, 1, experts + 1)) offsets[e] = base;
         int run = base;
+#pragma unroll 8
         for (int g = 0; g < groups; ++g) {
             const size_t i = static_cast<size_t>(g) * experts + e;
             const int c = grp[i];
