@@ -67,6 +67,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "debug_check.cuh"
 #include "internal.h"
 #include "ptx.cuh"
@@ -78,7 +80,7 @@ __device__ unsigned int g_gemm_error;
 
 // Schedule of the last GEMM launch on the host (testing aid).
 thread_local int t_last_schedule[5];
-uint64_t g_wait_limit_ns = 0;  // 0: kWaitNs
+std::atomic<uint64_t> g_wait_limit_ns{0};  // testing hook, any thread; 0: kWaitNs
 
 namespace {
 
@@ -1357,7 +1359,8 @@ cudaError_t launch_tt(const GemmProblem& pr, const GemmSchedule& sch, int num_sm
     a.hsf = pr.gated ? pr.hsf : nullptr;
     a.stages = lp.stages;
     a.tmem_cols = lp.tmem_cols;
-    a.wait_ns = g_wait_limit_ns ? g_wait_limit_ns : kWaitNs;
+    const uint64_t wait_limit = g_wait_limit_ns.load(std::memory_order_relaxed);
+    a.wait_ns = wait_limit ? wait_limit : kWaitNs;
     const size_t smem = lp.smem;
 
     cudaError_t err = cudaFuncSetAttribute(mxfp8_gemm_kernel<TT, PIPES, MODE>,
@@ -1457,7 +1460,8 @@ cudaError_t launch_dual(const GemmProblem& pr, int num_sms, cudaStream_t s, bool
     a.stages = stages;
     a.tmem_cols = pow2_cols(2 * TT + stages * 2 * G::kSlotCols);
     if (a.tmem_cols > 512) return cudaErrorInvalidConfiguration;
-    a.wait_ns = g_wait_limit_ns ? g_wait_limit_ns : kWaitNs;
+    const uint64_t wait_limit = g_wait_limit_ns.load(std::memory_order_relaxed);
+    a.wait_ns = wait_limit ? wait_limit : kWaitNs;
     const size_t smem = 1024 + static_cast<size_t>(stages) * G::kStageBytes + ctrl;
     cudaError_t err = cudaFuncSetAttribute(mxfp8_gemm_dual_kernel<TT>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
@@ -1490,9 +1494,11 @@ cudaError_t launch_dual(const GemmProblem& pr, int num_sms, cudaStream_t s, bool
 
 }  // namespace
 
-int g_force_pipes = 0;
+std::atomic<int> g_force_pipes{0};  // testing hook, any thread; 0: automatic
 
-void set_pipes(int pipes) { g_force_pipes = (pipes == 1 || pipes == 2 || pipes == 4) ? pipes : 0; }
+void set_pipes(int pipes) {
+    g_force_pipes.store((pipes == 1 || pipes == 2 || pipes == 4) ? pipes : 0, std::memory_order_relaxed);
+}
 
 GemmSchedule choose_schedule(const GemmProblem& p, int num_sms, int force_tt, int force_split,
                              int force_fuse) {
@@ -1576,7 +1582,7 @@ GemmSchedule choose_schedule(const GemmProblem& p, int num_sms, int force_tt, in
     if (p.offsets == nullptr && !persistent && tt == 64 &&
         (p.n_pad / 128) * ((p.m + tt - 1) / tt) * split <= num_sms)
         pipes = 2;
-    if (g_force_pipes) pipes = g_force_pipes;
+    if (const int fp = g_force_pipes.load(std::memory_order_relaxed)) pipes = fp;
     if (pipes == 2 && tt > 64) pipes = 1;
     if (pipes == 4 && tt != 16) pipes = tt <= 64 ? 2 : 1;
     sch.pipes = pipes;
@@ -1643,7 +1649,7 @@ cudaError_t launch_gemm(const GemmProblem& p, const GemmSchedule& sch, int num_s
     }
 }
 
-void set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns = ns; }
+void set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns, std::memory_order_relaxed); }
 
 void last_schedule(int* out5) {
     for (int i = 0; i < 5; ++i) out5[i] = t_last_schedule[i];
