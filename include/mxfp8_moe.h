@@ -12,9 +12,12 @@
  *      (token, slot) pairs sorted by expert, then token;
  *   2. gate_up: gather the token rows into expert-sorted order, quantize
  *      them (MXFP8, 8x4 scales), grouped GEMM1 against the gated weights and
- *      the SwiGLU epilogue h = silu(gate) * up, written as BF16 [rows][I];
- *   3. down: mxfp8_grouped_linear of h against GEMM2 (it quantizes h) into
- *      BF16 [rows][H];
+ *      the SwiGLU epilogue h = silu(gate) * up, rounded to BF16 [rows][I];
+ *   3. down: grouped GEMM2 of h into BF16 [rows][H].  Inside
+ *      mxfp8_moe_expert_mlp, GEMM1's epilogue quantizes the BF16 h straight
+ *      to MXFP8 (8x4 scales) for GEMM2; run as separate calls,
+ *      mxfp8_moe_gate_up_swiglu writes the BF16 h and mxfp8_grouped_linear
+ *      quantizes it: the same bytes either way;
  *   4. finalize: out[t] = sum over slots s of w[t,s] * down[row(t,s)] (FP32
  *      in slot order, one BF16 rounding).
  * Readings taken where the pages are silent: the gated activation is SwiGLU
@@ -42,7 +45,7 @@ typedef enum mxfp8_route_method {
     MXFP8_ROUTE_RENORMALIZE_NAIVE = 1  /* softmax over all experts, top-k, renormalize to sum 1 */
 } mxfp8_route_method;
 
-/* Workspace of mxfp8_moe_route: (ceil(tokens/32) * experts + tokens * topk)
+/* Workspace of mxfp8_moe_route: (ceil(tokens/8) * experts + tokens * topk)
  * int32. */
 size_t mxfp8_moe_route_workspace_bytes(int64_t tokens, int64_t experts, int64_t topk);
 

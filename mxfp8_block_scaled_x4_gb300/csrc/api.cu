@@ -514,7 +514,7 @@ int64_t mxfp8_tactic_count(void) { return mxk::tactic_count(); }
 // ------------------------------------------------------------------- MoE
 size_t mxfp8_moe_route_workspace_bytes(int64_t tokens, int64_t experts, int64_t topk) {
     if (tokens < 0 || tokens > kMaxRows || experts < 1 || experts > 1024 || topk < 1 || topk > 16) return 0;
-    return static_cast<size_t>(((tokens + 31) / 32 * experts + tokens * topk) * 4);
+    return static_cast<size_t>(((tokens + 7) / 8 * experts + tokens * topk) * 4);  // 8-token routing groups
 }
 
 static mxfp8_status check_route_shape(int64_t tokens, int64_t experts, int64_t topk) {

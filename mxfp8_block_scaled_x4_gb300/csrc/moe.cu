@@ -8,7 +8,7 @@
 // exact arithmetic), in descending order, ties to the lower expert id.  The
 // (token, slot) pairs are then sorted by expert, then token -- stable and
 // deterministic, no atomics:
-//   route_topk_kernel   one CTA per 32-token group, one warp per token: k
+//   route_topk_kernel   one CTA per 8-token group, one warp per token: k
 //                       rounds of warp arg-max over the logits, the weights,
 //                       then per-expert token masks -> group counts and each
 //                       pair's rank inside its group;
@@ -32,6 +32,9 @@ namespace {
 
 constexpr int kMaxTopK = 16;
 constexpr int kMaxExpertsRoute = 1024;
+// Tokens per routing group (one CTA of route_topk_kernel, one warp per
+// token): small groups spread the selections over many SMs.
+constexpr int kGroup = 8;
 
 // (v, e) ranks above (bv, be): larger logit, or equal logit and lower id.
 __device__ __forceinline__ bool better(float v, int e, float bv, int be) {
@@ -137,15 +140,15 @@ __device__ __forceinline__ void route_token(const float* __restrict__ lg, const 
     }
 }
 
-// One CTA per group of 32 tokens, one warp per token.  The group's picks
-// then go into per-expert 32-bit token masks in shared memory (atomicOr: the
-// result does not depend on the order), which give the group count of every
-// expert and each pair's rank among the group's tokens.
-__global__ void __launch_bounds__(1024)
+// One CTA per group of kGroup tokens, one warp per token.  The group's picks
+// then go into per-expert token masks in shared memory (atomicOr: the result
+// does not depend on the order), which give the group count of every expert
+// and each pair's rank among the group's tokens.
+__global__ void __launch_bounds__(32 * kGroup)
     route_topk_kernel(const float* __restrict__ logits, int tokens, int experts, int topk, int method,
                       int32_t* __restrict__ ids, float* __restrict__ weights,
                       int32_t* __restrict__ grp_count, int32_t* __restrict__ rank) {
-    __shared__ int sel[32][kMaxTopK];
+    __shared__ int sel[kGroup][kMaxTopK];
     __shared__ unsigned bits[kMaxExpertsRoute];
     // Its one dependent, route_scan_assign_kernel, may start at once (it waits
     // for this grid before reading anything); this grid itself waits for the
@@ -155,7 +158,7 @@ __global__ void __launch_bounds__(1024)
     const int lane = threadIdx.x & 31;
     const int w = threadIdx.x >> 5;
     const int group = blockIdx.x;
-    const int t = group * 32 + w;
+    const int t = group * kGroup + w;
     for (int e = threadIdx.x; e < experts; e += blockDim.x) bits[e] = 0u;
     if (t < tokens) {
         const float* lg = logits + static_cast<size_t>(t) * experts;
@@ -166,14 +169,14 @@ __global__ void __launch_bounds__(1024)
                     static_cast<int64_t>(tokens) * topk);
     }
     __syncthreads();
-    const int live = min(32, tokens - group * 32);
+    const int live = min(kGroup, tokens - group * kGroup);
     for (int i = threadIdx.x; i < live * topk; i += blockDim.x) atomicOr(&bits[sel[i / topk][i % topk]], 1u << (i / topk));
     __syncthreads();
     const int64_t pairs = static_cast<int64_t>(tokens) * topk;
-    const int64_t groups = (tokens + 31) / 32;
+    const int64_t groups = (tokens + kGroup - 1) / kGroup;
     for (int i = threadIdx.x; i < live * topk; i += blockDim.x) {
         const int tw = i / topk;
-        const int64_t o = static_cast<int64_t>(group * 32 + tw) * topk + (i % topk);
+        const int64_t o = static_cast<int64_t>(group * kGroup + tw) * topk + (i % topk);
         if (store_ok(o, 1, pairs)) rank[o] = __popc(bits[sel[tw][i % topk]] & ((1u << tw) - 1u));
     }
     for (int e = threadIdx.x; e < experts; e += blockDim.x)
@@ -194,7 +197,7 @@ __global__ void __launch_bounds__(1024)
     // Waits for route_topk_kernel; never releases its own dependents early:
     // the grouped GEMMs read the offsets in their prologue.
     pdl_wait();
-    const int groups = (tokens + 31) / 32;
+    const int groups = (tokens + kGroup - 1) / kGroup;
     const int e = threadIdx.x;
     int total = 0;
     if (e < experts) {
@@ -238,7 +241,7 @@ __global__ void __launch_bounds__(1024)
     const int pairs = tokens * topk;
     for (int i = threadIdx.x; i < pairs; i += blockDim.x) {
         const int t = i / topk;
-        const int r = grp[static_cast<size_t>(t >> 5) * experts + ids[i]] + rank[i];
+        const int r = grp[static_cast<size_t>(t / kGroup) * experts + ids[i]] + rank[i];
         if (store_ok(i, 1, pairs)) row_of[i] = r;
         if (store_ok(r, 1, pairs)) sorted_token[r] = t;
     }
@@ -310,13 +313,15 @@ cudaError_t launch_moe_route(const float* logits, int64_t tokens, int64_t expert
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     const int T = static_cast<int>(tokens), E = static_cast<int>(experts), K = static_cast<int>(topk);
-    const int groups = static_cast<int>((tokens + 31) / 32);
+    const int groups = static_cast<int>((tokens + kGroup - 1) / kGroup);
     int32_t* grp = ws;
     int32_t* rank = ws + static_cast<size_t>(groups) * experts;
     cfg.gridDim = dim3(groups, 1, 1);
+    cfg.blockDim = dim3(32 * kGroup, 1, 1);
     cudaError_t e = cudaLaunchKernelEx(&cfg, route_topk_kernel, logits, T, E, K, method, ids, weights, grp, rank);
     if (e != cudaSuccess) return e;
     cfg.gridDim = dim3(1, 1, 1);
+    cfg.blockDim = dim3(1024, 1, 1);  // one thread per expert
     return cudaLaunchKernelEx(&cfg, route_scan_assign_kernel, T, E, K, static_cast<const int32_t*>(ids), grp,
                               static_cast<const int32_t*>(rank), offsets, row_of, sorted_token);
 }

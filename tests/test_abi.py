@@ -152,7 +152,7 @@ def test_argument_errors_before_launch(mx):
 
 def test_moe_size_helpers_and_argument_checks(mx):
     lib = mx.library()
-    assert lib.mxfp8_moe_route_workspace_bytes(256, 128, 8) == ((256 + 31) // 32 * 128 + 256 * 8) * 4
+    assert lib.mxfp8_moe_route_workspace_bytes(256, 128, 8) == ((256 + 7) // 8 * 128 + 256 * 8) * 4  # 8-token groups
     assert lib.mxfp8_moe_route_workspace_bytes(-1, 128, 8) == 0
     assert lib.mxfp8_moe_workspace_bytes(256, 128, 17, 2048, 768) == 0   # topk > 16
     assert lib.mxfp8_moe_workspace_bytes(256, 4, 8, 2048, 768) == 0      # topk > experts
