@@ -313,7 +313,7 @@ def measure_prepare(mx, d, peaks, reps=12):
     nbytes = src_bytes + n_pad * d.k + n_pad * (d.k // 32)
     gbs = nbytes / (ms * 1e-3) / 1e9
     return {"us": ms * 1e3, "alg_bytes": nbytes, "gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"],
-            "reps": reps, "source_copies": copies, "source": "float32 [%d, %d]" % (d.n, d.k)}
+            "reps": reps, "source": "float32 [%d, %d]" % (d.n, d.k)}
 
 
 def measure_config(mx, name, d, peaks, calls=2000, tune=False):
@@ -608,7 +608,7 @@ def step_roofline(d, wb, launches_per_step, ms_step, ms_gemm, peak_gbs, traffic,
                   "achieved": gemm_bytes / (ms_gemm * 1e-3) / 1e9}
     if launches_per_step == 1:
         ms, nbytes = ms_step, fused_bytes
-        kernel = "mxfp8_gemm_kernel<16> (activation quantization fused; the step's only launch)"
+        kernel = "mxfp8_gemm_kernel<16> (quantization fused; the step's only launch)"
     else:
         ms, nbytes = ms_gemm, gemm_bytes
         kernel = "mxfp8_gemm_kernel<16>"
@@ -793,7 +793,7 @@ def main():
            "config": {"workload": d.name, "m": d.m, "n": d.n, "k": d.k, "bias": True,
                       "parallelism": "replicas" if ws > 1 else "single",
                       "l2": "inputs larger than L2: %d rotating copies (%.0f MB)" % (setup.R, setup.R * nbytes / 1e6),
-                      "timing": "CUDA-graph replays, CUDA events; 1 ms GPU delay queued before the start event"},
+                      "timing": "CUDA-graph replays, CUDA events, GPU delay before the start event"},
            "roofline": roof,
            "gpu_launches": launches_per_step * args.steps,
            "clocks": clk,
@@ -901,18 +901,17 @@ def measure_e2e(mx, setup, steps):
             "us_per_step": ms * 1e3 / steps, "steps": steps,
             "single_stream_us_per_step": ms1 * 1e3 / steps,
             "requests_in_flight": nreq,
-            "note": "mxfp8_linear_host called through ctypes with prepared arguments, %d streams in "
-                    "turn (host launch overhead included)" % nreq}
+            "note": "mxfp8_linear_host via ctypes, one stream per request in flight"}
 
 
 def load_traffic(kernel, workload):
     """DRAM bytes per launch from the committed ncu summary, valid only while
     the kernel source is unchanged since the capture."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
-    src = os.path.join(ROOT, "mxfp8_block_scaled_x4_gb300", "csrc", "gemm.cu")
     try:
         table = json.load(open(path))
         ent = table[kernel][workload]
+        src = os.path.join(ROOT, "mxfp8_block_scaled_x4_gb300", "csrc", ent.get("source", "gemm.cu"))
         sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
         if ent.get("source_sha") != sha:
             return None
