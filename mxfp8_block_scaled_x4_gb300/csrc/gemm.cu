@@ -52,8 +52,8 @@
 //                peer's slice into the peer's shared memory, counted on the
 //                peer's mbarrier; each owner sums its slice in rank order
 //                (deterministic) as soon as its bytes have landed.
-//   dual         mxfp8_gemm_dual_kernel<TT>: two 128-row weight tiles x 160
-//                or 192 tokens per CTA tile (dense, large M), below.
+//   dual         mxfp8_gemm_dual_kernel<TT>: two 128-row weight tiles x 144,
+//                160, 176 or 192 tokens per CTA tile (dense, large M), below.
 // Programmatic dependent launch: the kernel lets the next grid start at once;
 // it reads nothing a previous grid may write before griddepcontrol.wait,
 // except the weights, their scales, the bias and the grouped offsets, which
@@ -915,7 +915,7 @@ __global__ void __launch_bounds__(32 * num_warps(TT, PIPES),
 //                token tile, the raw 8x4 token scales
 //   warps 1, 11  MMA issuers of weight tile 0 / 1 (lane 0); warp 1 owns TMEM
 //   warps 2..9   epilogue: warp 2+e serves accumulator e/4, lane quadrant
-//                warp%4, 32 token columns at a time
+//                warp%4, 32 token columns at a time, stored from registers
 //   warp 10      token-scale re-order into the TMEM-copy order
 template <int TT>
 struct DualGeometry {
@@ -964,9 +964,7 @@ __global__ void __launch_bounds__(kDualThreads, 1) mxfp8_gemm_dual_kernel(const 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int S = p.stages;
-    // Epilogue staging: one 32 x 32 BF16 block per epilogue warp.
-    uint8_t* stage_out = smem + S * G::kStageBytes;
-    uint64_t* full = reinterpret_cast<uint64_t*>(stage_out + 8 * 2048);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * G::kStageBytes);
     uint64_t* empty = full + S;
     uint64_t* sfraw = empty + S;
     uint64_t* acc_full = sfraw + S;   // [2], one per accumulator
@@ -1152,14 +1150,13 @@ __global__ void __launch_bounds__(kDualThreads, 1) mxfp8_gemm_dual_kernel(const 
     } else {
         // ------------------------------------------------------- epilogue
         // 32 token columns at a time: TMEM -> registers (+ bias, BF16) ->
-        // this warp's 32 x 32 staging block transposed -> 16-byte stores of
-        // 64-byte output row segments (scalar stores when N is not a
-        // multiple of 8).
+        // stores straight from registers: lane l holds output feature n0 + l,
+        // so each store instruction of the warp writes one token's 64-byte
+        // row segment.  (No shared staging: the 16 KB it would take buys a
+        // fourth pipeline stage for tiles of <= 160 tokens.)
         const int ew = warp - 2;
         const int q = ew >> 2;   // accumulator / weight tile of the pair
         const int quad = warp & 3;
-        __nv_bfloat16* blk = reinterpret_cast<__nv_bfloat16*>(stage_out + ew * 2048);  // [32 tok][32 n]
-        const bool vec = (p.n & 7) == 0 && (reinterpret_cast<uintptr_t>(p.y) & 15) == 0;
         int tile_iter = 0;
         for (int t = tile_first; t < num_tiles; t += tile_stride, ++tile_iter) {
             const TileInfo ti = decode_dual<TT>(t, p);
@@ -1194,24 +1191,14 @@ __global__ void __launch_bounds__(kDualThreads, 1) mxfp8_gemm_dual_kernel(const 
                     if (lane == 0) mbar_arrive(&acc_empty[q]);
                 }
                 if (n0 >= p.n || c0 >= ti.count) continue;  // warp-uniform
-#pragma unroll
-                for (int j = 0; j < 32; ++j) blk[j * 32 + lane] = __float2bfloat16_rn(__uint_as_float(r[j]) + b);
-                __syncwarp();
                 const int jmax = min(32, ti.count - c0);
-                if (vec && n0 + 32 <= p.n) {
+                if (n < p.n) {
+                    __nv_bfloat16* yp = p.y + static_cast<size_t>(ti.tok0 + c0) * p.n + n;
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int j = i * 8 + (lane >> 2);
-                        const int part = lane & 3;
-                        if (j < jmax && store_ok(static_cast<int64_t>(ti.tok0 + c0 + j) * p.n + n0 + part * 8, 8,
+                    for (int j = 0; j < 32; ++j)
+                        if (j < jmax && store_ok(static_cast<int64_t>(ti.tok0 + c0 + j) * p.n + n, 1,
                                                  static_cast<int64_t>(p.m) * p.n))
-                            *reinterpret_cast<uint4*>(p.y + static_cast<size_t>(ti.tok0 + c0 + j) * p.n + n0 + part * 8) =
-                                *reinterpret_cast<const uint4*>(blk + j * 32 + part * 8);
-                    }
-                } else if (n < p.n) {
-                    for (int j = 0; j < jmax; ++j)
-                        if (store_ok(static_cast<int64_t>(ti.tok0 + c0 + j) * p.n + n, 1, static_cast<int64_t>(p.m) * p.n))
-                            p.y[static_cast<size_t>(ti.tok0 + c0 + j) * p.n + n] = blk[j * 32 + lane];
+                            yp[static_cast<size_t>(j) * p.n] = __float2bfloat16_rn(__uint_as_float(r[j]) + b);
                 }
                 __syncwarp();
             }
@@ -1453,7 +1440,7 @@ cudaError_t launch_dual(const GemmProblem& pr, int num_sms, cudaStream_t s, bool
     a.n_tiles = static_cast<int>(pr.n_pad / 128);
     a.splits = 1;
     a.persistent = 1;
-    const int ctrl = 1024 + 8 * 2048;  // barriers + epilogue staging
+    const int ctrl = 1024;  // barriers and the TMEM slot
     int stages = (227 * 1024 - 1024 - ctrl) / G::kStageBytes;
     if (stages > 6) stages = 6;
     if (stages < 2) return cudaErrorInvalidConfiguration;
@@ -1520,20 +1507,23 @@ GemmSchedule choose_schedule(const GemmProblem& p, int num_sms, int force_tt, in
     if (p.gated && tt > 128) tt = 128;  // the gated exchange buffer holds 64 x TT FP32
     // Dense large M: two weight tiles x TT tokens per CTA tile whenever that
     // still gives every SM a tile.  TT is the width with the least predicted
-    // time, waves x (fixed + per-token cost of a tile): on 8192^3 a tile of
-    // TT tokens measured about 27 us + 0.0625 us x TT (192: 391 us in 10
-    // waves, 176: 382 us in 10, 160: 406 us in 11, 144: 433 us in 12), i.e.
-    // a fixed cost worth ~434 tokens.  So 176-token tiles win there (1504
-    // tiles = 9.9 waves of 152, against 1376 = 9.05 for 192).
+    // time, waves x the measured cost of one tile of that width (8192^3,
+    // us per tile x 100; 192 and 176 run three pipeline stages, 160 and 144
+    // four): 192: 384 us in 10 waves, 176: 381.5 in 10, 160: 390.5 in 11,
+    // 144: 416 in 12.  So 176-token tiles win there (1504 tiles = 9.9 waves
+    // of 152, against 1376 = 9.05 for 192).
     bool dual = false;
     int dual_tt = 192;
     if (p.offsets == nullptr && !p.gated && !p.sf128 && tt == 256 && force_tt == 0 &&
         ((p.n_pad / 128 + 1) / 2) * ((p.m + 191) / 192) >= num_sms) {
         dual = true;
+        constexpr int kWidth[4] = {192, 176, 160, 144};
+        constexpr int64_t kTileCost[4] = {3840, 3815, 3550, 3470};
         int64_t best = -1;
-        for (int w : {192, 176, 160}) {
+        for (int i = 0; i < 4; ++i) {
+            const int w = kWidth[i];
             const int64_t tiles = ((p.n_pad / 128 + 1) / 2) * ((p.m + w - 1) / w);
-            const int64_t cost = ((tiles + num_sms - 1) / num_sms) * (434 + w);
+            const int64_t cost = ((tiles + num_sms - 1) / num_sms) * kTileCost[i];
             if (best < 0 || cost < best) { best = cost; dual_tt = w; }
         }
     }
