@@ -925,10 +925,15 @@ struct DualGeometry {
     static constexpr int kOffA = 32768;
     static constexpr int kOffWsf0 = kOffA + TT * 128;
     static constexpr int kOffWsf1 = kOffWsf0 + 512;
-    static constexpr int kOffAsfRaw = kOffWsf1 + 512;
-    static constexpr int kOffAsfT = kOffAsfRaw + 1152;
+    // The raw 8x4 token-scale groups land in the area that then holds them in
+    // the TMEM-copy order: the re-order warp reads all its words before it
+    // writes (in place).  Sharing the area is what lets 176-token tiles run
+    // four 56 KB stages.
+    static constexpr int kOffAsfT = kOffWsf1 + 512;
+    static constexpr int kOffAsfRaw = kOffAsfT;
     static constexpr int kStageBytes = ((kOffAsfT + 512 * kSfChunks) + 1023) / 1024 * 1024;
     static constexpr int kSlotCols = 4 + 4 * kSfChunks;  // per pipe per stage
+    static_assert((TT / 8 + 1) * 32 <= 512 * kSfChunks, "raw scale groups must fit the shared area");
 };
 
 constexpr int kDualThreads = 12 * 32;
@@ -1130,17 +1135,20 @@ __global__ void __launch_bounds__(kDualThreads, 1) mxfp8_gemm_dual_kernel(const 
                 }
                 uint8_t* st = smem + s * G::kStageBytes;
                 const uint32_t* raw = reinterpret_cast<const uint32_t*>(st + G::kOffAsfRaw);
+                // In place: every word is read before any is written.
+                uint32_t w[G::kSfChunks][4];
 #pragma unroll
-                for (int ch = 0; ch < G::kSfChunks; ++ch) {
-                    uint32_t w[4];
+                for (int ch = 0; ch < G::kSfChunks; ++ch)
 #pragma unroll
                     for (int jq = 0; jq < 4; ++jq) {
                         const int j = ch * 128 + jq * 32 + lane;
-                        w[jq] = (j < TT) ? raw[off8 + j] : 0u;
+                        w[ch][jq] = (j < TT) ? raw[off8 + j] : 0u;
                     }
+                __syncwarp();
+#pragma unroll
+                for (int ch = 0; ch < G::kSfChunks; ++ch)
                     *reinterpret_cast<uint4*>(st + G::kOffAsfT + ch * 512 + lane * 16) =
-                        make_uint4(w[0], w[1], w[2], w[3]);
-                }
+                        make_uint4(w[ch][0], w[ch][1], w[ch][2], w[ch][3]);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&full[s]);
@@ -1508,17 +1516,17 @@ GemmSchedule choose_schedule(const GemmProblem& p, int num_sms, int force_tt, in
     // Dense large M: two weight tiles x TT tokens per CTA tile whenever that
     // still gives every SM a tile.  TT is the width with the least predicted
     // time, waves x the measured cost of one tile of that width (8192^3,
-    // us per tile x 100; 192 and 176 run three pipeline stages, 160 and 144
-    // four): 192: 384 us in 10 waves, 176: 381.5 in 10, 160: 390.5 in 11,
-    // 144: 416 in 12.  So 176-token tiles win there (1504 tiles = 9.9 waves
-    // of 152, against 1376 = 9.05 for 192).
+    // us per tile x 100; 192 runs three pipeline stages, the others four):
+    // 192: 389 us in 10 waves, 176: 372 in 10, 160: 390.5 in 11, 144: 416
+    // in 12.  So 176-token tiles win there (1504 tiles = 9.9 waves of 152,
+    // against 1376 = 9.05 for 192).
     bool dual = false;
     int dual_tt = 192;
     if (p.offsets == nullptr && !p.gated && !p.sf128 && tt == 256 && force_tt == 0 &&
         ((p.n_pad / 128 + 1) / 2) * ((p.m + 191) / 192) >= num_sms) {
         dual = true;
         constexpr int kWidth[4] = {192, 176, 160, 144};
-        constexpr int64_t kTileCost[4] = {3840, 3815, 3550, 3470};
+        constexpr int64_t kTileCost[4] = {3890, 3720, 3550, 3470};
         int64_t best = -1;
         for (int i = 0; i < 4; ++i) {
             const int w = kWidth[i];
