@@ -119,7 +119,9 @@ def test_dual_schedule_unaligned_output(lib):
     d = workloads.dense(m=200, n=256, k=256, seed=35, bias=True)
     pw = lib.prepare_weight(to_dev_f32(d.w))
     x = to_dev_bf16(d.x)
-    buf = torch.empty(d.m * d.n + 8, dtype=torch.bfloat16, device="cuda")
+    # sentinel-filled around y: the element before it and the 7 after must stay
+    sentinel = torch.tensor([-1234.5], dtype=torch.bfloat16).view(torch.int16).item()
+    buf = torch.full((d.m * d.n + 8,), sentinel, dtype=torch.int16, device="cuda").view(torch.bfloat16)
     y = buf[1:1 + d.m * d.n].view(d.m, d.n)  # 2-byte offset from a 256-byte aligned base
     import ctypes
     lib.set_schedule(192, -1, 0)  # the dual weight-tile kernel
@@ -135,6 +137,8 @@ def test_dual_schedule_unaligned_output(lib):
         lib.set_schedule(0, 0, -1)
     wq, wsf = oracle_weight(d.w)
     assert_close_to_oracle(y, oracle.linear(d.x, wq, wsf, d.bias), "unaligned y")
+    raw = buf.view(torch.int16)
+    assert raw[0].item() == sentinel and bool((raw[1 + d.m * d.n:] == sentinel).all())
 
 
 def test_multi_pipe_fewer_k_blocks_than_pipes(lib):
