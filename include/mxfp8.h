@@ -237,9 +237,9 @@ mxfp8_status mxfp8_linear_128x4(const void* x, int64_t m, const mxfp8_weight* w,
 
 /* ------------------------------------------------------------------ tactics
  * A tactic is a GEMM schedule, four int32:
- *   [0] tokens per tile: 16, 32, 64, 128, 256, or 160 / 192 (with split_k
- *       -1) = two 128-row weight tiles x 160 / 192 tokens per CTA tile
- *       (dense only);
+ *   [0] tokens per tile: 16, 32, 64, 128, 256, or 144 / 160 / 176 / 192
+ *       (with split_k -1) = two 128-row weight tiles x that many tokens per
+ *       CTA tile (dense only);
  *   [1] split_k: -1 = persistent tiles, 1..8 = one output tile per cluster
  *       of that many CTAs with K split among them (tiles of <= 128 tokens,
  *       dense only);

@@ -16,7 +16,9 @@ extern "C" {
 #endif
 
 /* Testing hook: pin the GEMM schedule, process-wide.
- * tokens_per_tile: 0 (automatic) or 16, 32, 64, 128, 256 (256 needs split_k -1);
+ * tokens_per_tile: 0 (automatic) or 16, 32, 64, 128, 256 (256 needs split_k -1),
+ * or 144, 160, 176, 192: two 128-row weight tiles per CTA tile (dense,
+ * persistent);
  * split_k: 0 automatic, -1 persistent tiles, 1..8 one tile per cluster of
  * split_k CTAs (K split among them, tokens_per_tile <= 128);
  * fuse_quant: -1 automatic, 0 never, 1 whenever the schedule allows

@@ -608,7 +608,7 @@ def moe_workspace_bytes(tokens, experts, topk, hidden, inter) -> int:
 # ------------------------------------------------------------------ hooks
 def set_schedule(tokens_per_tile: int = 0, split_k: int = 0, fuse_quant: int = -1) -> None:
     """Pin the GEMM schedule (testing/benchmarking).  tokens_per_tile 0 = auto,
-    16..256, or 160 / 192 = two weight tiles per CTA tile (dense); split_k 0 =
+    16..256, or 144 / 160 / 176 / 192 = two weight tiles per CTA tile (dense); split_k 0 =
     auto, -1 = persistent, >0 = one tile per cluster of split_k CTAs;
     fuse_quant -1 = auto, 0 = off, 1 = on where possible."""
     library().mxfp8_set_schedule(int(tokens_per_tile), int(split_k), int(fuse_quant))

@@ -364,7 +364,7 @@ mxfp8_status mxfp8_linear_128x4(const void* x, int64_t m, const mxfp8_weight* w,
 
 // --------------------------------------------------------------- tactics
 namespace {
-// {tokens_per_tile (192 = two weight tiles), split_k (-1 = persistent),
+// {tokens_per_tile (144/160/176/192 = two weight tiles), split_k (-1 = persistent),
 //  fuse_quant, pipes}
 void encode_tactic(const mxk::GemmSchedule& s, int32_t* t4) {
     t4[0] = s.tokens_per_tile;
@@ -757,7 +757,7 @@ void mxfp8_last_schedule(int* out5) {
 }
 
 void mxfp8_set_schedule(int tokens_per_tile, int split_k, int fuse_quant) {
-    // 160 / 192: the dual weight-tile schedule (dense, persistent).
+    // 144 / 160 / 176 / 192: the dual weight-tile schedule (dense, persistent).
     const bool tt_ok = tokens_per_tile == 0 || tokens_per_tile == 16 || tokens_per_tile == 32 ||
                        tokens_per_tile == 64 || tokens_per_tile == 128 || tokens_per_tile == 256 ||
                        tokens_per_tile == 144 || tokens_per_tile == 160 || tokens_per_tile == 176 ||
