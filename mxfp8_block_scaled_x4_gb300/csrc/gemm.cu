@@ -25,7 +25,7 @@
 //               each) and commits the stage back to the producer.  Each
 //               tcgen05/TMA/mbarrier instruction costs its issuing thread
 //               ~55-170 cycles, which bounds one pipeline at small N.
-//   warps 2..   epilogue (4 warps for TT <= 32, else 8, one or two per TMEM
+//   warps 2..   epilogue (4 warps for TT = 32, else 8, one or two per TMEM
 //               lane quadrant): tcgen05.ld, release the accumulator, then
 //               + bias, BF16 rounding and masked stores (j < N, token < M);
 //               the gated mode passes the up half to the gate half through
@@ -200,9 +200,13 @@ __device__ __forceinline__ void record_timeout(volatile uint32_t* abort_flag) {
 // Pipe q owns the local K blocks i with i % PIPES == q of every tile, its own
 // ring of `stages` shared-memory stages and its own TMEM accumulator; the
 // epilogue sums the accumulators in pipe order.
-// Epilogue warps: one per TMEM lane quadrant for tiles of <= 32 tokens (so
-// that two CTAs with two pipelines fit one SM), two per quadrant above.
-__host__ __device__ constexpr int epi_warps(int tt) { return tt <= 32 ? 4 : 8; }
+// Epilogue warps: one per TMEM lane quadrant for 32-token tiles (so that two
+// CTAs with two pipelines fit one SM), two per quadrant otherwise.  16-token
+// tiles take eight: the fused quantizer then gives each warp one patch (the
+// decode call's quantization phase is on its critical path; measured M=16
+// 5.65 -> 5.27 us, M=1 5.53 -> 4.85 us), and at 72 registers two such CTAs
+// still fit an SM.
+__host__ __device__ constexpr int epi_warps(int tt) { return tt == 32 ? 4 : 8; }
 __host__ __device__ constexpr int num_warps(int tt, int pipes) { return 3 + epi_warps(tt) + 2 * (pipes - 1); }
 
 struct Ctx {
@@ -436,7 +440,7 @@ __device__ __forceinline__ void run_fused_quant(const GemmArgs& p, const Ctx& c,
     const int S = c.stages;
     constexpr int kEpi = epi_warps(TT);
     constexpr int kPatches = TT / 8;  // per K block
-    constexpr int kBatch = (TT == 16 || PIPES == 1) ? 2 : 4;  // within the register budget
+    constexpr int kBatch = TT == 16 ? 1 : ((PIPES == 1) ? 2 : 4);  // within the register budget
     const int total = nk * kPatches;
     const int r8 = lane >> 2;
     const int b4 = lane & 3;
