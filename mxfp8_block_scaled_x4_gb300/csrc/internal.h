@@ -24,7 +24,7 @@ cudaError_t launch_prepare_weight(const void* src, bool src_is_bf16, int64_t exp
                                   cudaStream_t s, int64_t inter = 0);
 
 // Mixture-of-experts helpers (moe.cu).  Routing: top-k per token, weights,
-// and the stable expert-sorted order; ws holds ceil(tokens/32) * experts
+// and the stable expert-sorted order; ws holds ceil(tokens/8) * experts
 // group counts plus tokens * topk ranks (int32).
 cudaError_t launch_moe_route(const float* logits, int64_t tokens, int64_t experts, int64_t topk, int method,
                              int32_t* ids, float* weights, int32_t* offsets, int32_t* sorted_token,

@@ -35,6 +35,9 @@ constexpr int kMaxExpertsRoute = 1024;
 // Tokens per routing group (one CTA of route_topk_kernel, one warp per
 // token): small groups spread the selections over many SMs.
 constexpr int kGroup = 8;
+// Largest group-count table route_scan_assign_kernel stages in shared memory
+// (48 KB less its own 128-byte static block).
+constexpr size_t kScanSmemBytes = 48 * 1024 - 128;
 
 // (v, e) ranks above (bv, be): larger logit, or equal logit and lower id.
 __device__ __forceinline__ bool better(float v, int e, float bv, int be) {
@@ -59,57 +62,89 @@ __device__ __forceinline__ void load_token_logits(const float* __restrict__ lg, 
     }
 }
 
-// Top-k of one token by its warp (lane-strided scan + butterfly arg-max per
-// round, each round excluding earlier picks by order) and its weights.
-// Lane 0 writes ids (global, and sel_row if given); lanes < topk write the
-// weights.  tl holds the logits when experts <= 32 * kRegLogits.
+// Order-preserving integer key of a logit: a larger key is a larger value;
+// -0 and +0 share one key (they compare equal) and NaN takes the lowest key.
+__device__ __forceinline__ uint32_t logit_key(float v) {
+    if (v != v) return 0u;
+    if (v == 0.0f) v = 0.0f;
+    const uint32_t b = __float_as_uint(v);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// Sum over the warp (fixed butterfly: every lane gets the same value).
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, d);
+    return v;
+}
+
+// Top-k of one token by its warp and its weights.  Round r picks the best
+// logit not yet taken (larger value, then lower id), so the picks come out in
+// that total order; lane r keeps pick r.  Logits in registers (experts <=
+// 32 * kRegLogits): every lane offers its best unpicked logit, the warp takes
+// the largest key (redux.sync max) and, among the lanes holding it, the
+// lowest expert id (redux.sync min); the owning lane marks it taken.  Wider
+// layers rescan the logits each round (lane-strided scan + butterfly arg-max,
+// excluding earlier picks by order).  The rounds are a loop, not unrolled:
+// the kernel runs once per layer on SMs whose instruction cache is cold, so
+// short code is faster than straight-line code.  Lane r < topk writes id r
+// (global, and sel_row if given) and weight r.
 __device__ __forceinline__ void route_token(const float* __restrict__ lg, const TokenLogits& tl, int experts,
                                             int topk, int method, int lane, int32_t* __restrict__ ids_t,
                                             float* __restrict__ w_t, int* sel_row, int64_t base, int64_t extent) {
     const bool in_regs = experts <= 32 * kRegLogits;
     float pv = INFINITY;
     int pe = -1;  // previous pick; round 0 admits everything
-    float top[kMaxTopK];
-#pragma unroll
-    for (int r = 0; r < kMaxTopK; ++r) {
-        if (r >= topk) break;
+    float my_v = 0.0f, top0 = 0.0f;
+    int my_e = 0;
+    uint32_t picked = 0u;  // in_regs: bit i = this lane's logit i is taken
+#pragma unroll 1
+    for (int r = 0; r < topk; ++r) {
         float bv = -INFINITY;
         int be = 0x7FFFFFFF;
         if (in_regs) {
+            // This lane's best unpicked logit (ids rise with i: a tie keeps
+            // the earlier, lower id).
+            uint32_t lk = 0u;
+            float lv = 0.0f;
+            int li = -1;
 #pragma unroll
             for (int i = 0; i < kRegLogits; ++i) {
-                const int e = lane + 32 * i;
-                const float v = tl.v[i];
-                if (e < experts && better(pv, pe, v, e) && better(v, e, bv, be)) { bv = v; be = e; }
+                const uint32_t k = logit_key(tl.v[i]);
+                if (lane + 32 * i < experts && !((picked >> i) & 1u) && (li < 0 || k > lk)) {
+                    lk = k;
+                    lv = tl.v[i];
+                    li = i;
+                }
             }
+            const uint32_t wk = __reduce_max_sync(0xFFFFFFFFu, li >= 0 ? lk : 0u);
+            const uint32_t cand = (li >= 0 && lk == wk) ? static_cast<uint32_t>(lane + 32 * li) : 0xFFFFFFFFu;
+            be = static_cast<int>(__reduce_min_sync(0xFFFFFFFFu, cand));
+            if ((be & 31) == lane) picked |= 1u << (be >> 5);
+            bv = __shfl_sync(0xFFFFFFFFu, lv, be & 31);
         } else {
             for (int e = lane; e < experts; e += 32) {
                 const float v = lg[e];
                 if (better(pv, pe, v, e) && better(v, e, bv, be)) { bv = v; be = e; }
             }
-        }
 #pragma unroll
-        for (int d = 16; d > 0; d >>= 1) {
-            const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, d);
-            const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, d);
-            if (better(ov, oe, bv, be)) { bv = ov; be = oe; }
+            for (int d = 16; d > 0; d >>= 1) {
+                const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, d);
+                const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, d);
+                if (better(ov, oe, bv, be)) { bv = ov; be = oe; }
+            }
         }
-        top[r] = bv;
-        if (lane == 0) {
-            if (store_ok(base + r, 1, extent)) ids_t[r] = be;  // ids_t = ids + base
-            if (sel_row) sel_row[r] = be;
-        }
+        if (lane == r) { my_v = bv; my_e = be; }
+        if (r == 0) top0 = bv;
         pv = bv;
         pe = be;
     }
-    // Weights (m = top[0] is the token's largest logit).
-    float z[kMaxTopK];
-    float zs = 0.0f;
-#pragma unroll
-    for (int r = 0; r < kMaxTopK; ++r) {
-        z[r] = r < topk ? expf(top[r] - top[0]) : 0.0f;
-        zs += z[r];
+    if (lane < topk) {
+        if (store_ok(base + lane, 1, extent)) ids_t[lane] = my_e;  // ids_t = ids + base
+        if (sel_row) sel_row[lane] = my_e;
     }
+    // Weights (top0 is the token's largest logit).
+    float z = lane < topk ? expf(my_v - top0) : 0.0f;
     if (method == 1) {
         // Softmax over all logits (lane-strided partial sums, then a fixed
         // butterfly: deterministic), then renormalize the k picks.
@@ -117,27 +152,14 @@ __device__ __forceinline__ void route_token(const float* __restrict__ lg, const 
         if (in_regs) {
 #pragma unroll
             for (int i = 0; i < kRegLogits; ++i)
-                if (lane + 32 * i < experts) all += expf(tl.v[i] - top[0]);
+                if (lane + 32 * i < experts) all += expf(tl.v[i] - top0);
         } else {
-            for (int e = lane; e < experts; e += 32) all += expf(lg[e] - top[0]);
+            for (int e = lane; e < experts; e += 32) all += expf(lg[e] - top0);
         }
-#pragma unroll
-        for (int d = 16; d > 0; d >>= 1) all += __shfl_xor_sync(0xFFFFFFFFu, all, d);
-        float ps = 0.0f;
-#pragma unroll
-        for (int r = 0; r < kMaxTopK; ++r) {
-            z[r] = z[r] / all;
-            ps += r < topk ? z[r] : 0.0f;
-        }
-        zs = ps;
+        z = z / warp_sum(all);
     }
-    if (lane < topk) {
-        float mine = 0.0f;
-#pragma unroll
-        for (int r = 0; r < kMaxTopK; ++r)
-            if (r == lane) mine = z[r];
-        if (store_ok(base + lane, 1, extent)) w_t[lane] = mine / zs;
-    }
+    const float zs = warp_sum(z);
+    if (lane < topk && store_ok(base + lane, 1, extent)) w_t[lane] = z / zs;
 }
 
 // One CTA per group of kGroup tokens, one warp per token.  The group's picks
@@ -187,22 +209,33 @@ __global__ void __launch_bounds__(32 * kGroup)
 // One CTA (thread e per expert, experts <= 1024): per-expert totals over the
 // groups -> offsets (block scan); each group's counts are replaced by the
 // group's first sorted row for that expert; then every pair gets its row
-// (group base + rank in the group) and each row its token.
+// (group base + rank in the group) and each row its token.  When the group
+// counts fit (use_smem) they are read once into shared memory with
+// independent loads and every later step works there.
 __global__ void __launch_bounds__(1024)
     route_scan_assign_kernel(int tokens, int experts, int topk, const int32_t* __restrict__ ids,
                              int32_t* __restrict__ grp, const int32_t* __restrict__ rank,
                              int32_t* __restrict__ offsets, int32_t* __restrict__ row_of,
-                             int32_t* __restrict__ sorted_token) {
+                             int32_t* __restrict__ sorted_token, int use_smem) {
+    extern __shared__ int sgrp[];
     __shared__ int warp_sum[32];
     // Waits for route_topk_kernel; never releases its own dependents early:
     // the grouped GEMMs read the offsets in their prologue.
     pdl_wait();
     const int groups = (tokens + kGroup - 1) / kGroup;
+    const int64_t cells = static_cast<int64_t>(groups) * experts;
+    int32_t* cnt = grp;
+    if (use_smem) {
+#pragma unroll 4
+        for (int i = threadIdx.x; i < static_cast<int>(cells); i += blockDim.x) sgrp[i] = grp[i];
+        __syncthreads();
+        cnt = sgrp;
+    }
     const int e = threadIdx.x;
     int total = 0;
     if (e < experts) {
 #pragma unroll 8
-        for (int g = 0; g < groups; ++g) total += grp[static_cast<size_t>(g) * experts + e];
+        for (int g = 0; g < groups; ++g) total += cnt[static_cast<size_t>(g) * experts + e];
     }
     // Block-wide exclusive scan of the totals over experts.
     const int lane = e & 31, w = e >> 5;
@@ -231,25 +264,31 @@ __global__ void __launch_bounds__(1024)
 #pragma unroll 8
         for (int g = 0; g < groups; ++g) {
             const size_t i = static_cast<size_t>(g) * experts + e;
-            const int c = grp[i];
-            if (store_ok(static_cast<int64_t>(i), 1, static_cast<int64_t>(groups) * experts)) grp[i] = run;
+            const int c = cnt[i];
+            if (use_smem || store_ok(static_cast<int64_t>(i), 1, cells)) cnt[i] = run;
             run += c;
         }
     }
     if (e == experts - 1) offsets[experts] = base + total;
     __syncthreads();  // this CTA's bases are visible to all of its threads
     const int pairs = tokens * topk;
+#pragma unroll 2
     for (int i = threadIdx.x; i < pairs; i += blockDim.x) {
         const int t = i / topk;
-        const int r = grp[static_cast<size_t>(t / kGroup) * experts + ids[i]] + rank[i];
+        const int r = cnt[static_cast<size_t>(t / kGroup) * experts + ids[i]] + rank[i];
         if (store_ok(i, 1, pairs)) row_of[i] = r;
         if (store_ok(r, 1, pairs)) sorted_token[r] = t;
     }
 }
 
 // One warp per (token, 256-column chunk): lane c8 sums 8 columns over the
-// token's k rows in slot order.
-constexpr int kFinThreads = 256;
+// token's k rows in slot order.  Slots go in chunks of kFinChunk: the
+// chunk's row indices and weights are loaded first, then its row segments,
+// so the loads overlap instead of forming k dependent round trips; the sum
+// keeps slot order.  Four-warp CTAs with a small register footprint stay
+// resident beside the grouped GEMM before it, waiting for it to finish.
+constexpr int kFinThreads = 128;
+constexpr int kFinChunk = 8;
 __global__ void __launch_bounds__(kFinThreads)
     finalize_kernel(const __nv_bfloat16* __restrict__ y2, const int32_t* __restrict__ row_of,
                     const float* __restrict__ weights, int64_t tokens, int topk, int64_t hidden,
@@ -266,15 +305,30 @@ __global__ void __launch_bounds__(kFinThreads)
         const int64_t c0 = (wi - t * chunks) * 256 + lane * 8;
         if (c0 >= hidden) continue;
         float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        for (int s = 0; s < topk; ++s) {
-            const int64_t r = row_of[t * topk + s];
-            const float w = weights[t * topk + s];
-            const uint4 raw = *reinterpret_cast<const uint4*>(y2 + r * hidden + c0);
-            const uint32_t wd[4] = {raw.x, raw.y, raw.z, raw.w};
+        for (int s0 = 0; s0 < topk; s0 += kFinChunk) {
+            int rows[kFinChunk];
+            float wts[kFinChunk];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                acc[2 * i] += w * __uint_as_float(wd[i] << 16);
-                acc[2 * i + 1] += w * __uint_as_float(wd[i] & 0xFFFF0000u);
+            for (int j = 0; j < kFinChunk; ++j) {
+                const bool live = s0 + j < topk;
+                rows[j] = live ? row_of[t * topk + s0 + j] : 0;
+                wts[j] = live ? weights[t * topk + s0 + j] : 0.0f;
+            }
+            uint4 raw[kFinChunk];
+#pragma unroll
+            for (int j = 0; j < kFinChunk; ++j)
+                raw[j] = s0 + j < topk
+                             ? *reinterpret_cast<const uint4*>(y2 + static_cast<int64_t>(rows[j]) * hidden + c0)
+                             : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int j = 0; j < kFinChunk; ++j) {
+                if (s0 + j >= topk) break;
+                const uint32_t wd[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    acc[2 * i] += wts[j] * __uint_as_float(wd[i] << 16);
+                    acc[2 * i + 1] += wts[j] * __uint_as_float(wd[i] & 0xFFFF0000u);
+                }
             }
         }
         uint32_t o[4];
@@ -322,8 +376,12 @@ cudaError_t launch_moe_route(const float* logits, int64_t tokens, int64_t expert
     if (e != cudaSuccess) return e;
     cfg.gridDim = dim3(1, 1, 1);
     cfg.blockDim = dim3(1024, 1, 1);  // one thread per expert
+    // Group counts in shared memory when they fit the default 48 KB.
+    const size_t cells_bytes = static_cast<size_t>(groups) * experts * sizeof(int32_t);
+    const int use_smem = cells_bytes <= kScanSmemBytes ? 1 : 0;
+    cfg.dynamicSmemBytes = use_smem ? cells_bytes : 0;
     return cudaLaunchKernelEx(&cfg, route_scan_assign_kernel, T, E, K, static_cast<const int32_t*>(ids), grp,
-                              static_cast<const int32_t*>(rank), offsets, row_of, sorted_token);
+                              static_cast<const int32_t*>(rank), offsets, row_of, sorted_token, use_smem);
 }
 
 cudaError_t launch_moe_finalize(const void* y2, const int32_t* row_of, const float* weights, int64_t tokens,
