@@ -78,51 +78,69 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// Inverse of logit_key (the shared key of +-0 reads back as +0, which
+// changes no weight: only differences with the largest pick are used).
+__device__ __forceinline__ float key_logit(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// Selection with the logits in registers, NREG per lane (lane l holds experts
+// l, l + 32, ...): every round each lane offers its best untaken key, the warp
+// takes the largest (redux.sync max) and, among the lanes holding it, the
+// lowest expert id (redux.sync min); the owning lane marks it taken.  Lane r
+// keeps pick r.  Keys are computed once; the rounds are a loop, not unrolled
+// (the kernel runs once per layer on SMs whose instruction cache is cold).
+template <int NREG>
+__device__ __forceinline__ void select_in_regs(const TokenLogits& tl, int experts, int topk, int lane, float& my_v,
+                                               int& my_e, float& top0) {
+    uint32_t key[NREG];
+    uint32_t avail = 0u;  // bit i: logit i of this lane exists and is not yet taken
+#pragma unroll
+    for (int i = 0; i < NREG; ++i) {
+        key[i] = logit_key(tl.v[i]);
+        if (lane + 32 * i < experts) avail |= 1u << i;
+    }
+#pragma unroll 1
+    for (int r = 0; r < topk; ++r) {
+        uint32_t lk = 0u;
+        int li = -1;
+#pragma unroll
+        for (int i = 0; i < NREG; ++i)
+            if (((avail >> i) & 1u) && (li < 0 || key[i] > lk)) { lk = key[i]; li = i; }
+        const uint32_t wk = __reduce_max_sync(0xFFFFFFFFu, li >= 0 ? lk : 0u);
+        const uint32_t cand = (li >= 0 && lk == wk) ? static_cast<uint32_t>(lane + 32 * li) : 0xFFFFFFFFu;
+        const int be = static_cast<int>(__reduce_min_sync(0xFFFFFFFFu, cand));
+        if ((be & 31) == lane) avail &= ~(1u << (be >> 5));
+        const float bv = key_logit(wk);
+        if (lane == r) { my_v = bv; my_e = be; }
+        if (r == 0) top0 = bv;
+    }
+}
+
 // Top-k of one token by its warp and its weights.  Round r picks the best
 // logit not yet taken (larger value, then lower id), so the picks come out in
 // that total order; lane r keeps pick r.  Logits in registers (experts <=
-// 32 * kRegLogits): every lane offers its best unpicked logit, the warp takes
-// the largest key (redux.sync max) and, among the lanes holding it, the
-// lowest expert id (redux.sync min); the owning lane marks it taken.  Wider
-// layers rescan the logits each round (lane-strided scan + butterfly arg-max,
-// excluding earlier picks by order).  The rounds are a loop, not unrolled:
-// the kernel runs once per layer on SMs whose instruction cache is cold, so
-// short code is faster than straight-line code.  Lane r < topk writes id r
-// (global, and sel_row if given) and weight r.
+// 32 * kRegLogits) go through select_in_regs; wider layers rescan the logits
+// each round (lane-strided scan + butterfly arg-max, excluding earlier picks
+// by order).  Lane r < topk writes id r (global, and sel_row if given) and
+// weight r.
 __device__ __forceinline__ void route_token(const float* __restrict__ lg, const TokenLogits& tl, int experts,
                                             int topk, int method, int lane, int32_t* __restrict__ ids_t,
                                             float* __restrict__ w_t, int* sel_row, int64_t base, int64_t extent) {
     const bool in_regs = experts <= 32 * kRegLogits;
-    float pv = INFINITY;
-    int pe = -1;  // previous pick; round 0 admits everything
     float my_v = 0.0f, top0 = 0.0f;
     int my_e = 0;
-    uint32_t picked = 0u;  // in_regs: bit i = this lane's logit i is taken
+    if (experts <= 32 * 4) {
+        select_in_regs<4>(tl, experts, topk, lane, my_v, my_e, top0);
+    } else if (in_regs) {
+        select_in_regs<kRegLogits>(tl, experts, topk, lane, my_v, my_e, top0);
+    } else {
+        float pv = INFINITY;
+        int pe = -1;  // previous pick; round 0 admits everything
 #pragma unroll 1
-    for (int r = 0; r < topk; ++r) {
-        float bv = -INFINITY;
-        int be = 0x7FFFFFFF;
-        if (in_regs) {
-            // This lane's best unpicked logit (ids rise with i: a tie keeps
-            // the earlier, lower id).
-            uint32_t lk = 0u;
-            float lv = 0.0f;
-            int li = -1;
-#pragma unroll
-            for (int i = 0; i < kRegLogits; ++i) {
-                const uint32_t k = logit_key(tl.v[i]);
-                if (lane + 32 * i < experts && !((picked >> i) & 1u) && (li < 0 || k > lk)) {
-                    lk = k;
-                    lv = tl.v[i];
-                    li = i;
-                }
-            }
-            const uint32_t wk = __reduce_max_sync(0xFFFFFFFFu, li >= 0 ? lk : 0u);
-            const uint32_t cand = (li >= 0 && lk == wk) ? static_cast<uint32_t>(lane + 32 * li) : 0xFFFFFFFFu;
-            be = static_cast<int>(__reduce_min_sync(0xFFFFFFFFu, cand));
-            if ((be & 31) == lane) picked |= 1u << (be >> 5);
-            bv = __shfl_sync(0xFFFFFFFFu, lv, be & 31);
-        } else {
+        for (int r = 0; r < topk; ++r) {
+            float bv = -INFINITY;
+            int be = 0x7FFFFFFF;
             for (int e = lane; e < experts; e += 32) {
                 const float v = lg[e];
                 if (better(pv, pe, v, e) && better(v, e, bv, be)) { bv = v; be = e; }
@@ -133,11 +151,11 @@ __device__ __forceinline__ void route_token(const float* __restrict__ lg, const 
                 const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, d);
                 if (better(ov, oe, bv, be)) { bv = ov; be = oe; }
             }
+            if (lane == r) { my_v = bv; my_e = be; }
+            if (r == 0) top0 = bv;
+            pv = bv;
+            pe = be;
         }
-        if (lane == r) { my_v = bv; my_e = be; }
-        if (r == 0) top0 = bv;
-        pv = bv;
-        pe = be;
     }
     if (lane < topk) {
         if (store_ok(base + lane, 1, extent)) ids_t[lane] = my_e;  // ids_t = ids + base
@@ -206,6 +224,31 @@ __global__ void __launch_bounds__(32 * kGroup)
             grp_count[static_cast<size_t>(group) * experts + e] = __popc(bits[e]);
 }
 
+// Exclusive prefix sum of v over the threads of the block in thread order
+// (every thread calls it; warp_sum holds 32 ints of shared memory).
+__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sum) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+        if (lane >= d) incl += y;
+    }
+    if (lane == 31) warp_sum[w] = incl;
+    __syncthreads();
+    if (w == 0) {
+        int sw = lane < static_cast<int>(blockDim.x >> 5) ? warp_sum[lane] : 0;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int y = __shfl_up_sync(0xFFFFFFFFu, sw, d);
+            if (lane >= d) sw += y;
+        }
+        warp_sum[lane] = sw;  // inclusive over warps
+    }
+    __syncthreads();
+    return incl - v + (w > 0 ? warp_sum[w - 1] : 0);
+}
+
 // One CTA (thread e per expert, experts <= 1024): per-expert totals over the
 // groups -> offsets (block scan); each group's counts are replaced by the
 // group's first sorted row for that expert; then every pair gets its row
@@ -237,27 +280,7 @@ __global__ void __launch_bounds__(1024)
 #pragma unroll 8
         for (int g = 0; g < groups; ++g) total += cnt[static_cast<size_t>(g) * experts + e];
     }
-    // Block-wide exclusive scan of the totals over experts.
-    const int lane = e & 31, w = e >> 5;
-    int incl = total;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        const int y = __shfl_up_sync(0xFFFFFFFFu, incl, d);
-        if (lane >= d) incl += y;
-    }
-    if (lane == 31) warp_sum[w] = incl;
-    __syncthreads();
-    if (w == 0) {
-        int sw = lane < (blockDim.x >> 5) ? warp_sum[lane] : 0;
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const int y = __shfl_up_sync(0xFFFFFFFFu, sw, d);
-            if (lane >= d) sw += y;
-        }
-        warp_sum[lane] = sw;  // inclusive over warps
-    }
-    __syncthreads();
-    const int base = incl - total + (w > 0 ? warp_sum[w - 1] : 0);
+    const int base = block_exclusive_scan(total, warp_sum);
     if (e < experts) {
         if (store_ok(e, 1, experts + 1)) offsets[e] = base;
         int run = base;
@@ -279,6 +302,98 @@ __global__ void __launch_bounds__(1024)
         if (store_ok(i, 1, pairs)) row_of[i] = r;
         if (store_ok(r, 1, pairs)) sorted_token[r] = t;
     }
+}
+
+// Routing in one launch for up to kClusterTokens tokens: one cluster of
+// kClusterCtas CTAs of 32 warps.  Tokens form 32-token groups; group g is
+// routed by CTA g % kClusterCtas in pass g / kClusterCtas, one warp per
+// token.  Each CTA records, per pass and expert, the mask of the group's
+// tokens that picked the expert.  After a cluster barrier every CTA reads
+// all groups' counts (mask popcounts) from its peers' shared memory in group
+// order, so that thread e knows expert e's total and the count before each of
+// its own groups; a block scan of the totals gives the offsets (written by
+// CTA 0), and each pair's row is its expert's offset + the count of earlier
+// groups + its rank among the group's tokens (a popcount of the mask below
+// it): the stable expert-sorted order.  A second barrier phase keeps every
+// CTA alive until no peer reads its masks any more.  The kernel never
+// releases its dependents early: the grouped GEMMs read the offsets in their
+// prologue.
+constexpr int kClusterCtas = 8;
+constexpr int kClusterMaxPasses = 2;
+constexpr int kClusterTokens = kClusterCtas * 32 * kClusterMaxPasses;
+__global__ void __launch_bounds__(1024, 1)
+    route_cluster_kernel(const float* __restrict__ logits, int tokens, int experts, int topk, int method,
+                         int32_t* __restrict__ ids, float* __restrict__ weights, int32_t* __restrict__ offsets,
+                         int32_t* __restrict__ row_of, int32_t* __restrict__ sorted_token) {
+    extern __shared__ uint32_t route_smem[];  // masks [passes][experts], then bases [passes][experts]
+    __shared__ int sel[kClusterMaxPasses][32][kMaxTopK];
+    __shared__ int warp_sum[32];
+    const int lane = threadIdx.x & 31;
+    const int w = threadIdx.x >> 5;
+    const int crank = static_cast<int>(cluster_rank());
+    const int groups = (tokens + 31) / 32;
+    const int passes = (groups + kClusterCtas - 1) / kClusterCtas;
+    uint32_t* masks = route_smem;
+    int* base = reinterpret_cast<int*>(route_smem + passes * experts);
+    for (int i = threadIdx.x; i < passes * experts; i += blockDim.x) masks[i] = 0u;
+    pdl_wait();  // the logits come from the previous kernel
+    const int64_t pairs = static_cast<int64_t>(tokens) * topk;
+    for (int j = 0; j < passes; ++j) {
+        const int t = (j * kClusterCtas + crank) * 32 + w;
+        if (t < tokens) {
+            const float* lg = logits + static_cast<size_t>(t) * experts;
+            TokenLogits tl;
+            if (experts <= 32 * kRegLogits) load_token_logits(lg, experts, lane, tl);
+            route_token(lg, tl, experts, topk, method, lane, ids + static_cast<size_t>(t) * topk,
+                        weights + static_cast<size_t>(t) * topk, sel[j][w], static_cast<int64_t>(t) * topk, pairs);
+        }
+    }
+    __syncthreads();
+    const int local_pairs = passes * 32 * topk;
+    for (int i = threadIdx.x; i < local_pairs; i += blockDim.x) {
+        const int j = i / (32 * topk), tw = (i / topk) % 32;
+        if ((j * kClusterCtas + crank) * 32 + tw < tokens) atomicOr(&masks[j * experts + sel[j][tw][i % topk]], 1u << tw);
+    }
+    cluster_arrive_release();  // every CTA's masks are complete ...
+    cluster_wait_acquire();    // ... before any peer reads them
+    const int e = threadIdx.x;
+    int total = 0;
+    int before[kClusterMaxPasses];
+#pragma unroll
+    for (int j = 0; j < kClusterMaxPasses; ++j) before[j] = 0;
+    if (e < experts) {
+#pragma unroll 4
+        for (int g = 0; g < groups; ++g) {
+            const uint32_t a = map_to_rank(smem_addr(&masks[(g / kClusterCtas) * experts + e]),
+                                           static_cast<uint32_t>(g % kClusterCtas));
+            const int c = __popc(ld_shared_cluster_u32(a));
+#pragma unroll
+            for (int j = 0; j < kClusterMaxPasses; ++j)
+                if (g < j * kClusterCtas + crank) before[j] += c;
+            total += c;
+        }
+    }
+    cluster_arrive_relaxed();  // this thread's remote reads are done
+    const int off = block_exclusive_scan(e < experts ? total : 0, warp_sum);
+    if (e < experts) {
+        if (crank == 0 && store_ok(e, 1, experts + 1)) offsets[e] = off;
+        if (crank == 0 && e == experts - 1) offsets[experts] = off + total;
+#pragma unroll
+        for (int j = 0; j < kClusterMaxPasses; ++j)
+            if (j < passes) base[j * experts + e] = off + before[j];
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < local_pairs; i += blockDim.x) {
+        const int j = i / (32 * topk), tw = (i / topk) % 32, sl = i % topk;
+        const int t = (j * kClusterCtas + crank) * 32 + tw;
+        if (t >= tokens) continue;
+        const int ex = sel[j][tw][sl];
+        const int r = base[j * experts + ex] + __popc(masks[j * experts + ex] & ((1u << tw) - 1u));
+        const int64_t pi = static_cast<int64_t>(t) * topk + sl;
+        if (store_ok(pi, 1, pairs)) row_of[pi] = r;
+        if (store_ok(r, 1, pairs)) sorted_token[r] = t;
+    }
+    cluster_wait();  // no peer reads this CTA's masks any more
 }
 
 // One warp per (token, 256-column chunk): lane c8 sums 8 columns over the
@@ -367,6 +482,23 @@ cudaError_t launch_moe_route(const float* logits, int64_t tokens, int64_t expert
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     const int T = static_cast<int>(tokens), E = static_cast<int>(experts), K = static_cast<int>(topk);
+    if (tokens <= kClusterTokens) {
+        // One launch: a single cluster routes every token and sorts the pairs.
+        cudaLaunchAttribute attrs[2];
+        attrs[0] = attr;
+        attrs[1].id = cudaLaunchAttributeClusterDimension;
+        attrs[1].val.clusterDim.x = kClusterCtas;
+        attrs[1].val.clusterDim.y = 1;
+        attrs[1].val.clusterDim.z = 1;
+        cfg.attrs = attrs;
+        cfg.numAttrs = 2;
+        cfg.gridDim = dim3(kClusterCtas, 1, 1);
+        cfg.blockDim = dim3(1024, 1, 1);
+        const int passes = (T + 32 * kClusterCtas - 1) / (32 * kClusterCtas);
+        cfg.dynamicSmemBytes = static_cast<size_t>(passes) * E * 2 * sizeof(uint32_t);
+        return cudaLaunchKernelEx(&cfg, route_cluster_kernel, logits, T, E, K, method, ids, weights, offsets, row_of,
+                                  sorted_token);
+    }
     const int groups = static_cast<int>((tokens + kGroup - 1) / kGroup);
     int32_t* grp = ws;
     int32_t* rank = ws + static_cast<size_t>(groups) * experts;

@@ -34,7 +34,9 @@ def _route_both(mx, logits, topk, method):
 @pytest.mark.parametrize("method", [M.RENORMALIZE, M.RENORMALIZE_NAIVE])
 @pytest.mark.parametrize("shape", [(256, 128, 8, False), (37, 8, 2, False), (64, 16, 16, False),
                                    (33, 8, 8, False), (200, 32, 4, True), (1, 4, 1, False),
-                                   # above 16384 (token, slot) pairs: the multi-CTA routing path
+                                   # up to 512 tokens one cluster routes (two passes above 256);
+                                   # above, two kernels (per-group selection, then one scan)
+                                   (300, 128, 8, False), (512, 64, 4, True), (513, 32, 2, False),
                                    (3000, 64, 8, False), (2100, 32, 8, True)])
 def test_route_matches_oracle(lib, method, shape):
     t, e, k, ties = shape
