@@ -523,10 +523,12 @@ static mxfp8_status check_route_shape(int64_t tokens, int64_t experts, int64_t t
     return MXFP8_OK;
 }
 
-mxfp8_status mxfp8_moe_route(const float* logits, int64_t tokens, int64_t experts, int64_t topk,
-                             mxfp8_route_method method, int32_t* topk_ids, float* topk_weights,
-                             int32_t* expert_offsets, int32_t* sorted_token, int32_t* row_of, void* ws,
-                             size_t ws_bytes, void* stream) {
+// release: the routing kernel may release the next kernel early (only the
+// MoE layer, whose next kernel is the gathering quantizer).
+static mxfp8_status route_checked(const float* logits, int64_t tokens, int64_t experts, int64_t topk,
+                                  mxfp8_route_method method, int32_t* topk_ids, float* topk_weights,
+                                  int32_t* expert_offsets, int32_t* sorted_token, int32_t* row_of, void* ws,
+                                  size_t ws_bytes, void* stream, bool release) {
     mxfp8_status st = check_route_shape(tokens, experts, topk);
     if (st != MXFP8_OK) return st;
     if (method != MXFP8_ROUTE_RENORMALIZE && method != MXFP8_ROUTE_RENORMALIZE_NAIVE) return MXFP8_ERR_INVALID_ARG;
@@ -541,8 +543,16 @@ mxfp8_status mxfp8_moe_route(const float* logits, int64_t tokens, int64_t expert
     if ((st = device_sms(&sms)) != MXFP8_OK) return st;
     cudaError_t e = mxk::launch_moe_route(logits, tokens, experts, topk, static_cast<int>(method), topk_ids,
                                           topk_weights, expert_offsets, sorted_token, row_of,
-                                          static_cast<int32_t*>(ws), static_cast<cudaStream_t>(stream));
+                                          static_cast<int32_t*>(ws), static_cast<cudaStream_t>(stream), release);
     return e == cudaSuccess ? MXFP8_OK : cuda_fail(e);
+}
+
+mxfp8_status mxfp8_moe_route(const float* logits, int64_t tokens, int64_t experts, int64_t topk,
+                             mxfp8_route_method method, int32_t* topk_ids, float* topk_weights,
+                             int32_t* expert_offsets, int32_t* sorted_token, int32_t* row_of, void* ws,
+                             size_t ws_bytes, void* stream) {
+    return route_checked(logits, tokens, experts, topk, method, topk_ids, topk_weights, expert_offsets,
+                         sorted_token, row_of, ws, ws_bytes, stream, false);
 }
 
 static mxfp8_status check_gated(const mxfp8_weight* w) {
@@ -606,8 +616,11 @@ mxfp8_status mxfp8_moe_gate_up_swiglu(const void* x, const int32_t* sorted_token
                           static_cast<cudaStream_t>(stream));
 }
 
-mxfp8_status mxfp8_moe_finalize(const void* y2, const int32_t* row_of, const float* topk_weights,
-                                int64_t tokens, int64_t topk, int64_t hidden, void* out, void* stream) {
+// slots_ready: row_of and the weights were complete before the kernel ahead
+// of the finalize kernel began (the MoE layer: they come from its routing).
+static mxfp8_status finalize_checked(const void* y2, const int32_t* row_of, const float* topk_weights,
+                                     int64_t tokens, int64_t topk, int64_t hidden, void* out, void* stream,
+                                     bool slots_ready) {
     if (tokens < 0 || topk < 1 || topk > 16 || hidden < 8 || hidden % 8 != 0 || hidden > kMaxK)
         return MXFP8_ERR_INVALID_ARG;
     if (tokens * topk >= (int64_t(1) << 31)) return MXFP8_ERR_INVALID_ARG;
@@ -620,8 +633,13 @@ mxfp8_status mxfp8_moe_finalize(const void* y2, const int32_t* row_of, const flo
     mxfp8_status st = device_sms(&sms);
     if (st != MXFP8_OK) return st;
     cudaError_t e = mxk::launch_moe_finalize(y2, row_of, topk_weights, tokens, topk, hidden, out, sms,
-                                             static_cast<cudaStream_t>(stream));
+                                             static_cast<cudaStream_t>(stream), slots_ready);
     return e == cudaSuccess ? MXFP8_OK : cuda_fail(e);
+}
+
+mxfp8_status mxfp8_moe_finalize(const void* y2, const int32_t* row_of, const float* topk_weights,
+                                int64_t tokens, int64_t topk, int64_t hidden, void* out, void* stream) {
+    return finalize_checked(y2, row_of, topk_weights, tokens, topk, hidden, out, stream, false);
 }
 
 namespace {
@@ -678,24 +696,29 @@ mxfp8_status mxfp8_moe_expert_mlp(const void* x, const float* logits, int64_t to
     int32_t* stok = reinterpret_cast<int32_t*>(b + l.sorted_token);
     int32_t* row_of = reinterpret_cast<int32_t*>(b + l.row_of);
     const int64_t r = tokens * topk;
-    st = mxfp8_moe_route(logits, tokens, experts, topk, method, ids, wts, off, stok, row_of, b + l.route,
-                         mxfp8_moe_route_workspace_bytes(tokens, experts, topk), stream);
-    if (st != MXFP8_OK) return st;
-    // GEMM1's SwiGLU epilogue writes h already quantized (E4M3 + 8x4 scales,
-    // the bytes the activation quantizer would make of the BF16 h) into the
-    // GEMM2 activation buffers, so GEMM2 runs on them directly.
     int sms = 0;
     if ((st = device_sms(&sms)) != MXFP8_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // GEMM1's SwiGLU epilogue writes h already quantized (E4M3 + 8x4 scales,
+    // the bytes the activation quantizer would make of the BF16 h) into the
+    // GEMM2 activation buffers, so GEMM2 runs on them directly.
     uint8_t* hq = b + l.g2;
     uint8_t* hsf = hq + ceil_to(r * inter, 256);
     if (r % 8 != 0) {
         // Rows r..ceil8(r)-1 of h's last 8-row scale group hold 0x00, as the
-        // quantizer writes them: clear that group; GEMM1 then fills rows < r.
+        // quantizer writes them: clear that group (before routing, so that the
+        // router's next kernel is the gathering quantizer); GEMM1 then fills
+        // rows < r.
         const int64_t grp = ceil_to(inter / 32, 4) * 8;
         cudaError_t e = cudaMemsetAsync(hsf + (r / 8) * grp, 0, static_cast<size_t>(grp), s);
         if (e != cudaSuccess) return cuda_fail(e);
     }
+    // The router may release the gathering quantizer early: that kernel waits
+    // for the router before it releases GEMM1, which reads the offsets in its
+    // prologue.
+    st = route_checked(logits, tokens, experts, topk, method, ids, wts, off, stok, row_of, b + l.route,
+                       mxfp8_moe_route_workspace_bytes(tokens, experts, topk), stream, true);
+    if (st != MXFP8_OK) return st;
     st = gate_up_launch(x, stok, r, off, w13, nullptr, hq, hsf, b + l.g1, sms, s);
     if (st != MXFP8_OK) return st;
     mxk::GemmProblem p2 = make_problem(hq, hsf, r, w2, nullptr, b + l.y2, off, nullptr);
@@ -703,7 +726,7 @@ mxfp8_status mxfp8_moe_expert_mlp(const void* x, const float* logits, int64_t to
     bool enc_fail = false;
     cudaError_t e = mxk::launch_gemm(p2, sch2, sms, s, &enc_fail);
     if ((st = launch_status(e, enc_fail)) != MXFP8_OK) return st;
-    return mxfp8_moe_finalize(b + l.y2, row_of, wts, tokens, topk, hidden, out, stream);
+    return finalize_checked(b + l.y2, row_of, wts, tokens, topk, hidden, out, stream, true);
 }
 
 const char* mxfp8_status_string(mxfp8_status s) {

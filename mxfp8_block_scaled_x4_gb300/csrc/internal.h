@@ -28,10 +28,13 @@ cudaError_t launch_prepare_weight(const void* src, bool src_is_bf16, int64_t exp
 // group counts plus tokens * topk ranks (int32).
 cudaError_t launch_moe_route(const float* logits, int64_t tokens, int64_t experts, int64_t topk, int method,
                              int32_t* ids, float* weights, int32_t* offsets, int32_t* sorted_token,
-                             int32_t* row_of, int32_t* ws, cudaStream_t s);
+                             int32_t* row_of, int32_t* ws, cudaStream_t s, bool release = false);
 // out[t] = bf16(sum_s weights[t, s] * y2[row_of[t * topk + s]]), FP32 sum in slot order.
+// slots_ready: row_of and weights were complete before the kernel this one
+// depends on began (they may then be read before the dependency wait).
 cudaError_t launch_moe_finalize(const void* y2, const int32_t* row_of, const float* weights, int64_t tokens,
-                                int64_t topk, int64_t hidden, void* out, int num_sms, cudaStream_t s);
+                                int64_t topk, int64_t hidden, void* out, int num_sms, cudaStream_t s,
+                                bool slots_ready = false);
 
 struct GemmProblem {
     const uint8_t* qa;         // [m][k] E4M3 activations

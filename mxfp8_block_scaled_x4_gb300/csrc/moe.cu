@@ -259,11 +259,13 @@ __global__ void __launch_bounds__(1024)
     route_scan_assign_kernel(int tokens, int experts, int topk, const int32_t* __restrict__ ids,
                              int32_t* __restrict__ grp, const int32_t* __restrict__ rank,
                              int32_t* __restrict__ offsets, int32_t* __restrict__ row_of,
-                             int32_t* __restrict__ sorted_token, int use_smem) {
+                             int32_t* __restrict__ sorted_token, int use_smem, int release) {
     extern __shared__ int sgrp[];
     __shared__ int warp_sum[32];
-    // Waits for route_topk_kernel; never releases its own dependents early:
-    // the grouped GEMMs read the offsets in their prologue.
+    // Waits for route_topk_kernel.  Releases its dependent early only when
+    // told (inside the MoE layer: the gathering quantizer, which waits for
+    // this grid before releasing the grouped GEMM that reads the offsets).
+    if (release) pdl_launch_dependents();
     pdl_wait();
     const int groups = (tokens + kGroup - 1) / kGroup;
     const int64_t cells = static_cast<int64_t>(groups) * experts;
@@ -315,17 +317,19 @@ __global__ void __launch_bounds__(1024)
 // CTA 0), and each pair's row is its expert's offset + the count of earlier
 // groups + its rank among the group's tokens (a popcount of the mask below
 // it): the stable expert-sorted order.  A second barrier phase keeps every
-// CTA alive until no peer reads its masks any more.  The kernel never
-// releases its dependents early: the grouped GEMMs read the offsets in their
-// prologue.
+// CTA alive until no peer reads its masks any more.  The kernel releases its
+// dependent early only when told (`release`): inside the MoE layer, whose
+// next kernel is the gathering quantizer that waits for this grid before it
+// releases the grouped GEMM (which reads the offsets in its prologue).
 constexpr int kClusterCtas = 8;
 constexpr int kClusterMaxPasses = 2;
 constexpr int kClusterTokens = kClusterCtas * 32 * kClusterMaxPasses;
 __global__ void __launch_bounds__(1024, 1)
     route_cluster_kernel(const float* __restrict__ logits, int tokens, int experts, int topk, int method,
                          int32_t* __restrict__ ids, float* __restrict__ weights, int32_t* __restrict__ offsets,
-                         int32_t* __restrict__ row_of, int32_t* __restrict__ sorted_token) {
+                         int32_t* __restrict__ row_of, int32_t* __restrict__ sorted_token, int release) {
     extern __shared__ uint32_t route_smem[];  // masks [passes][experts], then bases [passes][experts]
+    if (release) pdl_launch_dependents();
     __shared__ int sel[kClusterMaxPasses][32][kMaxTopK];
     __shared__ int warp_sum[32];
     const int lane = threadIdx.x & 31;
@@ -407,28 +411,36 @@ constexpr int kFinChunk = 8;
 __global__ void __launch_bounds__(kFinThreads)
     finalize_kernel(const __nv_bfloat16* __restrict__ y2, const int32_t* __restrict__ row_of,
                     const float* __restrict__ weights, int64_t tokens, int topk, int64_t hidden,
-                    __nv_bfloat16* __restrict__ out) {
+                    __nv_bfloat16* __restrict__ out, int slots_ready) {
     pdl_launch_dependents();
-    pdl_wait();  // y2 comes from the previous kernel
     const int lane = threadIdx.x & 31;
     const int64_t chunks = (hidden + 255) >> 8;
     const int64_t total = tokens * chunks;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kFinThreads) >> 5;
-    for (int64_t wi = (static_cast<int64_t>(blockIdx.x) * kFinThreads + threadIdx.x) >> 5; wi < total;
-         wi += nwarps) {
+    const int64_t first = (static_cast<int64_t>(blockIdx.x) * kFinThreads + threadIdx.x) >> 5;
+    int rows[kFinChunk];
+    float wts[kFinChunk];
+    auto load_slots = [&](int64_t t, int s0) {
+#pragma unroll
+        for (int j = 0; j < kFinChunk; ++j) {
+            const bool live = s0 + j < topk;
+            rows[j] = live ? row_of[t * topk + s0 + j] : 0;
+            wts[j] = live ? weights[t * topk + s0 + j] : 0.0f;
+        }
+    };
+    // slots_ready: row_of and the weights were complete before the kernel
+    // this grid depends on began (inside the MoE layer they come from its
+    // routing kernel), so the first item's slots load before the wait.
+    const bool early = slots_ready && first < total;
+    if (early) load_slots(first / chunks, 0);
+    pdl_wait();  // y2 comes from the previous kernel
+    for (int64_t wi = first; wi < total; wi += nwarps) {
         const int64_t t = wi / chunks;
         const int64_t c0 = (wi - t * chunks) * 256 + lane * 8;
         if (c0 >= hidden) continue;
         float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
         for (int s0 = 0; s0 < topk; s0 += kFinChunk) {
-            int rows[kFinChunk];
-            float wts[kFinChunk];
-#pragma unroll
-            for (int j = 0; j < kFinChunk; ++j) {
-                const bool live = s0 + j < topk;
-                rows[j] = live ? row_of[t * topk + s0 + j] : 0;
-                wts[j] = live ? weights[t * topk + s0 + j] : 0.0f;
-            }
+            if (!(early && wi == first && s0 == 0)) load_slots(t, s0);
             uint4 raw[kFinChunk];
 #pragma unroll
             for (int j = 0; j < kFinChunk; ++j)
@@ -462,16 +474,18 @@ __global__ void __launch_bounds__(kFinThreads)
 
 cudaError_t read_and_clear_oob_moe(unsigned int* out) { return read_and_clear_oob_word(out); }
 
-// Both routing kernels are launched with programmatic stream serialization so
+// The routing kernels are launched with programmatic stream serialization so
 // that their launches overlap the kernel before them (each waits for it
-// before reading its inputs).  route_topk_kernel releases its dependent (the
-// second routing kernel) at once; route_scan_assign_kernel never does: the
-// grouped GEMMs read the expert offsets in their prologue, before their own
-// griddepcontrol.wait, so every kernel after the router must start only once
-// the offsets are complete.
+// before reading its inputs).  Up to kClusterTokens tokens one cluster kernel
+// does everything; above, route_topk_kernel releases its dependent (the
+// second routing kernel) at once.  The kernel that writes the offsets
+// releases its own dependent early only with `release` (the MoE layer, whose
+// next kernel is the gathering quantizer): the grouped GEMMs read the expert
+// offsets in their prologue, before their own griddepcontrol.wait, so no
+// grouped GEMM may start before the offsets are complete.
 cudaError_t launch_moe_route(const float* logits, int64_t tokens, int64_t experts, int64_t topk, int method,
                              int32_t* ids, float* weights, int32_t* offsets, int32_t* sorted_token,
-                             int32_t* row_of, int32_t* ws, cudaStream_t s) {
+                             int32_t* row_of, int32_t* ws, cudaStream_t s, bool release) {
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr.val.programmaticStreamSerializationAllowed = 1;
@@ -497,7 +511,7 @@ cudaError_t launch_moe_route(const float* logits, int64_t tokens, int64_t expert
         const int passes = (T + 32 * kClusterCtas - 1) / (32 * kClusterCtas);
         cfg.dynamicSmemBytes = static_cast<size_t>(passes) * E * 2 * sizeof(uint32_t);
         return cudaLaunchKernelEx(&cfg, route_cluster_kernel, logits, T, E, K, method, ids, weights, offsets, row_of,
-                                  sorted_token);
+                                  sorted_token, release ? 1 : 0);
     }
     const int groups = static_cast<int>((tokens + kGroup - 1) / kGroup);
     int32_t* grp = ws;
@@ -513,11 +527,13 @@ cudaError_t launch_moe_route(const float* logits, int64_t tokens, int64_t expert
     const int use_smem = cells_bytes <= kScanSmemBytes ? 1 : 0;
     cfg.dynamicSmemBytes = use_smem ? cells_bytes : 0;
     return cudaLaunchKernelEx(&cfg, route_scan_assign_kernel, T, E, K, static_cast<const int32_t*>(ids), grp,
-                              static_cast<const int32_t*>(rank), offsets, row_of, sorted_token, use_smem);
+                              static_cast<const int32_t*>(rank), offsets, row_of, sorted_token, use_smem,
+                              release ? 1 : 0);
 }
 
 cudaError_t launch_moe_finalize(const void* y2, const int32_t* row_of, const float* weights, int64_t tokens,
-                                int64_t topk, int64_t hidden, void* out, int num_sms, cudaStream_t s) {
+                                int64_t topk, int64_t hidden, void* out, int num_sms, cudaStream_t s,
+                                bool slots_ready) {
     const int64_t work = tokens * ((hidden + 255) / 256);  // warps of work
     int64_t blocks = (work + (kFinThreads / 32) - 1) / (kFinThreads / 32);
     if (blocks > static_cast<int64_t>(num_sms) * 8) blocks = static_cast<int64_t>(num_sms) * 8;
@@ -533,7 +549,8 @@ cudaError_t launch_moe_finalize(const void* y2, const int32_t* row_of, const flo
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, finalize_kernel, static_cast<const __nv_bfloat16*>(y2), row_of, weights, tokens,
-                              static_cast<int>(topk), hidden, static_cast<__nv_bfloat16*>(out));
+                              static_cast<int>(topk), hidden, static_cast<__nv_bfloat16*>(out),
+                              slots_ready ? 1 : 0);
 }
 
 }  // namespace mxk

@@ -61,12 +61,16 @@ __global__ void __launch_bounds__(kThreads) quant_act_kernel(const __nv_bfloat16
                                                              const int32_t* __restrict__ src_rows,
                                                              uint8_t* __restrict__ q,
                                                              uint8_t* __restrict__ sf) {
-    // Dependent kernels (the GEMM) may start their prologue now; they wait
+    // Dependent kernels (the GEMM) may start their prologue early; they wait
     // for this grid's completion before reading what it writes.  This grid
     // itself may start before the kernel that produced x has finished: every
-    // CTA waits for it before touching x, q or sf.
-    pdl_launch_dependents();
+    // CTA waits for it before touching x, q or sf.  The gathering variant
+    // (MoE GEMM1's rows) releases its dependent only after that wait: the
+    // grouped GEMM reads the expert offsets in its prologue, and they come
+    // from the routing kernel this grid waits for.
+    if constexpr (!kGather) pdl_launch_dependents();
     pdl_wait();
+    if constexpr (kGather) pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int64_t quads = k >> 7;  // 128-column patches per row group
     const int64_t total = (m8 >> 3) * quads;
