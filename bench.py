@@ -148,8 +148,13 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------ timing utils
-def graph_of(fn, n):
-    """Capture n back-to-back invocations of fn(i) into one CUDA graph."""
+def graph_of(fn, n, pre=None, post=None):
+    """Capture n back-to-back invocations of fn(i) into one CUDA graph.
+    pre: an event recorded (event record node) once an untimed invocation
+    captured ahead of the n has completed, on a side branch: the first of the
+    n keeps its programmatic dependency on that invocation, as every call has
+    on the one before it.  post: an event recorded after the n (and the side
+    branch) complete."""
     import torch
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
@@ -159,21 +164,70 @@ def graph_of(fn, n):
     torch.cuda.current_stream().wait_stream(s)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
     with torch.cuda.graph(g):
+        cs = torch.cuda.current_stream()
+        if pre is not None:
+            fn(n)  # untimed: the call before the first timed one
+            side.wait_stream(cs)
+            with torch.cuda.stream(side):
+                pre.record()
         for i in range(n):
             fn(i)
+        if pre is not None:
+            cs.wait_stream(side)
+        if post is not None:
+            post.record()
     return g
+
+
+def graph_events():
+    """Two timing events that record inside a captured graph (event record
+    nodes), or None where this PyTorch has no such option."""
+    import torch
+    try:
+        return (torch.cuda.Event(enable_timing=True, external=True),
+                torch.cuda.Event(enable_timing=True, external=True))
+    except TypeError:
+        return None
+
+
+TIMING = {"in_graph": "CUDA events inside the captured graphs: start when an untimed call ahead of the "
+                      "timed ones completes, stop when the last timed call completes (steady-state periods)",
+          "delay": "CUDA events on the launching stream after a queued GPU delay"}
 
 
 def time_steps(fn, steps, warmup, chunk=1000, barrier=None):
     """Run exactly `warmup` untimed then `steps` timed invocations of fn(i)
-    as CUDA-graph replays; return elapsed ms of the timed region (CUDA events
-    on the launching stream, synchronised on both sides)."""
+    as CUDA-graph replays; return elapsed ms of the timed region (CUDA events,
+    synchronised on both sides).  Where PyTorch can record events inside a
+    captured graph, the first timed graph opens with one untimed call and the
+    start event records when it completes; the timed calls follow it as they
+    follow each other (the first may begin its prologue, e.g. its weight
+    loads, under that call, as every call does under its predecessor), and
+    the stop event records when the last timed call completes: the region is
+    `steps` steady-state periods, with no cold first call and no graph launch
+    latency in it.  Otherwise both events are recorded on the launching
+    stream around the replays."""
     import torch
     chunk = max(1, min(chunk, steps))
-    g_main = graph_of(fn, chunk)
-    rem = steps % chunk
-    g_rem = graph_of(fn, rem) if rem else None
+    sizes = [chunk] * (steps // chunk) + ([steps % chunk] if steps % chunk else [])
+    ev = graph_events()
+    if ev is not None:
+        e0, e1 = ev
+        if len(sizes) == 1:
+            graphs = [graph_of(fn, sizes[0], pre=e0, post=e1)]
+        else:
+            first = graph_of(fn, sizes[0], pre=e0)
+            mid = graph_of(fn, chunk) if len(sizes) > 2 else None
+            last = graph_of(fn, sizes[-1], post=e1)
+            graphs = [first] + [mid] * (len(sizes) - 2) + [last]
+    else:
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        g_main = graph_of(fn, chunk)
+        g_rem = graph_of(fn, sizes[-1]) if sizes[-1] != chunk else None
+        graphs = [g_main] * (steps // chunk) + ([g_rem] if g_rem is not None else [])
     wchunk = min(chunk, max(1, warmup))
     g_warm = graph_of(fn, wchunk)
     for _ in range(max(1, warmup // wchunk)):
@@ -183,23 +237,24 @@ def time_steps(fn, steps, warmup, chunk=1000, barrier=None):
         barrier()
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
     # A bounded GPU delay (a fixed number of clock cycles, ~1 ms) ahead of the
-    # start event: the host submits the graph replays while the GPU is still
-    # busy with it, so the timed region holds device work only and not the
-    # host's submission latency of the first replay.
+    # timed replays: the host submits them while the GPU is still busy with
+    # it, so no host submission latency falls between or before them.
     torch.cuda._sleep(GPU_DELAY_CYCLES)
-    e0.record(stream)
-    for _ in range(steps // chunk):
-        g_main.replay()
-    if g_rem is not None:
-        g_rem.replay()
-    e1.record(stream)
+    if ev is None:
+        e0.record(stream)
+    for g in graphs:
+        g.replay()
+    if ev is None:
+        e1.record(stream)
     torch.cuda.synchronize()
     if barrier:
         barrier()
     return e0.elapsed_time(e1)
+
+
+def timing_method():
+    return TIMING["in_graph" if graph_events() is not None else "delay"]
 
 
 def copies_for(nbytes, minimum=2, cap=96):
@@ -793,7 +848,7 @@ def main():
            "config": {"workload": d.name, "m": d.m, "n": d.n, "k": d.k, "bias": True,
                       "parallelism": "replicas" if ws > 1 else "single",
                       "l2": "inputs larger than L2: %d rotating copies (%.0f MB)" % (setup.R, setup.R * nbytes / 1e6),
-                      "timing": "CUDA-graph replays, CUDA events, GPU delay before the start event"},
+                      "timing": "CUDA-graph replays; " + timing_method()},
            "roofline": roof,
            "gpu_launches": launches_per_step * args.steps,
            "clocks": clk,

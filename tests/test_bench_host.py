@@ -56,3 +56,9 @@ def test_large_m_block_uses_the_fp8_peak():
 def test_host_description_names_cores_and_model():
     h = bench.host_description()
     assert h["host_cores"] == os.cpu_count() and isinstance(h["cpu_model"], str) and h["cpu_model"]
+
+
+def test_timing_method_is_named():
+    """The timed region's bounds: events inside the captured graphs where
+    this PyTorch records them there, else events around the replays."""
+    assert bench.timing_method() in bench.TIMING.values()
