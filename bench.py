@@ -959,16 +959,49 @@ def measure_e2e(mx, setup, steps):
             "note": "mxfp8_linear_host via ctypes, one stream per request in flight"}
 
 
+def code_sha(path):
+    """sha256 prefix (16 hex digits) of a C/CUDA source with its comments
+    removed, runs of blanks outside string and character literals collapsed
+    to one, lines stripped and empty lines dropped: a capture stays valid
+    across comment-only edits of the file and no longer across any edit of
+    its code."""
+    src = open(path, encoding="utf-8").read()
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        elif c in " \t":
+            if not out or out[-1] != " ":
+                out.append(" ")
+            i += 1
+        else:
+            out.append(c)
+            i += 1
+    body = "\n".join(ln.strip() for ln in "".join(out).splitlines() if ln.strip())
+    return hashlib.sha256(body.encode("utf-8")).hexdigest()[:16]
+
+
 def load_traffic(kernel, workload):
     """DRAM bytes per launch from the committed ncu summary, valid only while
-    the kernel source is unchanged since the capture."""
+    the kernel source's code (code_sha) is unchanged since the capture."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         table = json.load(open(path))
         ent = table[kernel][workload]
         src = os.path.join(ROOT, "mxfp8_block_scaled_x4_gb300", "csrc", ent.get("source", "gemm.cu"))
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        if ent.get("source_sha") != sha:
+        if ent.get("code_sha") != code_sha(src):
             return None
         return ent["dram_bytes_per_launch"]
     except Exception:  # noqa: BLE001

@@ -2,11 +2,13 @@
  * mxfp8_moe.h -- C ABI of the MXFP8 mixture-of-experts expert MLP on GB300.
  *
  * One MoE layer, as the FlashInfer pages describe it:
- *   FlashInfer PR #1214 "TRT-LLM Gen MoE" (Highlights): routing methods
- *   "Renormalize (TopK -> Softmax)" and "RenormalizeNaive (Softmax -> TopK ->
- *   Renormalize)"; "row reordering for gated activations" in the weight
- *   preparation.  The unified-MoE per-tensor FP8 PR (What changed): GEMM1
- *   (gate/linear) then GEMM2, with the gated-row reorder of GEMM1.
+ *   FlashInfer PR #1214 "TRT-LLM Gen MoE" (Highlights): two routing methods,
+ *   Renormalize (top-k of the logits, then a softmax over those k) and
+ *   RenormalizeNaive (a softmax over all experts, the top-k, then the k picks
+ *   rescaled to sum to 1); the GEMM1 weight rows are reordered for the gated
+ *   activation during weight preparation.  The unified-MoE per-tensor FP8 PR
+ *   (What changed): GEMM1 (gate/linear) then GEMM2, with the gated-row
+ *   reorder of GEMM1.
  * The steps of mxfp8_moe_expert_mlp:
  *   1. route: per token the top-k experts and their weights, then the
  *      (token, slot) pairs sorted by expert, then token;
@@ -56,7 +58,12 @@ size_t mxfp8_moe_route_workspace_bytes(int64_t tokens, int64_t experts, int64_t 
  *   expert_offsets int32 [experts + 1]  exclusive prefix of per-expert counts
  *   sorted_token  int32 [tokens*topk]   token of each expert-sorted row
  *   row_of        int32 [tokens*topk]   expert-sorted row of pair (t, s) at t*topk + s
- * ws: >= mxfp8_moe_route_workspace_bytes. */
+ * ws: >= mxfp8_moe_route_workspace_bytes.  Up to 512 tokens one launch does
+ * everything (a cluster of 8 CTAs that exchange per-group expert counts
+ * through distributed shared memory; ws is then not touched); above, two
+ * launches (per-group selection, then one scan over the groups).  The
+ * kernel that writes the offsets never releases its programmatic
+ * dependents early. */
 mxfp8_status mxfp8_moe_route(const float* logits, int64_t tokens, int64_t experts, int64_t topk,
                              mxfp8_route_method method, int32_t* topk_ids, float* topk_weights,
                              int32_t* expert_offsets, int32_t* sorted_token, int32_t* row_of,
@@ -82,7 +89,9 @@ size_t mxfp8_moe_gate_up_workspace_bytes(int64_t rows, int64_t k);
  * sorted_token (int32 [rows]) and expert_offsets (int32 [E + 1]) are read
  * on the device and not checked: every sorted_token value must lie in
  * [0, tokens), and the offsets must follow mxfp8_grouped_linear's rules,
- * including its ordering rule (mxfp8_moe_route's outputs satisfy both).
+ * including its ordering rule (mxfp8_moe_route's outputs satisfy both; the
+ * gathering quantizer this call launches first waits for the kernel before
+ * it and only then lets GEMM1 start).
  * ws: >= mxfp8_moe_gate_up_workspace_bytes(rows, k), 16-B aligned. */
 mxfp8_status mxfp8_moe_gate_up_swiglu(const void* x, const int32_t* sorted_token, int64_t rows,
                                       const int32_t* expert_offsets, const mxfp8_weight* w13, void* h,
@@ -105,7 +114,12 @@ size_t mxfp8_moe_workspace_bytes(int64_t tokens, int64_t experts, int64_t topk, 
  * w13: GEMM1 weights (E experts, n = 2I, k = H) from
  * mxfp8_prepare_gate_up_weight; w2: GEMM2 weights (E experts, n = H, k = I)
  * from mxfp8_prepare_weight; out: bfloat16 [tokens][H].
- * Requires H % 256 == 0 and I % 256 == 0 (both are GEMM K dimensions). */
+ * Requires H % 256 == 0 and I % 256 == 0 (both are GEMM K dimensions).
+ * Launches, each with programmatic dependent launch: routing, the gathering
+ * quantizer (which the router releases early: it waits for the router before
+ * it lets GEMM1 start), GEMM1 with the SwiGLU epilogue writing h as MXFP8,
+ * GEMM2, finalize (which loads the router's row indices and weights before
+ * it waits for GEMM2). */
 mxfp8_status mxfp8_moe_expert_mlp(const void* x, const float* logits, int64_t tokens, int64_t topk,
                                   mxfp8_route_method method, const mxfp8_weight* w13,
                                   const mxfp8_weight* w2, void* out, void* ws, size_t ws_bytes,

@@ -9,8 +9,8 @@
 // tile) and the tokens its B operand (N = 16..256 tokens per tile): the
 // accumulator D^T[n, token] lives in TMEM with one weight row per lane.  This
 // is why N is padded to 128 and why the small-M case needs no padding of the
-// token count beyond 16 (FlashInfer PR #1214 names the same choice:
-// "shuffling for transposed MMA outputs").
+// token count beyond 16 (FlashInfer PR #1214, Highlights, makes the same
+// choice: its MMA outputs come out transposed and are shuffled back).
 //
 // mxfp8_gemm_kernel<TT, PIPES, MODE> (TT tokens per tile, PIPES MMA
 // pipelines per CTA, MODE plain / gated SwiGLU / 128x4 activation scales):

@@ -1,16 +1,23 @@
 // moe.cu -- routing and finalize kernels of the MXFP8 mixture-of-experts
 // expert MLP.
 //
-// Routing follows FlashInfer PR #1214 "TRT-LLM Gen MoE" (Highlights):
-// "Renormalize (TopK -> Softmax)" and "RenormalizeNaive (Softmax -> TopK ->
-// Renormalize)".  The experts of a token are chosen on the raw logits (the
-// softmax is strictly monotone, so this is the top-k of the probabilities in
-// exact arithmetic), in descending order, ties to the lower expert id.  The
-// (token, slot) pairs are then sorted by expert, then token -- stable and
-// deterministic, no atomics:
-//   route_topk_kernel   one CTA per 8-token group, one warp per token: k
-//                       rounds of warp arg-max over the logits, the weights,
-//                       then per-expert token masks -> group counts and each
+// Routing follows FlashInfer PR #1214 "TRT-LLM Gen MoE" (Highlights): the
+// Renormalize method (top-k of the logits, then a softmax over those k) and
+// RenormalizeNaive (a softmax over all experts, top-k, then the k picks
+// rescaled to sum to 1).  The experts of a token are chosen on the raw
+// logits (the softmax is strictly monotone, so this is the top-k of the
+// probabilities in exact arithmetic), in descending order, ties to the lower
+// expert id.  The (token, slot) pairs are then sorted by expert, then token
+// -- stable and deterministic, no order-dependent atomics:
+//   route_cluster_kernel  up to kClusterTokens tokens, one launch: a cluster
+//                       of 8 CTAs, one warp per token; per 32-token group a
+//                       mask of the group's tokens per expert; the groups'
+//                       counts exchanged through distributed shared memory
+//                       -> offsets, then row_of[t*k + s] and
+//                       sorted_token[row];
+//   route_topk_kernel   above that, one CTA per 8-token group, one warp per
+//                       token: the same selection and weights, then
+//                       per-expert token masks -> group counts and each
 //                       pair's rank inside its group;
 //   route_scan_assign_kernel  one CTA: per-expert totals -> offsets, per
 //                       (group, expert) the first sorted row of that group,

@@ -5,13 +5,14 @@ benchmark's CPU-baseline / reference leg may import this module.  It shares no
 code with the CUDA library and never imports it.
 
 What it follows, by page:
-  * FlashInfer PR #1214 "TRT-LLM Gen MoE" (summary, Highlights): routing
-    methods "Renormalize (TopK -> Softmax)" and "RenormalizeNaive (Softmax ->
-    TopK -> Renormalize)"; "row reordering for gated activations" in the
-    weight preparation.
+  * FlashInfer PR #1214 "TRT-LLM Gen MoE" (summary, Highlights): two routing
+    methods, Renormalize (top-k of the logits, then a softmax over those k)
+    and RenormalizeNaive (a softmax over all experts, the top-k, then the k
+    picks rescaled to sum to 1); the GEMM1 weight rows are reordered for the
+    gated activation during weight preparation.
   * FlashInfer unified-MoE PR for per-tensor FP8 (What changed): the layer is
-    GEMM1 (gate/linear) then GEMM2, with "TRTLLM gated-row reorder" of the
-    GEMM1 weights and the MXFP8 scales of the row-permuted GEMM1/GEMM2 weights
+    GEMM1 (gate/linear) then GEMM2, the GEMM1 weights carry the gated-row
+    reorder, and the MXFP8 scales of the row-permuted GEMM1/GEMM2 weights are
     in the 128x4 interleaved layout.
 Readings where the pages are silent (each listed in the design notes):
   * The gated activation is SwiGLU: h = silu(gate) * up with

@@ -62,3 +62,19 @@ def test_timing_method_is_named():
     """The timed region's bounds: events inside the captured graphs where
     this PyTorch records them there, else events around the replays."""
     assert bench.timing_method() in bench.TIMING.values()
+
+
+def test_code_sha_ignores_comments_only(tmp_path):
+    """Captured traffic stays valid across comment edits of the kernel
+    source, not across code edits (bench.code_sha)."""
+    a = tmp_path / "a.cu"
+    a.write_text('int f(int x) {  // twice\n  /* body */ return 2 * x; }\nconst char* s = "//x";\n')
+    b = tmp_path / "b.cu"
+    b.write_text('// header\nint f(int x) {  // doubled\n\n  return 2 * x; }\nconst char* s = "//x";\n')
+    c = tmp_path / "c.cu"
+    c.write_text('int f(int x) {  // twice\n  return 3 * x; }\nconst char* s = "//x";\n')
+    d = tmp_path / "d.cu"
+    d.write_text('int f(int x) {  // twice\n  return 2 * x; }\nconst char* s = "//y";\n')
+    assert bench.code_sha(str(a)) == bench.code_sha(str(b))
+    assert bench.code_sha(str(a)) != bench.code_sha(str(c))
+    assert bench.code_sha(str(a)) != bench.code_sha(str(d))
