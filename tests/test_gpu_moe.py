@@ -230,6 +230,29 @@ def test_moe_arguments_rejected(lib):
         lib.moe_route(lg, 17)                     # topk > 16
 
 
+def test_gate_up_every_row_many_experts(lib):
+    """GEMM1 + SwiGLU over 128 experts with several tiles per persistent CTA
+    (128 experts x 4 n-tiles, two K blocks per tile, so each of the two MMA
+    pipelines takes one): every row of h against the oracle, and the layer
+    against its stages bit for bit."""
+    t, e, k, h, inter = 256, 128, 8, 256, 256
+    mw = workloads.moe(seed=71, tokens=t, experts=e, topk=k, hidden=h, inter=inter)
+    r = lib.moe_route(to_dev_f32(mw.logits), k)
+    w13 = lib.prepare_gate_up_weight(to_dev_f32(mw.w13))
+    hv = lib.moe_gate_up_swiglu(to_dev_bf16(mw.x), r, w13)
+    torch.cuda.synchronize()
+    ids, _ = M.route(mw.logits, k)
+    rows = np.arange(t * k)
+    assert_close_to_oracle(hv, _oracle_gate_up(mw, ids, rows), mw.name + " h")
+    w2 = lib.prepare_weight(to_dev_f32(mw.w2))
+    x, lg = to_dev_bf16(mw.x), to_dev_f32(mw.logits)
+    out = lib.moe_expert_mlp(x, lg, k, w13, w2)
+    y2 = lib.grouped_linear(hv, r.offsets, w2)
+    chain = lib.moe_finalize(y2, r)
+    torch.cuda.synchronize()
+    assert torch.equal(out, chain)
+
+
 @pytest.mark.parametrize("shape", [(37, 8, 2, 256, 256), (100, 16, 4, 512, 512), (256, 128, 8, 2048, 768)])
 def test_expert_mlp_is_the_stage_chain_and_each_stage_is_strict(lib, shape):
     """The whole layer equals, bit for bit, its stages run one by one (inside
