@@ -1580,13 +1580,17 @@ GemmSchedule choose_schedule(const GemmProblem& p, int num_sms, int force_tt, in
     // schedules that still fit one CTA per SM.
     int pipes = 1;
     if (p.offsets != nullptr && tt <= 64) pipes = 2;
+    // Grouped 32-token tiles: four pipelines (measured on the 128-expert
+    // layer: MoE 130.7 -> 125.2 us, gate_up 71.4 -> 70.0 us against two).
+    if (p.offsets != nullptr && tt == 32) pipes = 4;
     if (p.offsets == nullptr && !persistent && tt <= 32) pipes = 2;
     if (p.offsets == nullptr && !persistent && tt == 64 &&
         (p.n_pad / 128) * ((p.m + tt - 1) / tt) * split <= num_sms)
         pipes = 2;
     if (const int fp = g_force_pipes.load(std::memory_order_relaxed)) pipes = fp;
     if (pipes == 2 && tt > 64) pipes = 1;
-    if (pipes == 4 && tt != 16) pipes = tt <= 64 ? 2 : 1;
+    if (pipes == 4 && tt != 16 && tt != 32) pipes = tt <= 64 ? 2 : 1;
+    if (pipes == 4 && tt == 16 && p.gated) pipes = 2;  // no four-pipe gated 16-token kernel
     sch.pipes = pipes;
     return sch;
 }
@@ -1612,6 +1616,8 @@ cudaError_t launch_gemm(const GemmProblem& p, const GemmSchedule& sch, int num_s
                 default: return cudaErrorInvalidValue;
             }
         }
+        if (sch.pipes == 4 && sch.tokens_per_tile == 32)
+            return launch_tt<32, 4, kModeGated>(p, sch, num_sms, s, encode_failed);
         if (sch.pipes != 1) return cudaErrorInvalidValue;
         switch (sch.tokens_per_tile) {
             case 16: return launch_tt<16, 1, kModeGated>(p, sch, num_sms, s, encode_failed);
@@ -1639,6 +1645,7 @@ cudaError_t launch_gemm(const GemmProblem& p, const GemmSchedule& sch, int num_s
     }
     if (sch.pipes == 4) {
         if (sch.tokens_per_tile == 16) return launch_tt<16, 4, kModePlain>(p, sch, num_sms, s, encode_failed);
+        if (sch.tokens_per_tile == 32) return launch_tt<32, 4, kModePlain>(p, sch, num_sms, s, encode_failed);
         return cudaErrorInvalidValue;
     }
     switch (sch.tokens_per_tile) {

@@ -51,7 +51,8 @@ bool schedule_valid(const GemmSchedule& s, int kind, int64_t k) {
                s.pipes == 2;
     if (tt != 16 && tt != 32 && tt != 64 && tt != 128 && tt != 256) return false;
     if (s.pipes == 2 && tt > 64) return false;
-    if (s.pipes == 4 && tt != 16) return false;
+    // Four pipelines: 16-token tiles (not gated) and 32-token tiles.
+    if (s.pipes == 4 && !((tt == 16 && kind != kTacticGated) || tt == 32)) return false;
     if (s.pipes != 1 && s.pipes != 2 && s.pipes != 4) return false;
     if (kind == kTacticGated && tt > 128) return false;
     if (s.persistent) {

@@ -184,7 +184,8 @@ def test_tactic_table_host_operations(mx):
         (mx.KIND_LINEAR, (48, -1, 0, 1)),    # no such tile
         (mx.KIND_LINEAR, (16, 9, 0, 1)),     # cluster of 9
         (mx.KIND_LINEAR, (128, -1, 0, 2)),   # two pipes need tiles <= 64
-        (mx.KIND_LINEAR, (32, 1, 0, 4)),     # four pipes only with 16-token tiles
+        (mx.KIND_LINEAR, (64, 1, 0, 4)),     # four pipes only with 16- or 32-token tiles
+        (mx.KIND_GATED, (16, -1, 0, 4)),     # no four-pipe gated kernel of 16-token tiles
         (mx.KIND_GEMM, (16, 4, 1, 2)),       # fused quantization needs x
         (mx.KIND_GROUPED, (32, 2, 0, 2)),    # grouped tiles are persistent
         (mx.KIND_GROUPED, (192, -1, 0, 2)),  # two weight tiles: dense only
@@ -225,9 +226,9 @@ def test_heuristic_schedules_on_the_workloads(mx):
         ((L, 4096, 8192, 8192, 1), (192, -1, 0, 2)),
         # large M but too few tiles for the dual kernel: persistent 256
         ((L, 1024, 256, 1024, 1), (256, -1, 0, 1)),
-        # grouped: mean segment 16 rows -> 32-token tiles, two pipes
-        ((GR, 2048, 1536, 2048, 128), (32, -1, 0, 2)),
-        ((GA, 2048, 1536, 2048, 128), (32, -1, 0, 2)),
+        # grouped: mean segment 16 rows -> 32-token tiles, four pipes
+        ((GR, 2048, 1536, 2048, 128), (32, -1, 0, 4)),
+        ((GA, 2048, 1536, 2048, 128), (32, -1, 0, 4)),
         # gated with long segments: capped at 128 tokens
         ((GA, 12800, 1536, 2048, 128), (128, -1, 0, 1)),
     ]

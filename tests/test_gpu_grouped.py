@@ -61,7 +61,7 @@ def test_grouped_edge_segments(lib, tt):
     _run_grouped(lib, g, schedule=(tt, 0, -1))
 
 
-@pytest.mark.parametrize("tt,pipes", [(16, 2), (16, 4), (32, 2), (64, 2)])
+@pytest.mark.parametrize("tt,pipes", [(16, 2), (16, 4), (32, 2), (32, 4), (64, 2)])
 def test_grouped_multi_pipe(lib, tt, pipes):
     g = workloads.grouped_from_counts([5, 0, 300, 1, 0, 17, 40, 0], n=260, k=512, seed=53, bias=True)
     _run_grouped(lib, g, schedule=(tt, 0, -1), pipes=pipes)
