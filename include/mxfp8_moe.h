@@ -59,7 +59,8 @@ size_t mxfp8_moe_route_workspace_bytes(int64_t tokens, int64_t experts, int64_t 
  *   sorted_token  int32 [tokens*topk]   token of each expert-sorted row
  *   row_of        int32 [tokens*topk]   expert-sorted row of pair (t, s) at t*topk + s
  * ws: >= mxfp8_moe_route_workspace_bytes.  Up to 512 tokens one launch does
- * everything (a cluster of 8 CTAs that exchange per-group expert counts
+ * everything (one cluster of 16 CTAs where the GPU schedules it and
+ * experts <= 512, else of 8 CTAs, that exchange per-group expert counts
  * through distributed shared memory; ws is then not touched); above, two
  * launches (per-group selection, then one scan over the groups).  The
  * kernel that writes the offsets never releases its programmatic

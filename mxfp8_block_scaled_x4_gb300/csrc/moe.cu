@@ -29,6 +29,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "internal.h"
 #include "debug_check.cuh"
 #include "ptx.cuh"
@@ -313,9 +315,10 @@ __global__ void __launch_bounds__(1024)
     }
 }
 
-// Routing in one launch for up to kClusterTokens tokens: one cluster of
-// kClusterCtas CTAs of 32 warps.  Tokens form 32-token groups; group g is
-// routed by CTA g % kClusterCtas in pass g / kClusterCtas, one warp per
+// Routing in one launch for up to kClusterTokens tokens: one cluster of CTAS
+// CTAs of WARPS warps (16 x 16 where the GPU schedules a 16-CTA cluster and
+// experts <= 512: fewer tokens per SM; else 8 x 32).  Tokens form WARPS-token
+// groups; group g is routed by CTA g % CTAS in pass g / CTAS, one warp per
 // token.  Each CTA records, per pass and expert, the mask of the group's
 // tokens that picked the expert.  After a cluster barrier every CTA reads
 // all groups' counts (mask popcounts) from its peers' shared memory in group
@@ -328,29 +331,29 @@ __global__ void __launch_bounds__(1024)
 // dependent early only when told (`release`): inside the MoE layer, whose
 // next kernel is the gathering quantizer that waits for this grid before it
 // releases the grouped GEMM (which reads the offsets in its prologue).
-constexpr int kClusterCtas = 8;
 constexpr int kClusterMaxPasses = 2;
-constexpr int kClusterTokens = kClusterCtas * 32 * kClusterMaxPasses;
-__global__ void __launch_bounds__(1024, 1)
+constexpr int kClusterTokens = 512;  // CTAS * WARPS * kClusterMaxPasses for both shapes below
+template <int CTAS, int WARPS>
+__global__ void __launch_bounds__(32 * WARPS, 1)
     route_cluster_kernel(const float* __restrict__ logits, int tokens, int experts, int topk, int method,
                          int32_t* __restrict__ ids, float* __restrict__ weights, int32_t* __restrict__ offsets,
                          int32_t* __restrict__ row_of, int32_t* __restrict__ sorted_token, int release) {
     extern __shared__ uint32_t route_smem[];  // masks [passes][experts], then bases [passes][experts]
     if (release) pdl_launch_dependents();
-    __shared__ int sel[kClusterMaxPasses][32][kMaxTopK];
+    __shared__ int sel[kClusterMaxPasses][WARPS][kMaxTopK];
     __shared__ int warp_sum[32];
     const int lane = threadIdx.x & 31;
     const int w = threadIdx.x >> 5;
     const int crank = static_cast<int>(cluster_rank());
-    const int groups = (tokens + 31) / 32;
-    const int passes = (groups + kClusterCtas - 1) / kClusterCtas;
+    const int groups = (tokens + WARPS - 1) / WARPS;
+    const int passes = (groups + CTAS - 1) / CTAS;
     uint32_t* masks = route_smem;
     int* base = reinterpret_cast<int*>(route_smem + passes * experts);
     for (int i = threadIdx.x; i < passes * experts; i += blockDim.x) masks[i] = 0u;
     pdl_wait();  // the logits come from the previous kernel
     const int64_t pairs = static_cast<int64_t>(tokens) * topk;
     for (int j = 0; j < passes; ++j) {
-        const int t = (j * kClusterCtas + crank) * 32 + w;
+        const int t = (j * CTAS + crank) * WARPS + w;
         if (t < tokens) {
             const float* lg = logits + static_cast<size_t>(t) * experts;
             TokenLogits tl;
@@ -360,10 +363,10 @@ __global__ void __launch_bounds__(1024, 1)
         }
     }
     __syncthreads();
-    const int local_pairs = passes * 32 * topk;
+    const int local_pairs = passes * WARPS * topk;
     for (int i = threadIdx.x; i < local_pairs; i += blockDim.x) {
-        const int j = i / (32 * topk), tw = (i / topk) % 32;
-        if ((j * kClusterCtas + crank) * 32 + tw < tokens) atomicOr(&masks[j * experts + sel[j][tw][i % topk]], 1u << tw);
+        const int j = i / (WARPS * topk), tw = (i / topk) % WARPS;
+        if ((j * CTAS + crank) * WARPS + tw < tokens) atomicOr(&masks[j * experts + sel[j][tw][i % topk]], 1u << tw);
     }
     cluster_arrive_release();  // every CTA's masks are complete ...
     cluster_wait_acquire();    // ... before any peer reads them
@@ -375,12 +378,12 @@ __global__ void __launch_bounds__(1024, 1)
     if (e < experts) {
 #pragma unroll 4
         for (int g = 0; g < groups; ++g) {
-            const uint32_t a = map_to_rank(smem_addr(&masks[(g / kClusterCtas) * experts + e]),
-                                           static_cast<uint32_t>(g % kClusterCtas));
+            const uint32_t a = map_to_rank(smem_addr(&masks[(g / CTAS) * experts + e]),
+                                           static_cast<uint32_t>(g % CTAS));
             const int c = __popc(ld_shared_cluster_u32(a));
 #pragma unroll
             for (int j = 0; j < kClusterMaxPasses; ++j)
-                if (g < j * kClusterCtas + crank) before[j] += c;
+                if (g < j * CTAS + crank) before[j] += c;
             total += c;
         }
     }
@@ -395,8 +398,8 @@ __global__ void __launch_bounds__(1024, 1)
     }
     __syncthreads();
     for (int i = threadIdx.x; i < local_pairs; i += blockDim.x) {
-        const int j = i / (32 * topk), tw = (i / topk) % 32, sl = i % topk;
-        const int t = (j * kClusterCtas + crank) * 32 + tw;
+        const int j = i / (WARPS * topk), tw = (i / topk) % WARPS, sl = i % topk;
+        const int t = (j * CTAS + crank) * WARPS + tw;
         if (t >= tokens) continue;
         const int ex = sel[j][tw][sl];
         const int r = base[j * experts + ex] + __popc(masks[j * experts + ex] & ((1u << tw) - 1u));
@@ -481,6 +484,39 @@ __global__ void __launch_bounds__(kFinThreads)
 
 cudaError_t read_and_clear_oob_moe(unsigned int* out) { return read_and_clear_oob_word(out); }
 
+namespace {
+// Whether this GPU schedules the routing kernel as one 16-CTA cluster (a
+// size beyond the portable 8, allowed per kernel); asked once per device.
+bool cluster16_schedulable() {
+    static std::atomic<int> cached[64];  // 0 unknown, 1 yes, -1 no
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    const int known = cached[dev].load(std::memory_order_relaxed);
+    if (known != 0) return known > 0;
+    bool ok = cudaFuncSetAttribute(route_cluster_kernel<16, 16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+              cudaSuccess;
+    if (ok) {
+        cudaLaunchConfig_t cfg;
+        memset(&cfg, 0, sizeof(cfg));
+        cfg.gridDim = dim3(16, 1, 1);
+        cfg.blockDim = dim3(512, 1, 1);
+        cfg.dynamicSmemBytes = 2 * 512 * 2 * sizeof(uint32_t);
+        cudaLaunchAttribute a;
+        a.id = cudaLaunchAttributeClusterDimension;
+        a.val.clusterDim.x = 16;
+        a.val.clusterDim.y = 1;
+        a.val.clusterDim.z = 1;
+        cfg.attrs = &a;
+        cfg.numAttrs = 1;
+        int n = 0;
+        ok = cudaOccupancyMaxActiveClusters(&n, route_cluster_kernel<16, 16>, &cfg) == cudaSuccess && n >= 1;
+    }
+    if (!ok) (void)cudaGetLastError();  // the probe's own failure, not a caller's error
+    cached[dev].store(ok ? 1 : -1, std::memory_order_relaxed);
+    return ok;
+}
+}  // namespace
+
 // The routing kernels are launched with programmatic stream serialization so
 // that their launches overlap the kernel before them (each waits for it
 // before reading its inputs).  Up to kClusterTokens tokens one cluster kernel
@@ -505,20 +541,27 @@ cudaError_t launch_moe_route(const float* logits, int64_t tokens, int64_t expert
     const int T = static_cast<int>(tokens), E = static_cast<int>(experts), K = static_cast<int>(topk);
     if (tokens <= kClusterTokens) {
         // One launch: a single cluster routes every token and sorts the pairs.
-        cudaLaunchAttribute attrs[2];
-        attrs[0] = attr;
-        attrs[1].id = cudaLaunchAttributeClusterDimension;
-        attrs[1].val.clusterDim.x = kClusterCtas;
-        attrs[1].val.clusterDim.y = 1;
-        attrs[1].val.clusterDim.z = 1;
-        cfg.attrs = attrs;
-        cfg.numAttrs = 2;
-        cfg.gridDim = dim3(kClusterCtas, 1, 1);
-        cfg.blockDim = dim3(1024, 1, 1);
-        const int passes = (T + 32 * kClusterCtas - 1) / (32 * kClusterCtas);
-        cfg.dynamicSmemBytes = static_cast<size_t>(passes) * E * 2 * sizeof(uint32_t);
-        return cudaLaunchKernelEx(&cfg, route_cluster_kernel, logits, T, E, K, method, ids, weights, offsets, row_of,
-                                  sorted_token, release ? 1 : 0);
+        const bool wide = E <= 512 && cluster16_schedulable();
+        if (wide || E <= 1024) {
+            const int ctas = wide ? 16 : 8, warps = wide ? 16 : 32;
+            cudaLaunchAttribute attrs[2];
+            attrs[0] = attr;
+            attrs[1].id = cudaLaunchAttributeClusterDimension;
+            attrs[1].val.clusterDim.x = ctas;
+            attrs[1].val.clusterDim.y = 1;
+            attrs[1].val.clusterDim.z = 1;
+            cfg.attrs = attrs;
+            cfg.numAttrs = 2;
+            cfg.gridDim = dim3(ctas, 1, 1);
+            cfg.blockDim = dim3(32 * warps, 1, 1);
+            const int passes = (T + warps * ctas - 1) / (warps * ctas);
+            cfg.dynamicSmemBytes = static_cast<size_t>(passes) * E * 2 * sizeof(uint32_t);
+            if (wide)
+                return cudaLaunchKernelEx(&cfg, route_cluster_kernel<16, 16>, logits, T, E, K, method, ids, weights,
+                                          offsets, row_of, sorted_token, release ? 1 : 0);
+            return cudaLaunchKernelEx(&cfg, route_cluster_kernel<8, 32>, logits, T, E, K, method, ids, weights,
+                                      offsets, row_of, sorted_token, release ? 1 : 0);
+        }
     }
     const int groups = static_cast<int>((tokens + kGroup - 1) / kGroup);
     int32_t* grp = ws;
