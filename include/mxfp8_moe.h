@@ -12,9 +12,11 @@
  * The steps of mxfp8_moe_expert_mlp:
  *   1. route: per token the top-k experts and their weights, then the
  *      (token, slot) pairs sorted by expert, then token;
- *   2. gate_up: gather the token rows into expert-sorted order, quantize
- *      them (MXFP8, 8x4 scales), grouped GEMM1 against the gated weights and
- *      the SwiGLU epilogue h = silu(gate) * up, rounded to BF16 [rows][I];
+ *   2. gate_up: the token rows in expert-sorted order, quantized (MXFP8,
+ *      8x4 scales; inside mxfp8_moe_expert_mlp each token is quantized once
+ *      and written to its top-k rows, the gate_up call gathers rows through
+ *      sorted_token: the same bytes), grouped GEMM1 against the gated weights
+ *      and the SwiGLU epilogue h = silu(gate) * up, rounded to BF16 [rows][I];
  *   3. down: grouped GEMM2 of h into BF16 [rows][H].  Inside
  *      mxfp8_moe_expert_mlp, GEMM1's epilogue quantizes the BF16 h straight
  *      to MXFP8 (8x4 scales) for GEMM2; run as separate calls,
@@ -116,11 +118,13 @@ size_t mxfp8_moe_workspace_bytes(int64_t tokens, int64_t experts, int64_t topk, 
  * mxfp8_prepare_gate_up_weight; w2: GEMM2 weights (E experts, n = H, k = I)
  * from mxfp8_prepare_weight; out: bfloat16 [tokens][H].
  * Requires H % 256 == 0 and I % 256 == 0 (both are GEMM K dimensions).
- * Launches, each with programmatic dependent launch: routing, the gathering
- * quantizer (which the router releases early: it waits for the router before
- * it lets GEMM1 start), GEMM1 with the SwiGLU epilogue writing h as MXFP8,
- * GEMM2, finalize (which loads the router's row indices and weights before
- * it waits for GEMM2). */
+ * Launches, each with programmatic dependent launch: routing, the
+ * scattering quantizer (released by the router once the router's own wait
+ * has returned, so x is complete: it quantizes x while the router runs, then
+ * waits for it, writes the rows through the router's row indices and lets
+ * GEMM1 start), GEMM1 with the SwiGLU epilogue writing h as MXFP8, GEMM2,
+ * finalize (which loads the router's row indices and weights before it waits
+ * for GEMM2). */
 mxfp8_status mxfp8_moe_expert_mlp(const void* x, const float* logits, int64_t tokens, int64_t topk,
                                   mxfp8_route_method method, const mxfp8_weight* w13,
                                   const mxfp8_weight* w2, void* out, void* ws, size_t ws_bytes,

@@ -523,8 +523,9 @@ static mxfp8_status check_route_shape(int64_t tokens, int64_t experts, int64_t t
     return MXFP8_OK;
 }
 
-// release: the routing kernel may release the next kernel early (only the
-// MoE layer, whose next kernel is the gathering quantizer).
+// release: the routing kernel may release the next kernel once its own
+// dependency wait has returned (only the MoE layer, whose next kernel is the
+// scattering quantizer).
 static mxfp8_status route_checked(const float* logits, int64_t tokens, int64_t experts, int64_t topk,
                                   mxfp8_route_method method, int32_t* topk_ids, float* topk_weights,
                                   int32_t* expert_offsets, int32_t* sorted_token, int32_t* row_of, void* ws,
@@ -578,15 +579,18 @@ mxfp8_status mxfp8_prepare_gate_up_weight(const void* src, mxfp8_in_dtype dtype,
 
 size_t mxfp8_moe_gate_up_workspace_bytes(int64_t rows, int64_t k) { return mxfp8_linear_workspace_bytes(rows, k); }
 
-// Gather-quantize the expert-sorted rows of x, then GEMM1 with the SwiGLU
-// epilogue: h as BF16 into h, or (hq != null) quantized to MXFP8 into hq and
-// its 8x4 scales into hsf.  Arguments checked by the callers.
-static mxfp8_status gate_up_launch(const void* x, const int32_t* sorted_token, int64_t rows,
-                                   const int32_t* expert_offsets, const mxfp8_weight* w13, void* h, uint8_t* hq,
-                                   uint8_t* hsf, void* ws, int sms, cudaStream_t s) {
+// The expert-sorted rows of x quantized into ws (the layer's tokens scattered
+// through row_of, or the gate_up call's rows gathered through sorted_token),
+// then GEMM1 with the SwiGLU epilogue: h as BF16 into h, or (hq != null)
+// quantized to MXFP8 into hq and its 8x4 scales into hsf.  Arguments checked
+// by the callers.
+static mxfp8_status gate_up_launch(const void* x, const int32_t* sorted_token, const int32_t* row_of, int64_t tokens,
+                                   int64_t topk, int64_t rows, const int32_t* expert_offsets, const mxfp8_weight* w13,
+                                   void* h, uint8_t* hq, uint8_t* hsf, void* ws, int sms, cudaStream_t s) {
     uint8_t* qa = static_cast<uint8_t*>(ws);
     uint8_t* sfa = qa + ceil_to(rows * w13->k, 256);
-    cudaError_t e = mxk::launch_quant_act(x, rows, w13->k, qa, sfa, sms, s, sorted_token);
+    cudaError_t e = row_of ? mxk::launch_moe_scatter_quant(x, tokens, topk, w13->k, row_of, qa, sfa, sms, s)
+                           : mxk::launch_quant_act(x, rows, w13->k, qa, sfa, sms, s, sorted_token);
     if (e != cudaSuccess) return cuda_fail(e);
     mxk::GemmProblem p = make_problem(qa, sfa, rows, w13, nullptr, h, expert_offsets, nullptr);
     p.gated = true;
@@ -612,7 +616,7 @@ mxfp8_status mxfp8_moe_gate_up_swiglu(const void* x, const int32_t* sorted_token
     if (ws_bytes < mxfp8_moe_gate_up_workspace_bytes(rows, w13->k)) return MXFP8_ERR_WORKSPACE_TOO_SMALL;
     int sms = 0;
     if ((st = device_sms(&sms)) != MXFP8_OK) return st;
-    return gate_up_launch(x, sorted_token, rows, expert_offsets, w13, h, nullptr, nullptr, ws, sms,
+    return gate_up_launch(x, sorted_token, nullptr, 0, 0, rows, expert_offsets, w13, h, nullptr, nullptr, ws, sms,
                           static_cast<cudaStream_t>(stream));
 }
 
@@ -713,13 +717,15 @@ mxfp8_status mxfp8_moe_expert_mlp(const void* x, const float* logits, int64_t to
         cudaError_t e = cudaMemsetAsync(hsf + (r / 8) * grp, 0, static_cast<size_t>(grp), s);
         if (e != cudaSuccess) return cuda_fail(e);
     }
-    // The router may release the gathering quantizer early: that kernel waits
-    // for the router before it releases GEMM1, which reads the offsets in its
+    // The router releases the scattering quantizer once its own dependency
+    // wait has returned (x is then complete): the quantizer loads and
+    // quantizes x while the router runs, waits for it, scatters the rows
+    // through row_of and releases GEMM1, which reads the offsets in its
     // prologue.
     st = route_checked(logits, tokens, experts, topk, method, ids, wts, off, stok, row_of, b + l.route,
                        mxfp8_moe_route_workspace_bytes(tokens, experts, topk), stream, true);
     if (st != MXFP8_OK) return st;
-    st = gate_up_launch(x, stok, r, off, w13, nullptr, hq, hsf, b + l.g1, sms, s);
+    st = gate_up_launch(x, nullptr, row_of, tokens, topk, r, off, w13, nullptr, hq, hsf, b + l.g1, sms, s);
     if (st != MXFP8_OK) return st;
     mxk::GemmProblem p2 = make_problem(hq, hsf, r, w2, nullptr, b + l.y2, off, nullptr);
     const mxk::GemmSchedule sch2 = select_schedule(p2, sms, mxk::kTacticGrouped);

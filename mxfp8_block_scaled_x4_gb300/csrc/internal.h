@@ -29,6 +29,13 @@ cudaError_t launch_prepare_weight(const void* src, bool src_is_bf16, int64_t exp
 cudaError_t launch_moe_route(const float* logits, int64_t tokens, int64_t experts, int64_t topk, int method,
                              int32_t* ids, float* weights, int32_t* offsets, int32_t* sorted_token,
                              int32_t* row_of, int32_t* ws, cudaStream_t s, bool release = false);
+// MoE GEMM1's activations by token: x (BF16 [tokens][k], k a multiple of 128)
+// quantized once per token and written to rows row_of[t * topk + s] of qa
+// (E4M3 [tokens*topk][k]) with 8x4 scales in sfa (pad rows' scales zero).
+// Reads x before its dependency wait: the kernel ahead must release it only
+// once x is complete.
+cudaError_t launch_moe_scatter_quant(const void* x, int64_t tokens, int64_t topk, int64_t k, const int32_t* row_of,
+                                     uint8_t* qa, uint8_t* sfa, int num_sms, cudaStream_t s);
 // out[t] = bf16(sum_s weights[t, s] * y2[row_of[t * topk + s]]), FP32 sum in slot order.
 // slots_ready: row_of and weights were complete before the kernel this one
 // depends on began (they may then be read before the dependency wait).

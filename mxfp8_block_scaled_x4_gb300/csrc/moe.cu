@@ -22,8 +22,10 @@
 //   route_scan_assign_kernel  one CTA: per-expert totals -> offsets, per
 //                       (group, expert) the first sorted row of that group,
 //                       then row_of[t*k + s] and sorted_token[row].
-// Finalize sums each token's k expert outputs with its routing weights in
-// slot order (FP32) and rounds once to BF16.
+// Inside the layer, scatter_quant_kernel then quantizes each token's row of x
+// once and writes it to the token's k expert-sorted rows (GEMM1's
+// activations).  Finalize sums each token's k expert outputs with its
+// routing weights in slot order (FP32) and rounds once to BF16.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -34,6 +36,7 @@
 #include "internal.h"
 #include "debug_check.cuh"
 #include "ptx.cuh"
+#include "quant_block.cuh"
 
 namespace mxk {
 
@@ -272,10 +275,11 @@ __global__ void __launch_bounds__(1024)
     extern __shared__ int sgrp[];
     __shared__ int warp_sum[32];
     // Waits for route_topk_kernel.  Releases its dependent early only when
-    // told (inside the MoE layer: the gathering quantizer, which waits for
-    // this grid before releasing the grouped GEMM that reads the offsets).
-    if (release) pdl_launch_dependents();
+    // told, and only after that wait (inside the MoE layer: the scattering
+    // quantizer, which reads x before its own wait and waits for this grid
+    // before releasing the grouped GEMM that reads the offsets).
     pdl_wait();
+    if (release) pdl_launch_dependents();
     const int groups = (tokens + kGroup - 1) / kGroup;
     const int64_t cells = static_cast<int64_t>(groups) * experts;
     int32_t* cnt = grp;
@@ -328,9 +332,10 @@ __global__ void __launch_bounds__(1024)
 // groups + its rank among the group's tokens (a popcount of the mask below
 // it): the stable expert-sorted order.  A second barrier phase keeps every
 // CTA alive until no peer reads its masks any more.  The kernel releases its
-// dependent early only when told (`release`): inside the MoE layer, whose
-// next kernel is the gathering quantizer that waits for this grid before it
-// releases the grouped GEMM (which reads the offsets in its prologue).
+// dependent early only when told (`release`), and only after its own
+// dependency wait: inside the MoE layer, whose next kernel is the scattering
+// quantizer (it reads x before its wait, and waits for this grid before it
+// releases the grouped GEMM, which reads the offsets in its prologue).
 constexpr int kClusterMaxPasses = 2;
 constexpr int kClusterTokens = 512;  // CTAS * WARPS * kClusterMaxPasses for both shapes below
 template <int CTAS, int WARPS>
@@ -339,7 +344,6 @@ __global__ void __launch_bounds__(32 * WARPS, 1)
                          int32_t* __restrict__ ids, float* __restrict__ weights, int32_t* __restrict__ offsets,
                          int32_t* __restrict__ row_of, int32_t* __restrict__ sorted_token, int release) {
     extern __shared__ uint32_t route_smem[];  // masks [passes][experts], then bases [passes][experts]
-    if (release) pdl_launch_dependents();
     __shared__ int sel[kClusterMaxPasses][WARPS][kMaxTopK];
     __shared__ int warp_sum[32];
     const int lane = threadIdx.x & 31;
@@ -351,6 +355,7 @@ __global__ void __launch_bounds__(32 * WARPS, 1)
     int* base = reinterpret_cast<int*>(route_smem + passes * experts);
     for (int i = threadIdx.x; i < passes * experts; i += blockDim.x) masks[i] = 0u;
     pdl_wait();  // the logits come from the previous kernel
+    if (release) pdl_launch_dependents();
     const int64_t pairs = static_cast<int64_t>(tokens) * topk;
     for (int j = 0; j < passes; ++j) {
         const int t = (j * CTAS + crank) * WARPS + w;
@@ -408,6 +413,72 @@ __global__ void __launch_bounds__(32 * WARPS, 1)
         if (store_ok(r, 1, pairs)) sorted_token[r] = t;
     }
     cluster_wait();  // no peer reads this CTA's masks any more
+}
+
+// GEMM1's activation rows in the MoE layer, by token: lane (t, b) quantizes
+// 32-block b of token t's row of x once (the activation quantizer's
+// arithmetic: E4M3 bytes and one E8M0 scale per block) and writes it to the
+// token's topk expert-sorted rows row_of[t * topk + s] of qa, the scale
+// bytes in the 8x4 layout; block 0 then gives rows pairs .. ceil8(pairs)-1
+// of the last scale group zero scales, as the quantizer does.  Nothing before
+// the dependency wait depends on the routing: each lane's first block is
+// loaded and quantized while the router runs (x is complete by then: the
+// router releases this grid only after its own wait); row_of is read after
+// the wait.  The grouped GEMM is released after the wait too (it reads the
+// expert offsets in its prologue).  Thin CTAs (at most 64 registers a
+// thread) so that GEMM1's CTA fits beside one on an SM.
+constexpr int kScatThreads = 128;
+__global__ void __launch_bounds__(kScatThreads, 8)
+    scatter_quant_kernel(const __nv_bfloat16* __restrict__ x, int64_t tokens, int topk, int64_t k,
+                         const int32_t* __restrict__ row_of, uint8_t* __restrict__ qa, uint8_t* __restrict__ sfa) {
+    const int64_t kb = k >> 5;  // 32-blocks per row (a multiple of 4)
+    const int64_t total = tokens * kb;
+    const int64_t pairs = tokens * topk;
+    const int64_t rows8 = (pairs + 7) & ~static_cast<int64_t>(7);
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kScatThreads;
+    const int64_t first = static_cast<int64_t>(blockIdx.x) * kScatThreads + threadIdx.x;
+    // Task t * kb + b starts at x + (t * kb + b) * 32.
+    auto quantize = [&](int64_t task, uint32_t (&qq)[8]) {
+        const uint4* src = reinterpret_cast<const uint4*>(x + task * 32);
+        const uint4 raw[4] = {src[0], src[1], src[2], src[3]};
+        return quantize_block32(raw, qq);
+    };
+    auto scatter = [&](int64_t task, const uint32_t (&qq)[8], uint32_t sc) {
+        const int64_t t = task / kb, b = task - t * kb;
+        int rows[kMaxTopK];
+#pragma unroll
+        for (int sl = 0; sl < kMaxTopK; ++sl) rows[sl] = sl < topk ? row_of[t * topk + sl] : 0;
+#pragma unroll
+        for (int sl = 0; sl < kMaxTopK; ++sl) {
+            if (sl >= topk) break;
+            const int64_t r = rows[sl];
+            if (store_ok(r * k + b * 32, 32, pairs * k)) {
+                uint4* dst = reinterpret_cast<uint4*>(qa + r * k + b * 32);
+                dst[0] = make_uint4(qq[0], qq[1], qq[2], qq[3]);
+                dst[1] = make_uint4(qq[4], qq[5], qq[6], qq[7]);
+            }
+            const int64_t o = ((r >> 3) * (kb >> 2) + (b >> 2)) * 32 + (r & 7) * 4 + (b & 3);
+            if (store_ok(o, 1, rows8 * kb)) sfa[o] = static_cast<uint8_t>(sc);
+        }
+    };
+    uint32_t q0[8];
+    uint32_t s0 = 0;
+    if (first < total) s0 = quantize(first, q0);
+    pdl_wait();  // row_of comes from the router
+    pdl_launch_dependents();
+    if (first < total) scatter(first, q0, s0);
+    for (int64_t task = first + stride; task < total; task += stride) {
+        uint32_t qq[8];
+        const uint32_t sc = quantize(task, qq);
+        scatter(task, qq, sc);
+    }
+    if (blockIdx.x == 0) {
+        for (int64_t i = threadIdx.x; i < (rows8 - pairs) * kb; i += kScatThreads) {
+            const int64_t r = pairs + i / kb, b = i % kb;
+            const int64_t o = ((r >> 3) * (kb >> 2) + (b >> 2)) * 32 + (r & 7) * 4 + (b & 3);
+            if (store_ok(o, 1, rows8 * kb)) sfa[o] = 0;
+        }
+    }
 }
 
 // One warp per (token, 256-column chunk): lane c8 sums 8 columns over the
@@ -579,6 +650,38 @@ cudaError_t launch_moe_route(const float* logits, int64_t tokens, int64_t expert
     return cudaLaunchKernelEx(&cfg, route_scan_assign_kernel, T, E, K, static_cast<const int32_t*>(ids), grp,
                               static_cast<const int32_t*>(rank), offsets, row_of, sorted_token, use_smem,
                               release ? 1 : 0);
+}
+
+cudaError_t launch_moe_scatter_quant(const void* x, int64_t tokens, int64_t topk, int64_t k, const int32_t* row_of,
+                                     uint8_t* qa, uint8_t* sfa, int num_sms, cudaStream_t s) {
+    // An SM changes its L1 / shared-memory split only while idle: ask for the
+    // largest shared carveout (once per device) so that an SM running one of
+    // these CTAs can take a grouped GEMM CTA.
+    static std::atomic<int> carveout_set[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64 &&
+        carveout_set[dev].load(std::memory_order_relaxed) == 0) {
+        if (cudaFuncSetAttribute(scatter_quant_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+            (void)cudaGetLastError();  // a hint only
+        carveout_set[dev].store(1, std::memory_order_relaxed);
+    }
+    const int64_t total = tokens * (k / 32);
+    int64_t blocks = (total + kScatThreads - 1) / kScatThreads;
+    if (blocks > static_cast<int64_t>(num_sms) * 4) blocks = static_cast<int64_t>(num_sms) * 4;
+    if (blocks < 1) blocks = 1;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+    cfg.blockDim = dim3(kScatThreads, 1, 1);
+    cfg.stream = s;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, scatter_quant_kernel, static_cast<const __nv_bfloat16*>(x), tokens,
+                              static_cast<int>(topk), k, row_of, qa, sfa);
 }
 
 cudaError_t launch_moe_finalize(const void* y2, const int32_t* row_of, const float* weights, int64_t tokens,

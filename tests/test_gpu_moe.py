@@ -253,6 +253,56 @@ def test_gate_up_every_row_many_experts(lib):
     assert torch.equal(out, chain)
 
 
+def _layer_and_chain(lib, mw, k, w13, w2, ws=None):
+    x, lg = to_dev_bf16(mw.x), to_dev_f32(mw.logits)
+    out = lib.moe_expert_mlp(x, lg, k, w13, w2, workspace=ws)
+    r = lib.moe_route(lg, k)
+    hv = lib.moe_gate_up_swiglu(x, r, w13)
+    chain = lib.moe_finalize(lib.grouped_linear(hv, r.offsets, w2), r)
+    torch.cuda.synchronize()
+    return out, chain
+
+
+@pytest.mark.parametrize("shape", [(600, 16, 2, 256, 256),    # > 512 tokens: two routing kernels + gather
+                                   (40, 520, 4, 256, 256),    # > 512 experts: the 8-CTA cluster
+                                   (512, 64, 8, 256, 256),    # the one-launch limit: two passes per CTA
+                                   (3, 4, 1, 256, 256)])      # 3 rows: 5 pad rows in the scale group
+def test_expert_mlp_routing_paths_are_the_stage_chain(lib, shape):
+    """Each routing path of the layer (the one-launch cluster router, 16- or
+    8-CTA, up to 512 tokens; the two-kernel router above) gives the bytes of
+    the stages run one by one."""
+    t, e, k, h, inter = shape
+    mw = workloads.moe(seed=80 + t, tokens=t, experts=e, topk=k, hidden=h, inter=inter)
+    w13 = lib.prepare_gate_up_weight(to_dev_f32(mw.w13))
+    w2 = lib.prepare_weight(to_dev_f32(mw.w2))
+    out, chain = _layer_and_chain(lib, mw, k, w13, w2)
+    assert torch.equal(out.view(torch.int16), chain.view(torch.int16))
+
+
+def test_expert_mlp_back_to_back_on_one_workspace(lib):
+    """Consecutive layer calls on one workspace with different routings,
+    queued back to back (the kernels of neighbouring calls overlap through
+    programmatic dependent launch): each call's GEMMs take that call's
+    offsets and rows, never the previous call's (same total, different
+    segments)."""
+    t, e, k, h, inter = 128, 32, 4, 256, 256
+    base = workloads.moe(seed=90, tokens=t, experts=e, topk=k, hidden=h, inter=inter)
+    w13 = lib.prepare_gate_up_weight(to_dev_f32(base.w13))
+    w2 = lib.prepare_weight(to_dev_f32(base.w2))
+    ws = torch.empty(lib.moe_workspace_bytes(t, e, k, h, inter), dtype=torch.uint8, device="cuda")
+    x = to_dev_bf16(base.x)
+    rng = np.random.default_rng(91)
+    logits = [to_dev_f32(rng.standard_normal((t, e)).astype(np.float32) * (1 + i)) for i in range(4)]
+    outs = [lib.moe_expert_mlp(x, lg, k, w13, w2, workspace=ws) for lg in logits]  # queued back to back
+    torch.cuda.synchronize()
+    for lg, out in zip(logits, outs):
+        r = lib.moe_route(lg, k)
+        hv = lib.moe_gate_up_swiglu(x, r, w13)
+        chain = lib.moe_finalize(lib.grouped_linear(hv, r.offsets, w2), r)
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), chain.view(torch.int16))
+
+
 @pytest.mark.parametrize("shape", [(37, 8, 2, 256, 256), (100, 16, 4, 512, 512), (256, 128, 8, 2048, 768)])
 def test_expert_mlp_is_the_stage_chain_and_each_stage_is_strict(lib, shape):
     """The whole layer equals, bit for bit, its stages run one by one (inside
