@@ -89,3 +89,19 @@ def _check_guard_bytes():
     binding allocate are intact."""
     yield
     GUARDS.check()
+
+
+@pytest.fixture(autouse=True)
+def _check_device_error(request):
+    """After every test that used the CUDA library: no kernel of it gave up
+    a bounded wait (a timeout skips that CTA's remaining tiles, which shows
+    in a parity check only for the rows it happens to sample) and, in the
+    debug build, none computed an out-of-bounds store index.  Reads and
+    clears the device error words; tests that provoke a timeout read and
+    clear it themselves."""
+    yield
+    if "lib" not in request.fixturenames:
+        return
+    import mxfp8_block_scaled_x4_gb300 as mx
+    err = mx.device_error()
+    assert err == 0, "device error after the test: %s" % mx.status_string(err)
