@@ -381,15 +381,27 @@ __global__ void __launch_bounds__(32 * WARPS, 1)
 #pragma unroll
     for (int j = 0; j < kClusterMaxPasses; ++j) before[j] = 0;
     if (e < experts) {
-#pragma unroll 4
-        for (int g = 0; g < groups; ++g) {
-            const uint32_t a = map_to_rank(smem_addr(&masks[(g / CTAS) * experts + e]),
-                                           static_cast<uint32_t>(g % CTAS));
-            const int c = __popc(ld_shared_cluster_u32(a));
+        // All of a chunk's remote loads go out before any is used: one
+        // DSMEM round trip per chunk instead of one per few groups.
+        constexpr int kChunk = 16;
+        for (int g0 = 0; g0 < groups; g0 += kChunk) {
+            uint32_t mk[kChunk];
 #pragma unroll
-            for (int j = 0; j < kClusterMaxPasses; ++j)
-                if (g < j * CTAS + crank) before[j] += c;
-            total += c;
+            for (int k = 0; k < kChunk; ++k) {
+                const int g = g0 + k;
+                mk[k] = g < groups ? ld_shared_cluster_u32(map_to_rank(smem_addr(&masks[(g / CTAS) * experts + e]),
+                                                                       static_cast<uint32_t>(g % CTAS)))
+                                   : 0u;
+            }
+#pragma unroll
+            for (int k = 0; k < kChunk; ++k) {
+                const int g = g0 + k;
+                const int c = __popc(mk[k]);
+#pragma unroll
+                for (int j = 0; j < kClusterMaxPasses; ++j)
+                    if (g < j * CTAS + crank) before[j] += c;
+                total += c;
+            }
         }
     }
     cluster_arrive_relaxed();  // this thread's remote reads are done
