@@ -384,7 +384,7 @@ def measure_config(mx, name, d, peaks, calls=2000, tune=False):
     tactic = None
     if tune:
         mx.tactic_clear()
-        tactic = mx.autotune_linear(setup.xs[0], setup.pws[0], setup.bias, iters=50)
+        tactic = mx.autotune_linear(setup.xs[0], setup.pws[0], setup.bias, iters=200)
     warm = max(3, calls // 10)
     ms = time_steps(setup.linear, calls, warmup=warm) / calls
     ms_g = time_steps(setup.gemm, calls, warmup=warm) / calls

@@ -262,8 +262,13 @@ typedef enum mxfp8_call_kind {
 /* Times every valid tactic for this call (arguments as mxfp8_linear, `iters`
  * timed calls each, <= 0 means 20) on the caller's buffers, stores the
  * fastest in the table for the call's class and writes it to chosen[4] (may
- * be NULL).  SYNCHRONOUS: it waits for the stream; not allowed while the
- * stream is being captured (MXFP8_ERR_INVALID_ARG).  y is overwritten. */
+ * be NULL).  Each tactic is timed as one CUDA graph of `iters` calls back to
+ * back on a private stream that waits for the caller's (no host launch
+ * latency in the timing; best of three launches after a warm one); a weight smaller than twice the L2 is rotated
+ * over temporary copies (allocated for the call, at most ~2x L2 bytes, freed
+ * before it returns) so that every timed call streams its weight from HBM.
+ * SYNCHRONOUS: it waits for the stream; not allowed while the stream is
+ * being captured (MXFP8_ERR_INVALID_ARG).  y is overwritten. */
 mxfp8_status mxfp8_autotune_linear(const void* x, int64_t m, const mxfp8_weight* w,
                                    const void* bias, void* y, void* workspace,
                                    size_t workspace_bytes, int iters, void* stream,
