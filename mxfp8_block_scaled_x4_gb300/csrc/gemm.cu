@@ -1161,11 +1161,15 @@ __global__ void __launch_bounds__(kDualThreads, 1) mxfp8_gemm_dual_kernel(const 
         __syncwarp();
     } else {
         // ------------------------------------------------------- epilogue
-        // 32 token columns at a time: TMEM -> registers (+ bias, BF16) ->
-        // stores straight from registers: lane l holds output feature n0 + l,
-        // so each store instruction of the warp writes one token's 64-byte
-        // row segment.  (No shared staging: the 16 KB it would take buys a
-        // fourth pipeline stage for tiles of <= 160 tokens.)
+        // The warp's whole accumulator slice (its 32 output features x the
+        // tile's columns) is read from TMEM 32 columns at a time, biased and
+        // rounded to BF16 into registers (two columns per register), and only
+        // then is the accumulator released: the issuer's next tile waits for
+        // the TMEM reads alone, not for the stores.  Stores straight from
+        // registers: lane l holds output feature n0 + l, so each store
+        // instruction of the warp writes one token's 64-byte row segment.
+        // (No shared staging: the 16 KB it would take buys a fourth pipeline
+        // stage for tiles of <= 160 tokens.)
         const int ew = warp - 2;
         const int q = ew >> 2;   // accumulator / weight tile of the pair
         const int quad = warp & 3;
@@ -1180,40 +1184,43 @@ __global__ void __launch_bounds__(kDualThreads, 1) mxfp8_gemm_dual_kernel(const 
             if (!ok) { if (lane == 0) record_timeout(abort_flag); break; }
             tc_fence_after();
             const uint32_t taddr = tmem_base + q * TT + (static_cast<uint32_t>(quad * 32) << 16);
-#pragma unroll 1
-            for (int c0 = 0; c0 < TT; c0 += 32) {
-                // 32 columns at a time; a tile width that is an odd multiple
-                // of 16 ends with a 16-column load, so no load reaches past
-                // this accumulator's own columns.
-                uint32_t r[32];
-                if (TT % 32 == 0 || c0 + 32 <= TT) {
-                    tmem_load_32(taddr + c0, r);
-                } else {
-                    uint32_t r16[16];
-                    tmem_load_16(taddr + c0, r16);
+            uint32_t hv[TT / 2];  // BF16 pairs: columns 2i, 2i + 1 of the slice
+            // 16 columns per TMEM load (TT is a multiple of 16: no load
+            // reaches past this accumulator's own columns).
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) r[i] = r16[i];
-#pragma unroll
-                    for (int i = 16; i < 32; ++i) r[i] = 0u;
-                }
+            for (int h = 0; h < TT / 16; ++h) {
+                uint32_t r[16];
+                tmem_load_16(taddr + h * 16, r);
                 tmem_load_wait();
-                if (c0 + 32 >= TT) {  // accumulator fully read: the issuer may go on
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&acc_empty[q]);
-                }
-                if (n0 >= p.n || c0 >= ti.count) continue;  // warp-uniform
-                const int jmax = min(32, ti.count - c0);
-                if (n < p.n) {
-                    __nv_bfloat16* yp = p.y + static_cast<size_t>(ti.tok0 + c0) * p.n + n;
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        if (j < jmax && store_ok(static_cast<int64_t>(ti.tok0 + c0 + j) * p.n + n, 1,
-                                                 static_cast<int64_t>(p.m) * p.n))
-                            yp[static_cast<size_t>(j) * p.n] = __float2bfloat16_rn(__uint_as_float(r[j]) + b);
+                for (int i = 0; i < 16; i += 2) {
+                    const __nv_bfloat162 v2 = __floats2bfloat162_rn(__uint_as_float(r[i]) + b,
+                                                                    __uint_as_float(r[i + 1]) + b);
+                    hv[h * 8 + i / 2] = *reinterpret_cast<const uint32_t*>(&v2);
                 }
-                __syncwarp();
             }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[q]);  // accumulator read: the issuer may go on
+            if (n0 < p.n && n < p.n) {
+                // One pointer walks the tile's token rows.
+                __nv_bfloat16* yp = p.y + static_cast<size_t>(ti.tok0) * p.n + n;
+                const size_t row = static_cast<size_t>(p.n);
+                const int cnt = ti.count;
+#pragma unroll
+                for (int k = 0; k < TT / 2; ++k) {
+                    const uint32_t w2 = hv[k];
+                    if (2 * k < cnt && store_ok(static_cast<int64_t>(ti.tok0 + 2 * k) * p.n + n, 1,
+                                                static_cast<int64_t>(p.m) * p.n))
+                        *yp = __ushort_as_bfloat16(static_cast<unsigned short>(w2 & 0xFFFFu));
+                    yp += row;
+                    if (2 * k + 1 < cnt && store_ok(static_cast<int64_t>(ti.tok0 + 2 * k + 1) * p.n + n, 1,
+                                                    static_cast<int64_t>(p.m) * p.n))
+                        *yp = __ushort_as_bfloat16(static_cast<unsigned short>(w2 >> 16));
+                    yp += row;
+                }
+            }
+            __syncwarp();
         }
         __syncwarp();
     }
