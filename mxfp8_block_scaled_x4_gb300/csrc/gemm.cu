@@ -235,7 +235,14 @@ __device__ __forceinline__ int pipe_jobs(int q, int nk) {
 template <int TT, int PIPES, int MODE>
 __device__ __forceinline__ void run_producer(const GemmArgs& p, const Ctx& c, int q) {
     using G = Geometry<TT>;
-    const uint64_t pol_w = policy_evict_normal();
+    // Weights stream through once per call (a tile is read again only by the
+    // token tiles right after it): first in line for eviction, so that they
+    // do not push out of L2 what is read again -- the activations, which
+    // every weight tile of the call reads, and what the next kernel reads
+    // (GEMM1's h for GEMM2, GEMM2's output rows for the MoE finalize).
+    // Measured on one box: decode 5.26 -> 5.13 us, mid 9.60 -> 9.19 us, the
+    // MoE layer 125.0 -> 114.3 us, grouped gate_up 70.5 -> 66.0 us.
+    const uint64_t pol_w = policy_evict_first();
     const uint64_t pol_a = policy_evict_last();
     const int nk = c.kb_end - c.kb_begin;
     const int nq = pipe_jobs<PIPES>(q, nk);
