@@ -266,7 +266,9 @@ def _layer_and_chain(lib, mw, k, w13, w2, ws=None):
 @pytest.mark.parametrize("shape", [(600, 16, 2, 256, 256),    # > 512 tokens: two routing kernels + gather
                                    (40, 520, 4, 256, 256),    # > 512 experts: the 8-CTA cluster
                                    (512, 64, 8, 256, 256),    # the one-launch limit: two passes per CTA
-                                   (3, 4, 1, 256, 256)])      # 3 rows: 5 pad rows in the scale group
+                                   (3, 4, 1, 256, 256),       # 3 rows: 5 pad rows in the scale group
+                                   (40, 16, 16, 256, 256),    # top-16 (the limit): 16 copies of each row
+                                   (1, 64, 8, 2048, 256)])    # one token, K = 2048: 8 rows, one scale group
 def test_expert_mlp_routing_paths_are_the_stage_chain(lib, shape):
     """Each routing path of the layer (the one-launch cluster router, 16- or
     8-CTA, up to 512 tokens; the two-kernel router above) gives the bytes of
