@@ -928,7 +928,7 @@ __global__ void __launch_bounds__(32 * num_warps(TT, PIPES),
 //   warps 2..9   epilogue: warp 2+e serves accumulator e/4, lane quadrant
 //                warp%4, 32 token columns at a time, stored from registers
 //   warp 10      token-scale re-order into the TMEM-copy order
-template <int TT>
+template <int TT, bool SF128 = false>
 struct DualGeometry {
     static constexpr int kSfChunks = (TT + 127) / 128;
     static constexpr int kOffW0 = 0;
@@ -942,9 +942,13 @@ struct DualGeometry {
     // four 56 KB stages.
     static constexpr int kOffAsfT = kOffWsf1 + 512;
     static constexpr int kOffAsfRaw = kOffAsfT;
-    static constexpr int kStageBytes = ((kOffAsfT + 512 * kSfChunks) + 1023) / 1024 * 1024;
+    // With 128x4 token scales (SF128) the raw area holds the 512-byte scale
+    // tiles of every 128-row tile the token tile touches: up to three.
+    static constexpr int kRawTiles = SF128 ? (TT + 126) / 128 + 1 : 0;
+    static constexpr int kAreaBytes = SF128 && 512 * kRawTiles > 512 * kSfChunks ? 512 * kRawTiles : 512 * kSfChunks;
+    static constexpr int kStageBytes = ((kOffAsfT + kAreaBytes) + 1023) / 1024 * 1024;
     static constexpr int kSlotCols = 4 + 4 * kSfChunks;  // per pipe per stage
-    static_assert((TT / 8 + 1) * 32 <= 512 * kSfChunks, "raw scale groups must fit the shared area");
+    static_assert(SF128 || (TT / 8 + 1) * 32 <= 512 * kSfChunks, "raw scale groups must fit the shared area");
 };
 
 constexpr int kDualThreads = 12 * 32;
@@ -969,9 +973,18 @@ __device__ __forceinline__ TileInfo decode_dual(int t, const GemmArgs& p) {
     return ti;
 }
 
+// 128x4 scale tiles (of 128 rows) a token tile starting at tok0 touches,
+// counting none past the last row tile of an m-row buffer (ceil128(m) rows).
 template <int TT>
+__host__ __device__ __forceinline__ int dual_raw_tiles(int tok0, int m) {
+    const int last = (m + 127) / 128 - 1;
+    const int r1 = (tok0 + TT - 1) >> 7;
+    return (r1 < last ? r1 : last) - (tok0 >> 7) + 1;
+}
+
+template <int TT, bool SF128 = false>
 __global__ void __launch_bounds__(kDualThreads, 1) mxfp8_gemm_dual_kernel(const __grid_constant__ GemmArgs p) {
-    using G = DualGeometry<TT>;
+    using G = DualGeometry<TT, SF128>;
     extern __shared__ uint8_t smem_dyn[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -992,7 +1005,7 @@ __global__ void __launch_bounds__(kDualThreads, 1) mxfp8_gemm_dual_kernel(const 
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&p.map_w);
         tma_prefetch_desc(&p.map_a);
-        tma_prefetch_desc(&p.map_asf);
+        if constexpr (!SF128) tma_prefetch_desc(&p.map_asf);
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 2);   // producer (+ bytes), re-order warp
             mbar_init(&empty[s], 2);  // both MMA issuers
@@ -1038,8 +1051,19 @@ __global__ void __launch_bounds__(kDualThreads, 1) mxfp8_gemm_dual_kernel(const 
             auto issue_a = [&](const TileInfo& ti, int kb, int s) {
                 uint8_t* st = smem + s * G::kStageBytes;
                 tma_load_2d(st + G::kOffA, &p.map_a, kb * 128, ti.tok0, &full[s], pol_a);
-                mbar_arrive_expect_tx(&sfraw[s], static_cast<uint32_t>(p.sf_groups * 32));
-                tma_load_2d(st + G::kOffAsfRaw, &p.map_asf, kb * 32, ti.tok0 >> 3, &sfraw[s], pol_a);
+                if constexpr (SF128) {
+                    // The 128x4 scale tiles (row tile, K block) of the rows
+                    // the token tile touches, none past the buffer's last.
+                    const int r0 = ti.tok0 >> 7;
+                    const int nt = dual_raw_tiles<TT>(ti.tok0, p.m);
+                    mbar_arrive_expect_tx(&sfraw[s], static_cast<uint32_t>(nt * 512));
+                    for (int i = 0; i < nt; ++i)
+                        bulk_load(st + G::kOffAsfRaw + i * 512,
+                                  p.asf128 + (static_cast<size_t>(r0 + i) * p.kq + kb) * 512, 512, &sfraw[s], pol_a);
+                } else {
+                    mbar_arrive_expect_tx(&sfraw[s], static_cast<uint32_t>(p.sf_groups * 32));
+                    tma_load_2d(st + G::kOffAsfRaw, &p.map_asf, kb * 32, ti.tok0 >> 3, &sfraw[s], pol_a);
+                }
             };
             int pre = 0;
             for (int t = tile_first; t < num_tiles && pre < S; t += tile_stride) {
@@ -1135,6 +1159,8 @@ __global__ void __launch_bounds__(kDualThreads, 1) mxfp8_gemm_dual_kernel(const 
         for (int t = tile_first; t < num_tiles && !stop; t += tile_stride) {
             const TileInfo ti = decode_dual<TT>(t, p);
             const int off8 = ti.tok0 & 7;
+            const int r0 = ti.tok0 >> 7;
+            const int nt = SF128 ? dual_raw_tiles<TT>(ti.tok0, p.m) : 0;
             for (int kb = 0; kb < nk; ++kb, ++job) {
                 const int s = job % S;
                 bool ok = mbar_wait(&sfraw[s], (job / S) & 1, p.wait_ns);
@@ -1153,7 +1179,15 @@ __global__ void __launch_bounds__(kDualThreads, 1) mxfp8_gemm_dual_kernel(const 
 #pragma unroll
                     for (int jq = 0; jq < 4; ++jq) {
                         const int j = ch * 128 + jq * 32 + lane;
-                        w[ch][jq] = (j < TT) ? raw[off8 + j] : 0u;
+                        if constexpr (SF128) {
+                            // Row g's word (its four block scales) sits at
+                            // (g % 32) * 4 + (g % 128) / 32 of its row tile.
+                            const int g = ti.tok0 + j;
+                            const int rt = (g >> 7) - r0;
+                            w[ch][jq] = (j < TT && rt < nt) ? raw[rt * 128 + (g & 31) * 4 + ((g & 127) >> 5)] : 0u;
+                        } else {
+                            w[ch][jq] = (j < TT) ? raw[off8 + j] : 0u;
+                        }
                     }
                 __syncwarp();
 #pragma unroll
@@ -1438,10 +1472,10 @@ cudaError_t launch_tt(const GemmProblem& pr, const GemmSchedule& sch, int num_sm
     return cudaLaunchKernelEx(&cfg, mxfp8_gemm_kernel<TT, PIPES, MODE>, a);
 }
 
-template <int TT>
+template <int TT, bool SF128 = false>
 cudaError_t launch_dual(const GemmProblem& pr, int num_sms, cudaStream_t s, bool* encode_failed) {
-    using G = DualGeometry<TT>;
-    if (pr.sf128) return cudaErrorInvalidValue;  // 192-token tiles straddle 128x4 scale tiles
+    using G = DualGeometry<TT, SF128>;
+    if (pr.sf128 != SF128) return cudaErrorInvalidValue;
     GemmArgs a;
     memset(&a, 0, sizeof(a));
     const int64_t m8 = (pr.m + 7) / 8 * 8;
@@ -1449,7 +1483,8 @@ cudaError_t launch_dual(const GemmProblem& pr, int num_sms, cudaStream_t s, bool
     a.sf_groups = TT / 8 + 1;
     const bool ok = encode_2d_u8(&a.map_w, pr.wq, pr.k, pr.n_pad, pr.k, 128, 128, true) &&
                     encode_2d_u8(&a.map_a, pr.qa, pr.k, pr.m, pr.k, 128, TT, true) &&
-                    encode_2d_u8(&a.map_asf, pr.sfa, pr.k / 4, m8 / 8, pr.k / 4, 32, a.sf_groups, false);
+                    (SF128 || encode_2d_u8(&a.map_asf, pr.sfa, pr.k / 4, m8 / 8, pr.k / 4, 32, a.sf_groups, false));
+    a.asf128 = SF128 ? pr.sfa : nullptr;
     if (!ok) {
         *encode_failed = true;
         return cudaErrorInvalidValue;
@@ -1476,11 +1511,12 @@ cudaError_t launch_dual(const GemmProblem& pr, int num_sms, cudaStream_t s, bool
     const uint64_t wait_limit = g_wait_limit_ns.load(std::memory_order_relaxed);
     a.wait_ns = wait_limit ? wait_limit : kWaitNs;
     const size_t smem = 1024 + static_cast<size_t>(stages) * G::kStageBytes + ctrl;
-    cudaError_t err = cudaFuncSetAttribute(mxfp8_gemm_dual_kernel<TT>,
+    cudaError_t err = cudaFuncSetAttribute(mxfp8_gemm_dual_kernel<TT, SF128>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (err != cudaSuccess) return err;
     int per_sm = 1;
-    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mxfp8_gemm_dual_kernel<TT>, kDualThreads, smem);
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mxfp8_gemm_dual_kernel<TT, SF128>, kDualThreads,
+                                                        smem);
     if (err != cudaSuccess) return err;
     if (per_sm < 1 || static_cast<uint32_t>(per_sm) * a.tmem_cols > 512u) return cudaErrorInvalidConfiguration;
     const int tok_tiles = static_cast<int>((pr.m + TT - 1) / TT);
@@ -1502,7 +1538,7 @@ cudaError_t launch_dual(const GemmProblem& pr, int num_sms, cudaStream_t s, bool
     t_last_schedule[2] = 0;
     t_last_schedule[3] = grid;
     t_last_schedule[4] = stages;
-    return cudaLaunchKernelEx(&cfg, mxfp8_gemm_dual_kernel<TT>, a);
+    return cudaLaunchKernelEx(&cfg, mxfp8_gemm_dual_kernel<TT, SF128>, a);
 }
 
 }  // namespace
@@ -1612,6 +1648,12 @@ GemmSchedule choose_schedule(const GemmProblem& p, int num_sms, int force_tt, in
 cudaError_t launch_gemm(const GemmProblem& p, const GemmSchedule& sch, int num_sms, cudaStream_t s,
                         bool* encode_failed) {
     *encode_failed = false;
+    if (sch.dual && p.sf128) {
+        // 128x4 token scales (up to three raw scale tiles per stage, so three
+        // 57 KB stages): 176-token tiles only.
+        if (sch.tokens_per_tile != 176) return cudaErrorInvalidValue;
+        return launch_dual<176, true>(p, num_sms, s, encode_failed);
+    }
     if (sch.dual) {
         switch (sch.tokens_per_tile) {
             case 144: return launch_dual<144>(p, num_sms, s, encode_failed);

@@ -64,3 +64,32 @@ def test_linear_128x4_prefill_sampled_rows(lib):
     wq, wsf = oracle.quantize_rows(d.w)
     assert_close_to_oracle(y[torch.as_tensor(rows, device=y.device)], oracle.linear(d.x, wq, wsf, rows=rows),
                            "prefill 128x4")
+
+
+def test_linear_128x4_dual_tiles(lib):
+    """Large enough for the dual weight-tile kernel (two weight tiles x 176
+    tokens per CTA tile), with M = 1000: token tiles that straddle two or
+    three 128-row scale tiles and a last tile of 120 rows.  The result equals,
+    bit for bit, the 8x4 layer forced to the same schedule (the same E4M3
+    bytes and scale values, only the scale layout differs), and the oracle on
+    every tile and scale-tile boundary row."""
+    m, n, k = 1000, 8192, 256
+    d = workloads.dense(m, n, k, seed=77, bias=True)
+    pw = lib.prepare_weight(to_dev_f32(d.w))
+    x, b = to_dev_bf16(d.x), to_dev_bf16(d.bias)
+    y = lib.linear_128x4(x, pw, b)
+    torch.cuda.synchronize()
+    sched = lib.last_schedule()
+    assert sched["tokens_per_tile"] == 176 and sched["split"] == -2
+    lib.set_schedule(176, -1, 0)
+    try:
+        y8 = lib.linear(x, pw, b)
+    finally:
+        lib.set_schedule(0, 0, -1)
+    torch.cuda.synchronize()
+    assert torch.equal(y, y8)
+    rows = np.array([0, 1, 127, 128, 175, 176, 255, 256, 351, 352, 383, 384, 527, 528, 639, 640, 703, 704,
+                     767, 768, 879, 880, 895, 896, 999])
+    wq, wsf = oracle.quantize_rows(d.w)
+    assert_close_to_oracle(y[torch.as_tensor(rows, device=y.device)],
+                           oracle.linear(d.x, wq, wsf, d.bias, rows=rows), "linear_128x4 dual")
