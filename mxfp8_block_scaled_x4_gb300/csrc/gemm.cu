@@ -1005,7 +1005,7 @@ __global__ void __launch_bounds__(kDualThreads, 1) mxfp8_gemm_dual_kernel(const 
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&p.map_w);
         tma_prefetch_desc(&p.map_a);
-        if constexpr (!SF128) tma_prefetch_desc(&p.map_asf);
+        tma_prefetch_desc(&p.map_asf);
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 2);   // producer (+ bytes), re-order warp
             mbar_init(&empty[s], 2);  // both MMA issuers
@@ -1052,14 +1052,11 @@ __global__ void __launch_bounds__(kDualThreads, 1) mxfp8_gemm_dual_kernel(const 
                 uint8_t* st = smem + s * G::kStageBytes;
                 tma_load_2d(st + G::kOffA, &p.map_a, kb * 128, ti.tok0, &full[s], pol_a);
                 if constexpr (SF128) {
-                    // The 128x4 scale tiles (row tile, K block) of the rows
-                    // the token tile touches, none past the buffer's last.
-                    const int r0 = ti.tok0 >> 7;
-                    const int nt = dual_raw_tiles<TT>(ti.tok0, p.m);
-                    mbar_arrive_expect_tx(&sfraw[s], static_cast<uint32_t>(nt * 512));
-                    for (int i = 0; i < nt; ++i)
-                        bulk_load(st + G::kOffAsfRaw + i * 512,
-                                  p.asf128 + (static_cast<size_t>(r0 + i) * p.kq + kb) * 512, 512, &sfraw[s], pol_a);
+                    // One box: the 512-byte 128x4 scale tiles (K block kb)
+                    // of kRawTiles row tiles from the token tile's first;
+                    // rows past the buffer's last tile read as zero.
+                    mbar_arrive_expect_tx(&sfraw[s], static_cast<uint32_t>(G::kRawTiles * 512));
+                    tma_load_2d(st + G::kOffAsfRaw, &p.map_asf, kb * 128, ti.tok0 >> 7, &sfraw[s], pol_a);
                 } else {
                     mbar_arrive_expect_tx(&sfraw[s], static_cast<uint32_t>(p.sf_groups * 32));
                     tma_load_2d(st + G::kOffAsfRaw, &p.map_asf, kb * 32, ti.tok0 >> 3, &sfraw[s], pol_a);
@@ -1293,18 +1290,23 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-bool encode_2d_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
-                  uint64_t row_stride, uint32_t box_inner, uint32_t box_outer, bool swizzle128) {
+bool encode_2d(CUtensorMap* map, const void* base, CUtensorMapDataType type, uint64_t inner, uint64_t outer,
+               uint64_t row_stride, uint32_t box_inner, uint32_t box_outer, bool swizzle128) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {inner, outer};
     const cuuint64_t strides[1] = {row_stride};
     const cuuint32_t box[2] = {box_inner, box_outer};
     const cuuint32_t estr[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+    return fn(map, type, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
               swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_2d_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                  uint64_t row_stride, uint32_t box_inner, uint32_t box_outer, bool swizzle128) {
+    return encode_2d(map, base, CU_TENSOR_MAP_DATA_TYPE_UINT8, inner, outer, row_stride, box_inner, box_outer,
+                     swizzle128);
 }
 
 uint32_t pow2_cols(int need) {
@@ -1483,7 +1485,9 @@ cudaError_t launch_dual(const GemmProblem& pr, int num_sms, cudaStream_t s, bool
     a.sf_groups = TT / 8 + 1;
     const bool ok = encode_2d_u8(&a.map_w, pr.wq, pr.k, pr.n_pad, pr.k, 128, 128, true) &&
                     encode_2d_u8(&a.map_a, pr.qa, pr.k, pr.m, pr.k, 128, TT, true) &&
-                    (SF128 || encode_2d_u8(&a.map_asf, pr.sfa, pr.k / 4, m8 / 8, pr.k / 4, 32, a.sf_groups, false));
+                    (SF128 ? encode_2d(&a.map_asf, pr.sfa, CU_TENSOR_MAP_DATA_TYPE_UINT32, (pr.k / 128) * 128,
+                                       (pr.m + 127) / 128, (pr.k / 128) * 512, 128, G::kRawTiles, false)
+                           : encode_2d_u8(&a.map_asf, pr.sfa, pr.k / 4, m8 / 8, pr.k / 4, 32, a.sf_groups, false));
     a.asf128 = SF128 ? pr.sfa : nullptr;
     if (!ok) {
         *encode_failed = true;
