@@ -220,10 +220,13 @@ int mxfp8_static_scratch_last_cuda_error(void);
  * activation-scale path"): activation scales laid out like the prepared
  * weights' (tiles of 128 rows x 4 blocks, 512 bytes, tile (m/128, b/4) at
  * ((m/128)*(KB/4) + b/4)*512, row r = m%128 and block b at
- * (r%32)*16 + (r/32)*4 + (b%4); rows M..ceil128(M)-1 hold 0x00), so the GEMM
- * copies each tile into tensor memory as it is.  The GEMM then runs
- * persistent tiles of 256 tokens (128 when M <= 128) that start on 128-token
- * boundaries.  Same arithmetic and results as the 8x4 entry points. */
+ * (r%32)*16 + (r/32)*4 + (b%4); rows M..ceil128(M)-1 hold 0x00).  At large
+ * M (when CTA tiles of two 128-row weight tiles x 176 tokens give every SM a
+ * tile) the GEMM runs the dual weight-tile schedule of mxfp8_linear, taking
+ * per K block the scale tiles of the 128-row tiles each token tile touches;
+ * otherwise persistent tiles of 256 tokens (128 when M <= 128) that start on
+ * 128-token boundaries, each scale tile copied into tensor memory as it is.
+ * Same arithmetic and results as the 8x4 entry points. */
 size_t mxfp8_act_scale_bytes_128x4(int64_t m, int64_t k);          /* ceil(m/128)*128 * k/32 */
 size_t mxfp8_linear_128x4_workspace_bytes(int64_t m, int64_t k);
 mxfp8_status mxfp8_quantize_act_128x4(const void* x, int64_t m, int64_t k, void* q,
